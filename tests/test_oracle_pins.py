@@ -1,0 +1,383 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: values the
+pages print for a worked example (``tests/golden``), closed forms, invariants
+stated on the pages, finite differences of the forward, or a small
+independent brute force.  Chosen so that a dropped term, a wrong sign, a
+wrong mask direction, a transposed operand or a missing scale factor anywhere
+in the oracle fails at least one of them.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import (
+    attention_backward_head,
+    attention_forward_head,
+    attention_forward_rows,
+    causal_mask,
+    matmul_backward,
+    merge_outputs,
+    merge_stats,
+    naive_softmax,
+    online_softmax_steps,
+    softmax_3pass,
+    softmax_backward,
+    tiled_forward_head,
+)
+
+
+def _load(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ---------------------------------------------------------------- online softmax
+
+
+def test_worked_example_online_steps(golden_dir):
+    """Flash Attention page, 2.Online Softmax §六: step table for x = [1, 3, 2, 5]."""
+    g = _load(golden_dir, "online_softmax_worked_example.json")
+    tol = 0.5 * 10 ** -g["printed_decimals"] + 1e-12
+    steps = online_softmax_steps(g["x"])
+    assert len(steps) == len(g["steps"])
+    for (m, factor, ell), want in zip(steps, g["steps"]):
+        assert m == want["m"]
+        assert abs(factor - want["factor"]) <= tol
+        assert abs(ell - want["l"]) <= tol
+    # the standard (3-pass) column of the same example
+    y, m3, l3 = softmax_3pass(np.array(g["x"], dtype=float))
+    assert m3 == g["standard"]["m"]
+    assert abs(l3 - g["standard"]["l"]) <= tol
+    for t, want in zip(np.exp(np.array(g["x"]) - m3), g["standard"]["terms"]):
+        assert abs(t - want) <= tol
+    # exactness claim (§五): online and 3-pass agree to rounding
+    assert abs(steps[-1][2] - l3) <= 1e-12
+    assert abs(y.sum() - 1.0) <= 1e-15
+
+
+def test_merge_associative_and_equal_to_3pass():
+    """2.Online Softmax §3.1: the two-block merge is associative and exact."""
+    rng = _rng(11)
+    x = rng.uniform(-50.0, 50.0, size=1000)
+    _, m_ref, l_ref = softmax_3pass(x)
+    cuts = np.sort(rng.choice(np.arange(1, 1000), size=17, replace=False))
+    blocks = np.split(x, cuts)
+    stats = [(b.max(), np.exp(b - b.max()).sum()) for b in blocks]
+
+    left = (-math.inf, 0.0)
+    for s in stats:
+        left = merge_stats(*left, *s)
+    right = (-math.inf, 0.0)
+    for s in reversed(stats):
+        right = merge_stats(*s, *right)
+
+    def tree(items):
+        if len(items) == 1:
+            return items[0]
+        mid = len(items) // 2
+        return merge_stats(*tree(items[:mid]), *tree(items[mid:]))
+
+    for m, ell in (left, right, tree(stats)):
+        assert m == m_ref
+        assert abs(ell - l_ref) <= 1e-13 * l_ref
+
+
+def test_merge_outputs_matches_definition():
+    """2.Online Softmax §4.1: merging unnormalised outputs gives softmax(x)·V."""
+    rng = _rng(12)
+    x = rng.normal(size=300) * 5
+    v = rng.normal(size=(300, 7))
+    y, _, _ = softmax_3pass(x)
+    a, b = slice(0, 113), slice(113, 300)
+    ma, mb = x[a].max(), x[b].max()
+    la, lb = np.exp(x[a] - ma).sum(), np.exp(x[b] - mb).sum()
+    oa, ob = np.exp(x[a] - ma) @ v[a], np.exp(x[b] - mb) @ v[b]
+    m, ell, o = merge_outputs(ma, la, oa, mb, lb, ob)
+    np.testing.assert_allclose(o / ell, y @ v, rtol=0, atol=1e-13)
+    # an empty block (-inf, 0, 0) is the identity of the merge
+    m2, l2, o2 = merge_outputs(-math.inf, 0.0, np.zeros(7), ma, la, oa)
+    assert m2 == ma and l2 == la
+    np.testing.assert_array_equal(o2, oa)
+
+
+def test_softmax_rows_sum_to_one():
+    """附录A 结论二 一: Σ_i p_i = 1 and p_i > 0."""
+    rng = _rng(13)
+    x = rng.normal(size=(64, 333)) * 20
+    y, _, _ = softmax_3pass(x)
+    assert np.all(y > 0)
+    assert np.max(np.abs(y.sum(axis=1) - 1.0)) <= 1e-12
+
+
+def test_overflow_and_shift_invariance():
+    """2.Online Softmax §1.2-1.3 and the cnnetsun.cn page §2.1: x = 1000 overflows
+    the naive form; the max-subtracted form is finite and shift invariant."""
+    x = np.array([1000.0, 999.0, 10.0, -1000.0])
+    assert not np.all(np.isfinite(naive_softmax(x)))      # negative control
+    y, m, ell = softmax_3pass(x)
+    assert np.all(np.isfinite(y)) and m == 1000.0
+    y2, _, _ = softmax_3pass(x - 777.25)
+    np.testing.assert_allclose(y, y2, rtol=1e-12, atol=0)
+    # attention level: adding t·e_0 to every key shifts row i's scores by
+    # scale·t·q_i0, a per-row constant, so O is unchanged and LSE moves by it.
+    rng = _rng(14)
+    n, d = 40, 16
+    scale = d ** -0.5
+    q, k, v = rng.normal(size=(n, d)), rng.normal(size=(n, d)), rng.normal(size=(n, d))
+    q[:, 0] = rng.choice([-1.0, 1.0], size=n) * rng.uniform(0.5, 1.0, size=n)
+    t = 4000.0
+    k2 = k.copy()
+    k2[:, 0] += t
+    for causal in (False, True):
+        o, lse = attention_forward_head(q, k, v, scale, causal)
+        o2, lse2 = attention_forward_head(q, k2, v, scale, causal)
+        assert np.all(np.isfinite(o2)) and np.all(np.isfinite(lse2))
+        assert np.max(np.abs(scale * t * q[:, 0])) > 1e3 * 0.9
+        np.testing.assert_allclose(o2, o, rtol=0, atol=1e-9)
+        np.testing.assert_allclose(lse2 - scale * t * q[:, 0], lse, rtol=1e-12, atol=1e-9)
+
+
+# ---------------------------------------------------------------- forward closed forms
+
+
+def test_two_key_worked_example(golden_dir):
+    """附录A 结论二 七's numbers embedded in one head pin the scale, O, LSE and all
+    three gradients (see the fixture's construction)."""
+    g = _load(golden_dir, "attention_two_key_example.json")
+    q, k, v, do = (np.array(g[x], dtype=float) for x in ("q", "k", "v", "do"))
+    o, lse = attention_forward_head(q, k, v, g["scale"])
+    dq, dk, dv = attention_backward_head(q, k, v, do, g["scale"])
+    e = g["expected"]
+    tol = g["tolerance"]
+    np.testing.assert_allclose(o, e["O"], atol=tol, rtol=0)
+    np.testing.assert_allclose(lse, e["LSE"], atol=tol, rtol=0)
+    np.testing.assert_allclose(dv, e["dV"], atol=tol, rtol=0)
+    np.testing.assert_allclose(dq, e["dQ"], atol=tol, rtol=0)
+    np.testing.assert_allclose(dk, e["dK"], atol=tol, rtol=0)
+
+
+def test_two_key_closed_form():
+    """Two visible keys: p_1 is the logistic of the score gap, LSE = ln(e^{s1}+e^{s2})."""
+    rng = _rng(15)
+    d = 8
+    scale = 0.37
+    q, k, v = rng.normal(size=(1, d)), rng.normal(size=(2, d)), rng.normal(size=(2, d))
+    s1, s2 = scale * float(q[0] @ k[0]), scale * float(q[0] @ k[1])
+    p1 = 1.0 / (1.0 + math.exp(s2 - s1))
+    o, lse = attention_forward_head(q, k, v, scale)
+    np.testing.assert_allclose(o[0], p1 * v[0] + (1 - p1) * v[1], atol=1e-14, rtol=0)
+    assert abs(lse[0] - math.log(math.exp(s1) + math.exp(s2))) <= 1e-13
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_v_gives_constant_o(causal):
+    """Rows of P sum to one, so V_j = c for all j gives O_i = c."""
+    rng = _rng(16)
+    n, d = 50, 12
+    q, k = rng.normal(size=(n, d)) * 3, rng.normal(size=(n, d)) * 3
+    c = rng.normal(size=d)
+    o, _ = attention_forward_head(q, k, np.tile(c, (n, 1)), d ** -0.5, causal)
+    assert np.max(np.abs(o - c)) <= 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_identical_keys_give_mean_of_v(causal):
+    """K_j = k for all j makes P uniform over the visible keys: O_i = mean_{j visible} V_j."""
+    rng = _rng(17)
+    n, d = 45, 10
+    q = rng.normal(size=(n, d))
+    k = np.tile(rng.normal(size=d), (n, 1))
+    v = rng.normal(size=(n, d))
+    o, lse = attention_forward_head(q, k, v, d ** -0.5, causal)
+    if causal:
+        want = np.cumsum(v, axis=0) / np.arange(1, n + 1)[:, None]
+        count = np.arange(1, n + 1)
+    else:
+        want = np.tile(v.mean(axis=0), (n, 1))
+        count = np.full(n, n)
+    assert np.max(np.abs(o - want)) <= 1e-12
+    s = (d ** -0.5) * (q @ k[0])
+    np.testing.assert_allclose(lse, s + np.log(count), atol=1e-12, rtol=0)
+
+
+def test_causal_mask_direction():
+    """Key j is visible to query i iff j <= i; the first query sees only key 0."""
+    m = causal_mask(4, 4)
+    assert m[0].tolist() == [True, False, False, False]
+    assert m[3].tolist() == [True, True, True, True]
+    rng = _rng(18)
+    q, k, v = rng.normal(size=(6, 4)), rng.normal(size=(6, 4)), rng.normal(size=(6, 4))
+    o, lse = attention_forward_head(q, k, v, 0.5, causal=True)
+    np.testing.assert_allclose(o[0], v[0], atol=1e-15, rtol=0)
+    assert abs(lse[0] - 0.5 * float(q[0] @ k[0])) <= 1e-15
+
+
+def _brute_force_head(q, k, v, scale, causal):
+    """Scalar loops with math.exp; independent of numpy's vectorised path."""
+    n, d = len(q), len(q[0])
+    o, lse = [], []
+    for i in range(n):
+        keys = [j for j in range(len(k)) if (not causal or j <= i)]
+        s = [scale * sum(q[i][t] * k[j][t] for t in range(d)) for j in keys]
+        mx = max(s)
+        w = [math.exp(x - mx) for x in s]
+        z = math.fsum(w)
+        o.append([math.fsum(w[a] * v[j][t] for a, j in enumerate(keys)) / z for t in range(len(v[0]))])
+        lse.append(mx + math.log(z))
+    return np.array(o), np.array(lse)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_matches_scalar_brute_force(causal):
+    rng = _rng(19)
+    q, k, v = rng.normal(size=(7, 5)), rng.normal(size=(7, 5)), rng.normal(size=(7, 5))
+    o, lse = attention_forward_head(q, k, v, 0.61, causal)
+    ob, lseb = _brute_force_head(q.tolist(), k.tolist(), v.tolist(), 0.61, causal)
+    np.testing.assert_allclose(o, ob, atol=1e-14, rtol=0)
+    np.testing.assert_allclose(lse, lseb, atol=1e-14, rtol=0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("block", [1, 7, 32, 64, 300])
+def test_tiled_algorithm_equals_definition(causal, block):
+    """2.Online Softmax §4.2 + §五: the one-pass tiled forward reaches the same O and
+    LSE as the materialised definition (ragged last block included)."""
+    rng = _rng(20 + block)
+    n, d = 150, 16
+    q, k, v = rng.normal(size=(n, d)) * 2, rng.normal(size=(n, d)) * 2, rng.normal(size=(n, d))
+    o, lse = attention_forward_head(q, k, v, d ** -0.5, causal)
+    ot, lset = tiled_forward_head(q, k, v, d ** -0.5, block, causal)
+    np.testing.assert_allclose(ot, o, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lset, lse, atol=1e-12, rtol=0)
+
+
+def test_self_test_shape_of_cnnetsun_page():
+    """cnnetsun.cn page §4 self-test shape (1, 256, 64), scale 64^-0.5, block 128."""
+    rng = _rng(42)
+    q, k, v = rng.normal(size=(256, 64)), rng.normal(size=(256, 64)), rng.normal(size=(256, 64))
+    o, lse = attention_forward_head(q, k, v, 64 ** -0.5)
+    ot, lset = tiled_forward_head(q, k, v, 64 ** -0.5, 128)
+    assert np.max(np.abs(o - ot)) <= 1e-13 and np.max(np.abs(lse - lset)) <= 1e-13
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_subset_equals_full(causal):
+    rng = _rng(21)
+    q, k, v = rng.normal(size=(64, 8)), rng.normal(size=(64, 8)), rng.normal(size=(64, 8))
+    rows = [0, 5, 17, 63]
+    o, lse = attention_forward_head(q, k, v, 0.3, causal)
+    orow, lserow = attention_forward_rows(q, k, v, rows, 0.3, causal)
+    np.testing.assert_allclose(orow, o[rows], atol=1e-14, rtol=0)
+    np.testing.assert_allclose(lserow, lse[rows], atol=1e-14, rtol=0)
+
+
+# ---------------------------------------------------------------- backward pins
+
+
+def test_matmul_gradient_example(golden_dir):
+    """附录A 结论一 七 (1x2 example) and the 八 table row for Y = A Bᵀ."""
+    g = _load(golden_dir, "matmul_gradient_worked_example.json")
+    da, db = matmul_backward(g["A"], g["B"], g["dY"])
+    np.testing.assert_array_equal(da, g["dA"])
+    np.testing.assert_array_equal(db, g["dB"])
+    rng = _rng(22)
+    a, b, dy = rng.normal(size=(3, 4)), rng.normal(size=(5, 4)), rng.normal(size=(3, 5))
+    da, dbt = matmul_backward(a, b.T, dy)       # Y = A Bᵀ
+    np.testing.assert_allclose(da, dy @ b, atol=1e-14, rtol=0)
+    np.testing.assert_allclose(dbt.T, dy.T @ a, atol=1e-14, rtol=0)
+
+
+def test_softmax_backward_example(golden_dir):
+    """附录A 结论二 七: s = (1, 2), dp = (1, 0) gives ds ≈ (0.197, -0.197)."""
+    g = _load(golden_dir, "softmax_backward_worked_example.json")
+    tol = 0.5 * 10 ** -g["printed_decimals"] + 1e-12
+    p, _, _ = softmax_3pass(np.array(g["s"], dtype=float))
+    np.testing.assert_allclose(p, g["p"], atol=tol, rtol=0)
+    ds = softmax_backward(p, np.array(g["dp"], dtype=float))
+    np.testing.assert_allclose(ds, g["ds"], atol=tol, rtol=0)
+    assert abs(float(p @ np.array(g["dp"])) - g["rho"]) <= tol
+    # the exact value: p1 (1 - p1) = e / (1 + e)^2
+    exact = math.e / (1.0 + math.e) ** 2
+    assert abs(ds[0] - exact) <= 1e-15 and abs(ds[1] + exact) <= 1e-15
+    # the Jacobian built column by column from unit upstream gradients
+    jac = np.stack([softmax_backward(p, np.eye(2)[c]) for c in range(2)], axis=1)
+    np.testing.assert_allclose(jac, g["J"], atol=tol, rtol=0)
+
+
+def test_softmax_jacobian_properties():
+    """附录A 结论二 2.4 / 5.3 / 九: column sums of J are 0, constant dp gives ds = 0,
+    and the cross-entropy upstream gradient gives ds = p - y."""
+    rng = _rng(23)
+    s = rng.normal(size=9) * 3
+    p, _, _ = softmax_3pass(s)
+    jac = np.stack([softmax_backward(p, np.eye(9)[c]) for c in range(9)], axis=1)
+    np.testing.assert_allclose(jac, np.diag(p) - np.outer(p, p), atol=1e-15, rtol=0)
+    assert np.max(np.abs(jac.sum(axis=0))) <= 1e-15
+    assert np.max(np.abs(softmax_backward(p, np.full(9, 3.7)))) <= 1e-14
+    y = np.zeros(9)
+    y[4] = 1.0
+    np.testing.assert_allclose(softmax_backward(p, -y / p), p - y, atol=1e-14, rtol=0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_d_identity(causal):
+    """"反向传播的公式推导" 五: rowsum(dP ⊙ P) = rowsum(dO ⊙ O)."""
+    rng = _rng(24)
+    n, d = 70, 16
+    q, k, v, do = (rng.normal(size=(n, d)) for _ in range(4))
+    o, _ = attention_forward_head(q, k, v, d ** -0.5, causal)
+    *_, mid = attention_backward_head(q, k, v, do, d ** -0.5, causal, return_intermediates=True)
+    lhs = (mid["dP"] * mid["P"]).sum(axis=1)
+    rhs = (do * o).sum(axis=1)
+    assert np.max(np.abs(lhs - rhs)) <= 1e-12 * max(1.0, np.max(np.abs(rhs)))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gradient_invariants(causal):
+    """Σ_j dS_ij = 0 (constant-dp invariance), hence Σ_j dK_j = 0; rows of P sum to
+    one, hence Σ_j dV_j = Σ_i dO_i."""
+    rng = _rng(25)
+    n, d = 60, 16
+    q, k, v, do = (rng.normal(size=(n, d)) for _ in range(4))
+    dq, dk, dv, mid = attention_backward_head(q, k, v, do, d ** -0.5, causal, return_intermediates=True)
+    assert np.max(np.abs(mid["dS"].sum(axis=1))) <= 1e-12
+    assert np.max(np.abs(dk.sum(axis=0))) <= 1e-11
+    np.testing.assert_allclose(dv.sum(axis=0), do.sum(axis=0), atol=1e-11, rtol=0)
+
+
+def _loss(q, k, v, do, scale, causal):
+    o, _ = attention_forward_head(q, k, v, scale, causal)
+    return float((do * o).sum())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n", [4, 8])
+def test_finite_difference_gradients(causal, n):
+    """Central differences of L = Σ dO ⊙ O (h = 1e-6) against dQ, dK, dV."""
+    rng = _rng(26 + n)
+    d = 4
+    scale = 0.7
+    q, k, v, do = (rng.normal(size=(n, d)) for _ in range(4))
+    grads = attention_backward_head(q, k, v, do, scale, causal)
+    h = 1e-6
+    for which, g in zip(range(3), grads):
+        fd = np.zeros((n, d))
+        for i in range(n):
+            for t in range(d):
+                args = [q.copy(), k.copy(), v.copy()]
+                args[which][i, t] += h
+                up = _loss(*args, do, scale, causal)
+                args[which][i, t] -= 2 * h
+                dn = _loss(*args, do, scale, causal)
+                fd[i, t] = (up - dn) / (2 * h)
+        err = np.linalg.norm(fd - g) / max(np.linalg.norm(g), 1e-30)
+        assert err <= 1e-6, (which, err)

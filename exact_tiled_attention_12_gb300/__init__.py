@@ -1,1 +1,19 @@
-"""Exact tiled attention (forward + backward) for GB300 / sm_103a."""
+"""Exact tiled attention (forward + backward) for GB300 / sm_103a.
+
+The compute path is the C-ABI library ``libfa.so`` built from ``csrc/``;
+``fwd``/``bwd`` are thin argument-marshalling wrappers around it.  The shared
+library is loaded on first use and the wrappers raise if it is missing: there
+is no fallback implementation.
+"""
+
+from .binding import (  # noqa: F401
+    FaError,
+    bwd,
+    bwd_stages,
+    bwd_workspace_size,
+    fwd,
+    lib,
+    library_path,
+    status_string,
+    sync_status,
+)

@@ -1,0 +1,177 @@
+"""ctypes binding for libfa.so — argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+allocates outputs with torch (the library allocates nothing), passes device
+pointers and the current CUDA stream, and turns status codes into exceptions.
+If libfa.so is missing the calls raise: there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+FA_DTYPE_BF16 = 0
+FA_DTYPE_FP32 = 1
+_STATUS = {
+    0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_MISALIGNED",
+    4: "FA_ERR_WORKSPACE", 5: "FA_ERR_CUDA", 6: "FA_ERR_TIMEOUT",
+}
+# Every function include/fa.h declares, with (restype, argtypes).
+_P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "fa_status_string": (ctypes.c_char_p, [_I]),
+    "fa_version": (_I, []),
+    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "fa_bwd_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P, _Z, _P]),
+    "fa_bwd_prep": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "fa_bwd_tiles": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P, _Z, _P]),
+    "fa_bwd_dq_finish": (_I, [_P, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
+    "fa_sync_status": (_I, [_P]),
+}
+
+
+class FaError(RuntimeError):
+    """A non-zero fa_status returned by the library."""
+
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {status_string(code)}")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libfa.so")
+
+
+def lib():
+    """Loads libfa.so once (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+        handle = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = handle
+    return _LIB
+
+
+def status_string(code: int) -> str:
+    try:
+        return lib().fa_status_string(int(code)).decode()
+    except Exception:  # library not loadable: fall back to the static table
+        return _STATUS.get(int(code), f"status {code}")
+
+
+def _check(fn: str, code: int) -> None:
+    if code != 0:
+        raise FaError(fn, code)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return FA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return FA_DTYPE_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}; use torch.bfloat16 or torch.float32")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else ctypes.c_void_p(0)
+
+
+def _stream(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _check_qkv(*ts):
+    ref = ts[0]
+    if ref.dim() != 4:
+        raise ValueError("tensors must be [B, H, N, d]")
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must be CUDA tensors")
+        if t.shape != ref.shape or t.dtype != ref.dtype or t.device != ref.device:
+            raise ValueError("q, k, v (and o, dO) must share shape, dtype and device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous [B, H, N, d]")
+
+
+def fwd(q, k, v, scale=None, causal=False):
+    """Attention forward.  Returns (o [B,H,N,d] in q's dtype, lse [B,H,N] float32)."""
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    scale = float(d ** -0.5 if scale is None else scale)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        _check("fa_fwd", lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
+                                      int(bool(causal)), _dtype_code(q), _stream(q)))
+    return o, lse
+
+
+def bwd_workspace_size(B, H, N, d, dtype=torch.bfloat16) -> int:
+    code = FA_DTYPE_BF16 if dtype == torch.bfloat16 else FA_DTYPE_FP32
+    return int(lib().fa_bwd_workspace_size(B, H, N, d, code))
+
+
+def _workspace(q):
+    B, H, N, d = q.shape
+    n = bwd_workspace_size(B, H, N, d, q.dtype)
+    # torch's caching allocator returns blocks aligned to at least 512 bytes
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=q.device), n
+
+
+def bwd(q, k, v, o, do, lse, scale=None, causal=False, workspace=None):
+    """Attention backward.  Returns (dq, dk, dv) in q's dtype."""
+    _check_qkv(q, k, v, o, do)
+    B, H, N, d = q.shape
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    scale = float(d ** -0.5 if scale is None else scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws, n = _workspace(q) if workspace is None else (workspace, workspace.numel())
+    with torch.cuda.device(q.device):
+        _check("fa_bwd", lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                                      _ptr(dv), B, H, N, d, scale, int(bool(causal)), _dtype_code(q), _ptr(ws), n,
+                                      _stream(q)))
+    return dq, dk, dv
+
+
+def bwd_stages(q, k, v, o, do, lse, dq, dk, dv, workspace, scale=None, causal=False, between=None):
+    """fa_bwd as its three stages on the current stream, writing into dq/dk/dv.
+
+    ``between`` is an optional pair of callables run just before and just
+    after the tiled stage (the bench records CUDA events there).
+    """
+    B, H, N, d = q.shape
+    scale = float(d ** -0.5 if scale is None else scale)
+    code = _dtype_code(q)
+    s = _stream(q)
+    L = lib()
+    n = workspace.numel()
+    _check("fa_bwd_prep", L.fa_bwd_prep(_ptr(o), _ptr(do), _ptr(lse), B, H, N, d, code, _ptr(workspace), n, s))
+    if between:
+        between[0]()
+    _check("fa_bwd_tiles", L.fa_bwd_tiles(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N,
+                                          d, scale, int(bool(causal)), code, _ptr(workspace), n, s))
+    if between:
+        between[1]()
+    _check("fa_bwd_dq_finish", L.fa_bwd_dq_finish(_ptr(dq), B, H, N, d, scale, code, _ptr(workspace), n, s))
+
+
+def sync_status(device=None) -> int:
+    """Synchronises the current stream and returns the library's fault status (0 = OK)."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(lib().fa_sync_status(ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)))

@@ -1,0 +1,306 @@
+// fa_abi.cu — the extern "C" boundary of libfa.so (declared in include/fa.h).
+//
+// Host-side only: argument validation, TMA tensor-map encoding, workspace
+// carving and kernel dispatch.  Every argument check runs before any CUDA call,
+// so invalid calls return an error with no side effect (and need no GPU).
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "fa.h"
+#include "fa_kernels.h"
+
+namespace {
+
+// One fault word per device; kernels record the first timed-out wait here.
+__device__ unsigned int g_fault_word;
+
+constexpr int kMaxDevices = 64;
+std::atomic<unsigned int*> g_fault_ptr[kMaxDevices];
+
+unsigned int* fault_word_for_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  unsigned int* p = g_fault_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_fault_word) != cudaSuccess) return nullptr;
+  p = static_cast<unsigned int*>(addr);
+  g_fault_ptr[dev].store(p, std::memory_order_release);
+  return p;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 f = fn.load(std::memory_order_acquire);
+  if (f) return f;
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || p == nullptr)
+    return nullptr;
+  f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  fn.store(f, std::memory_order_release);
+  return f;
+}
+
+// 2-D map over a [rows, d] bf16 row-major matrix; boxes of 64 columns
+// (128 bytes) × box_rows rows, 128-byte swizzle.
+bool encode_bf16_rows(CUtensorMap* m, const void* base, unsigned long long rows, int d, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+inline size_t pad256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// ------------------------------------------------------------------ validation
+
+struct Shape {
+  long long B, H, N, d;
+  long long rows() const { return B * H * N; }
+  long long elems() const { return B * H * N * d; }
+  bool empty() const { return B == 0 || H == 0 || N == 0; }
+};
+
+fa_status check_shape(int B, int H, int N, int d, fa_dtype dtype, Shape* out) {
+  if (B < 0 || H < 0 || N < 0 || d <= 0) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP32) return FA_ERR_INVALID_ARG;
+  Shape s{B, H, N, d};
+  if (s.elems() > (1ll << 40)) return FA_ERR_UNSUPPORTED;
+  if (!s.empty()) {
+    if (dtype == FA_DTYPE_BF16) {
+      if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+      if (N % 128 != 0) return FA_ERR_UNSUPPORTED;
+      if (s.rows() >= (1ll << 31) || N / 128 > 65535) return FA_ERR_UNSUPPORTED;
+    } else {
+      if (d > 128) return FA_ERR_UNSUPPORTED;
+      if (s.B * s.H > 65535 || s.rows() >= (1ll << 31)) return FA_ERR_UNSUPPORTED;
+    }
+  }
+  *out = s;
+  return FA_OK;
+}
+
+fa_status check_scale(float scale) {
+  return (isfinite(scale) && scale > 0.f) ? FA_OK : FA_ERR_INVALID_ARG;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status check_ptrs(std::initializer_list<const void*> ptrs, fa_dtype dtype) {
+  for (const void* p : ptrs)
+    if (p == nullptr) return FA_ERR_INVALID_ARG;
+  if (dtype == FA_DTYPE_BF16)
+    for (const void* p : ptrs)
+      if (!aligned16(p)) return FA_ERR_MISALIGNED;
+  for (const void* p : ptrs)
+    if ((reinterpret_cast<uintptr_t>(p) & 3u) != 0) return FA_ERR_MISALIGNED;
+  return FA_OK;
+}
+
+size_t workspace_bytes_for(const Shape& s, fa_dtype dtype) {
+  if (s.empty()) return 0;
+  const size_t rows = (size_t)s.rows();
+  if (dtype == FA_DTYPE_FP32) return 2 * pad256(rows * 4);
+  return 2 * pad256(rows * 4) + pad256((size_t)s.elems() * 4);
+}
+
+// Workspace parts: D (float32 per row), the forward's LSE per row (base 2 for
+// bf16, natural-log copy for fp32), and for bf16 the float32 dQ accumulator.
+struct Workspace {
+  float* dvec;
+  float* lse2;
+  float* dqacc;
+};
+
+fa_status carve_workspace(const Shape& s, fa_dtype dtype, void* ws, size_t bytes, Workspace* w) {
+  const size_t need = workspace_bytes_for(s, dtype);
+  if (need == 0) return FA_OK;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || bytes < need) return FA_ERR_WORKSPACE;
+  char* p = static_cast<char*>(ws);
+  const size_t rows = (size_t)s.rows();
+  w->dvec = reinterpret_cast<float*>(p);
+  w->lse2 = reinterpret_cast<float*>(p + pad256(rows * 4));
+  w->dqacc = dtype == FA_DTYPE_FP32 ? nullptr : reinterpret_cast<float*>(p + 2 * pad256(rows * 4));
+  return FA_OK;
+}
+
+inline fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+constexpr float kLog2e = 1.4426950408889634074f;
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null pointer, negative size or bad scale/causal/dtype";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: shape or dtype not implemented";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED: pointer not aligned (bf16 needs 16 bytes)";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing, misaligned (256 B) or too small";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call or kernel launch failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel abandoned a pipeline wait";
+  }
+  return "unknown fa_status";
+}
+
+int fa_version(void) { return 100; }
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 float scale, int causal, fa_dtype dtype, fa_stream_t stream) {
+  Shape s;
+  fa_status st = check_shape(B, H, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (s.empty()) return FA_OK;
+  if ((st = check_ptrs({q, k, v, o, lse}, dtype)) != FA_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  unsigned int* fault = fault_word_for_current_device();
+  if (!fault) return FA_ERR_CUDA;
+  if (dtype == FA_DTYPE_FP32)
+    return from_cuda(fa::launch_fwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                        static_cast<const float*>(v), static_cast<float*>(o), lse, (int)(s.B * s.H),
+                                        N, d, scale, causal, cs));
+  fa::FwdArgs a;
+  if (!encode_bf16_rows(&a.tm_q, q, (unsigned long long)s.rows(), d, 128) ||
+      !encode_bf16_rows(&a.tm_k, k, (unsigned long long)s.rows(), d, 128) ||
+      !encode_bf16_rows(&a.tm_v, v, (unsigned long long)s.rows(), d, 128))
+    return FA_ERR_CUDA;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.scale_log2 = scale * kLog2e;
+  a.causal = causal;
+  a.fault = fault;
+  return from_cuda(fa::launch_fwd_bf16(a, cs));
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d, fa_dtype dtype) {
+  Shape s;
+  if (check_shape(B, H, N, d, dtype, &s) != FA_OK) return 0;
+  return workspace_bytes_for(s, dtype);
+}
+
+fa_status fa_bwd_prep(const void* o, const void* dO, const float* lse, int B, int H, int N, int d, fa_dtype dtype,
+                      void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  Shape s;
+  fa_status st = check_shape(B, H, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  if (s.empty()) return FA_OK;
+  if ((st = check_ptrs({o, dO, lse}, dtype)) != FA_OK) return st;
+  Workspace w;
+  if ((st = carve_workspace(s, dtype, workspace, workspace_bytes, &w)) != FA_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == FA_DTYPE_FP32)
+    return from_cuda(fa::launch_bwd_prep_f32(static_cast<const float*>(o), static_cast<const float*>(dO), lse, w.dvec,
+                                             w.lse2, s.rows(), d, cs));
+  return from_cuda(fa::launch_bwd_prep_bf16(static_cast<const __nv_bfloat16*>(o),
+                                            static_cast<const __nv_bfloat16*>(dO), lse, w.dvec, w.lse2, w.dqacc,
+                                            s.rows(), d, cs));
+}
+
+fa_status fa_bwd_tiles(const void* q, const void* k, const void* v, const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+                                fa_dtype dtype, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  Shape s;
+  fa_status st = check_shape(B, H, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (s.empty()) return FA_OK;
+  if ((st = check_ptrs({q, k, v, dO, dk, dv}, dtype)) != FA_OK) return st;
+  if (dtype == FA_DTYPE_FP32 && (st = check_ptrs({dq}, dtype)) != FA_OK) return st;
+  Workspace w;
+  if ((st = carve_workspace(s, dtype, workspace, workspace_bytes, &w)) != FA_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == FA_DTYPE_FP32)
+    return from_cuda(fa::launch_bwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                        static_cast<const float*>(v), static_cast<const float*>(dO), w.lse2, w.dvec,
+                                        static_cast<float*>(dq), static_cast<float*>(dk), static_cast<float*>(dv),
+                                        (int)(s.B * s.H), N, d, scale, causal, cs));
+  unsigned int* fault = fault_word_for_current_device();
+  if (!fault) return FA_ERR_CUDA;
+  fa::BwdArgs a;
+  const int bm = fa::bwd_bf16_block_m(d);
+  const unsigned long long rows = (unsigned long long)s.rows();
+  if (!encode_bf16_rows(&a.tm_q, q, rows, d, bm) || !encode_bf16_rows(&a.tm_k, k, rows, d, 128) ||
+      !encode_bf16_rows(&a.tm_v, v, rows, d, 128) || !encode_bf16_rows(&a.tm_do, dO, rows, d, bm))
+    return FA_ERR_CUDA;
+  a.lse2 = w.lse2;
+  a.dvec = w.dvec;
+  a.dqacc = w.dqacc;
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.scale_log2 = scale * kLog2e;
+  a.scale = scale;
+  a.causal = causal;
+  a.fault = fault;
+  return from_cuda(fa::launch_bwd_bf16(a, cs));
+}
+
+fa_status fa_bwd_dq_finish(void* dq, int B, int H, int N, int d, float scale, fa_dtype dtype, void* workspace,
+                           size_t workspace_bytes, fa_stream_t stream) {
+  Shape s;
+  fa_status st = check_shape(B, H, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (s.empty() || dtype == FA_DTYPE_FP32) return FA_OK;
+  if ((st = check_ptrs({dq}, dtype)) != FA_OK) return st;
+  Workspace w;
+  if ((st = carve_workspace(s, dtype, workspace, workspace_bytes, &w)) != FA_OK) return st;
+  return from_cuda(fa::launch_dq_finish_bf16(w.dqacc, static_cast<__nv_bfloat16*>(dq), s.elems(), scale,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                 void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, fa_dtype dtype,
+                 void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  Shape s;
+  fa_status st = check_shape(B, H, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (s.empty()) return FA_OK;
+  if ((st = check_ptrs({q, k, v, o, dO, lse, dq, dk, dv}, dtype)) != FA_OK) return st;
+  Workspace w;
+  if ((st = carve_workspace(s, dtype, workspace, workspace_bytes, &w)) != FA_OK) return st;
+  if ((st = fa_bwd_prep(o, dO, lse, B, H, N, d, dtype, workspace, workspace_bytes, stream)) != FA_OK) return st;
+  if ((st = fa_bwd_tiles(q, k, v, dO, dq, dk, dv, B, H, N, d, scale, causal, dtype, workspace, workspace_bytes,
+                         stream)) != FA_OK)
+    return st;
+  return fa_bwd_dq_finish(dq, B, H, N, d, scale, dtype, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_sync_status(fa_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_fault_word, sizeof(word)) != cudaSuccess) return FA_ERR_CUDA;
+  if (word != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+}  // extern "C"

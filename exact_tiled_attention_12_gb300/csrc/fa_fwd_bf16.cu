@@ -1,0 +1,354 @@
+// fa_fwd_bf16.cu — tiled attention forward on the sm_103a tensor cores.
+//
+// What it computes: "Flash Attention" tutorial, 2.Online Softmax §4.2 — one
+// pass over K/V tiles with the running (m, ℓ) of §3.1 and the unnormalised
+// output Õ of §4.1, divided by ℓ once at the end; the saved statistic is
+// LSE = m + ln ℓ (3.Recomputation 三).  Scores never leave the SM.
+//
+// CTA = two 128-row query tiles of one (batch, head), 10 warps:
+//   warps 0-3  softmax for query tile 0 (one thread per query row)
+//   warps 4-7  softmax for query tile 1
+//   warp  8    TMA producer: Q once, then K_j / V_j through a 2-stage ring
+//   warp  9    MMA issuer (one thread) and tensor-memory owner
+// Tensor memory (512 columns × 128 lanes × 32 bit):
+//   S_t  = cols [128 t, 128 t + 128)   fp32 scores of tile t (S = Q_t K_jᵀ)
+//   P_t  = cols [128 t, 128 t + 64)    bf16x2 probabilities, written over S_t
+//   O_t  = cols [256 + d t, 256 + d t + d)   fp32 unnormalised output
+// Per K/V tile the MMA thread issues, for each query tile, O_t += P_t V_j (A
+// from tensor memory) and then S_t = Q_t K_{j+1}ᵀ, so the softmax of one
+// tile overlaps the products of the other.
+//
+// Rescaling is lazy: the reference max m only moves when a row's new max
+// exceeds it by more than 8 (base 2), so P ≤ 2^8 and ℓ and Õ keep sharing one
+// reference — the merge of §3.1/§4.1 with a stale but common reference is
+// still exact.  When it moves, the softmax thread rescales its row of O_t in
+// tensor memory; the commit that signalled S_t also guarantees the previous
+// O_t += P_t V product has finished.
+#include "fa_kernels.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBM = 128;           // query rows per tile
+constexpr int kBN = 128;           // keys per K/V tile
+constexpr int kThreads = 320;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kBoxBytes = 128 * 128;   // one TMA box: 128 rows × 128 bytes
+
+// Shared-memory layout (offsets from a 1024-byte aligned base).
+template <int D>
+struct FwdLayout {
+  static constexpr int kTile = kBM * D * 2;       // bytes of one 128 × D bf16 tile
+  static constexpr int kQ = 0;                    // Q tile t at kQ + t·kTile
+  static constexpr int kK = kQ + 2 * kTile;       // K stage s
+  static constexpr int kV = kK + 2 * kTile;       // V stage s
+  static constexpr int kBar = kV + 2 * kTile;
+  static constexpr int kBytes = kBar + 256;
+};
+
+// Barrier slots (8 bytes each) inside the barrier block.
+enum FwdBar : int {
+  kQFull = 0,
+  kKFull = 1,    // +stage
+  kKEmpty = 3,   // +stage
+  kVFull = 5,    // +stage
+  kVEmpty = 7,   // +stage
+  kSFull = 9,    // +tile
+  kPFull = 11,   // +tile
+  kOFull = 13,   // +tile
+  kMmaDone = 15,
+  kNumBars = 16,
+};
+
+// Fault codes recorded when a wait runs out of time (kernel id 1 in the high byte).
+__device__ __forceinline__ uint32_t site(int s) { return 0x0100u | (uint32_t)s; }
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_constant__ FwdArgs a) {
+  using L = FwdLayout<D>;
+  // Dynamic shared memory starts on a 1024-byte boundary (no static shared
+  // memory is declared); 128-byte swizzled tiles need that alignment.
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t sbase = smem_u32(smem_raw);
+  uint8_t* sgen = smem_raw;
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) atomicCAS(a.fault, 0u, site(0));
+    return;
+  }
+  const uint32_t bars = sbase + L::kBar;
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sgen + L::kBar + 8 * kNumBars);
+  int* abort_flag = reinterpret_cast<int*>(sgen + L::kBar + 8 * kNumBars + 4);
+  const WaitCtx wc{abort_flag, a.fault};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int N = a.N;
+  const int bh = blockIdx.x;
+  const int pair = (int)gridDim.y - 1 - (int)blockIdx.y;   // heaviest query tiles first
+  const int q0 = pair * 2 * kBM;
+  const int row0 = bh * N;                                 // first row of this head in the [B·H·N, d] view
+  const int n_kv = N / kBN;
+
+  // Number of K/V tiles each query tile visits (0 if the tile is past N).
+  int n_t[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qt = q0 + t * kBM;
+    n_t[t] = qt >= N ? 0 : (CAUSAL ? qt / kBN + 1 : n_kv);
+  }
+  const int J = n_t[0] > n_t[1] ? n_t[0] : n_t[1];
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kQFull), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kKFull + s), 1);
+      mbar_init(bar(kKEmpty + s), 1);
+      mbar_init(bar(kVFull + s), 1);
+      mbar_init(bar(kVEmpty + s), 1);
+      mbar_init(bar(kSFull + s), 1);
+      mbar_init(bar(kPFull + s), 128);
+      mbar_init(bar(kOFull + s), 1);
+    }
+    mbar_init(bar(kMmaDone), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  auto s_col = [](int t) -> uint32_t { return (uint32_t)(128 * t); };
+  auto o_col = [](int t) -> uint32_t { return (uint32_t)(256 + D * t); };
+
+  if (warp < 8) {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;                // row within the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int nt = n_t[t];
+    const float sl2 = a.scale_log2;
+    float m_ref = -INFINITY;   // reference max of the row, base-2 scaled units
+    float ell = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      ok = mbar_wait(bar(kSFull + t), (uint32_t)(j & 1), wc, site(1));
+      ok = __all_sync(kFull, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[128];
+      tmem_ld_x128(tmem + lane_off + s_col(t), s);
+      if (CAUSAL && j == nt - 1) {
+        // Diagonal tile: key j·128 + c is visible to query j·128 + r iff c ≤ r.
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > r) s[c] = f2u(-INFINITY);
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; c += 4) {
+        mx0 = fmaxf(mx0, u2f(s[c]));
+        mx1 = fmaxf(mx1, u2f(s[c + 1]));
+        mx2 = fmaxf(mx2, u2f(s[c + 2]));
+        mx3 = fmaxf(mx3, u2f(s[c + 3]));
+      }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const bool move = mx > m_ref + 8.0f;                 // always true on the first tile
+      const float m_new = move ? mx : m_ref;
+      const float alpha = ex2(m_ref - m_new);              // 0 on the first tile, 1 if the reference stays
+      if (j > 0 && __any_sync(kFull, move)) {
+        // O_t += P_t V_{j-1} has completed (it was issued before S_t = Q_t K_jᵀ,
+        // whose commit we just waited on) and the next product into O_t waits
+        // for P_full, so this row of O_t is ours to rescale.
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld_x32(tmem + lane_off + o_col(t) + 32 * cc, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+          tmem_st_x32(tmem + lane_off + o_col(t) + 32 * cc, o);
+        }
+      }
+      ell *= alpha;
+      m_ref = m_new;
+      const float neg = -m_ref;
+      float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t p[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float e0 = ex2(fmaf(u2f(s[32 * cc + 2 * i]), sl2, neg));
+          const float e1 = ex2(fmaf(u2f(s[32 * cc + 2 * i + 1]), sl2, neg));
+          l0 += e0;
+          l1 += e1;
+          p[i] = pack_bf16x2(e0, e1);
+        }
+        tmem_st_x16(tmem + lane_off + s_col(t) + 16 * cc, p);
+      }
+      ell += l0 + l1;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(kPFull + t));
+    }
+    if (ok && nt > 0) {
+      ok = mbar_wait(bar(kOFull + t), 0, wc, site(2));
+      ok = __all_sync(kFull, ok);
+      if (ok) {
+        tc_fence_after();
+        const int q = q0 + t * kBM + r;
+        const float inv = 1.0f / ell;
+        __nv_bfloat16* orow = a.o + ((size_t)row0 + (size_t)q) * D;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld_x32(tmem + lane_off + o_col(t) + 32 * cc, o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            st_global_v4(orow + 32 * cc + 8 * v4, pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+        // LSE in natural log of the scaled scores: (m + log2 ℓ) · ln 2.
+        a.lse[(size_t)row0 + (size_t)q] = (m_ref + log2f(ell)) * 0.69314718055994530942f;
+      }
+    }
+  } else if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&a.tm_q);
+      prefetch_tmap(&a.tm_k);
+      prefetch_tmap(&a.tm_v);
+      int issued_k[2] = {0, 0}, issued_v[2] = {0, 0};
+      const uint32_t tile = (uint32_t)L::kTile;
+      const uint32_t qbytes = (n_t[0] > 0 ? tile : 0u) + (n_t[1] > 0 ? tile : 0u);
+      const bool have_q = qbytes > 0;
+      if (have_q) {
+        mbar_arrive_expect_tx(bar(kQFull), qbytes);
+        for (int t = 0; t < 2; ++t)
+          if (n_t[t] > 0)
+            for (int b = 0; b < D / 64; ++b)
+              tma_load_2d(sbase + L::kQ + t * L::kTile + b * kBoxBytes, &a.tm_q, bar(kQFull), 64 * b,
+                          row0 + q0 + t * kBM);
+      }
+      for (int j = 0; j < J; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(bar(kKEmpty + s), (uint32_t)(((j >> 1) - 1) & 1), wc, site(3))) break;
+        mbar_arrive_expect_tx(bar(kKFull + s), tile);
+        for (int b = 0; b < D / 64; ++b)
+          tma_load_2d(sbase + L::kK + s * L::kTile + b * kBoxBytes, &a.tm_k, bar(kKFull + s), 64 * b,
+                      row0 + j * kBN);
+        ++issued_k[s];
+        if (j >= 2 && !mbar_wait(bar(kVEmpty + s), (uint32_t)(((j >> 1) - 1) & 1), wc, site(4))) break;
+        mbar_arrive_expect_tx(bar(kVFull + s), tile);
+        for (int b = 0; b < D / 64; ++b)
+          tma_load_2d(sbase + L::kV + s * L::kTile + b * kBoxBytes, &a.tm_v, bar(kVFull + s), 64 * b,
+                      row0 + j * kBN);
+        ++issued_v[s];
+      }
+      // Never leave the CTA with copies in flight: wait for the last load of
+      // every stage (already complete in the normal case).
+      if (have_q) mbar_wait_drain(bar(kQFull), 0, wc, site(5));
+      for (int s = 0; s < 2; ++s) {
+        if (issued_k[s] > 0) mbar_wait_drain(bar(kKFull + s), (uint32_t)((issued_k[s] - 1) & 1), wc, site(5));
+        if (issued_v[s] > 0) mbar_wait_drain(bar(kVFull + s), (uint32_t)((issued_v[s] - 1) & 1), wc, site(5));
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, kBN, false, false);   // S = Q Kᵀ, both K-major
+      constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);      // O += P V, V is MN-major
+      bool ok = J == 0 || mbar_wait(bar(kQFull), 0, wc, site(6));
+      int k_ready = -1;
+      auto issue_s = [&](int t, int j) -> bool {
+        if (k_ready < j) {
+          if (!mbar_wait(bar(kKFull + (j & 1)), (uint32_t)((j >> 1) & 1), wc, site(7))) return false;
+          k_ready = j;
+        }
+        tc_fence_after();
+        const uint32_t qa = sbase + L::kQ + t * L::kTile;
+        const uint32_t kb = sbase + L::kK + (j & 1) * L::kTile;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (uint32_t)((ks >> 2) * kBoxBytes + (ks & 3) * 32);
+          mma_ss(tmem + s_col(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdS,
+                 ks > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(kSFull + t));
+        return true;
+      };
+      if (ok && J > 0) {
+        for (int t = 0; t < 2 && ok; ++t)
+          if (n_t[t] > 0) ok = issue_s(t, 0);
+        if (ok) tc_commit(bar(kKEmpty + 0));
+      }
+      for (int j = 0; ok && j < J; ++j) {
+        if (!mbar_wait(bar(kVFull + (j & 1)), (uint32_t)((j >> 1) & 1), wc, site(8))) {
+          ok = false;
+          break;
+        }
+        const uint32_t vb = sbase + L::kV + (j & 1) * L::kTile;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= n_t[t]) continue;
+          if (!mbar_wait(bar(kPFull + t), (uint32_t)(j & 1), wc, site(9))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks)
+            mma_ts(tmem + o_col(t), tmem + s_col(t) + (uint32_t)(8 * ks),
+                   sdesc_sw128(vb + (uint32_t)(ks * 2048), kBoxBytes, 1024), kIdO, (j > 0 || ks > 0) ? 1u : 0u);
+          if (j == n_t[t] - 1) tc_commit(bar(kOFull + t));
+          if (j + 1 < n_t[t]) ok = issue_s(t, j + 1);
+        }
+        if (!ok) break;
+        tc_commit(bar(kVEmpty + (j & 1)));
+        if (j + 1 < J) tc_commit(bar(kKEmpty + ((j + 1) & 1)));
+      }
+      // Every product must be finished before tensor memory is released.
+      tc_commit(bar(kMmaDone));
+      mbar_wait_drain(bar(kMmaDone), 0, wc, site(10));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_impl(const FwdArgs& a, cudaStream_t s) {
+  auto kern = fa_fwd_bf16_kernel<D, CAUSAL>;
+  const size_t smem = FwdLayout<D>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)(a.B * a.H), (unsigned)((a.N + 2 * kBM - 1) / (2 * kBM)));
+  kern<<<grid, kThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t fwd_bf16_smem_bytes(int d) {
+  return d == 64 ? FwdLayout<64>::kBytes : FwdLayout<128>::kBytes;
+}
+
+cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s) {
+  if (a.d == 128) return a.causal ? launch_impl<128, true>(a, s) : launch_impl<128, false>(a, s);
+  if (a.d == 64) return a.causal ? launch_impl<64, true>(a, s) : launch_impl<64, false>(a, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -1,0 +1,66 @@
+// fa_kernels.h — launch parameters and host launchers shared between the C-ABI
+// layer (fa_abi.cu) and the kernel translation units.  Internal to libfa.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fa {
+
+// ---------------------------------------------------------------- bf16 tensor-core path
+
+// Forward: 2-D tensor maps over the [B·H·N, d] bf16 row view of Q, K, V with
+// 64-column (128-byte) boxes of 128 rows and 128-byte swizzle.
+struct FwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v;
+  __nv_bfloat16* o;
+  float* lse;
+  int B, H, N, d;
+  float scale_log2;       // scale · log2(e): scores are handled in base 2
+  int causal;
+  unsigned int* fault;
+};
+size_t fwd_bf16_smem_bytes(int d);
+cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s);
+
+// Backward tiled loop.  tm_k / tm_v: boxes of 128 rows; tm_q / tm_do: boxes
+// of BM rows (BM = 64 for d = 128, 128 for d = 64).
+struct BwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  const float* lse2;      // workspace: LSE · log2(e), [B·H·N]
+  const float* dvec;      // workspace: D = rowsum(dO ⊙ O), [B·H·N]
+  float* dqacc;           // workspace: fp32 dQ accumulator, [B·H·N, d]
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int B, H, N, d;
+  float scale_log2;
+  float scale;
+  int causal;
+  unsigned int* fault;
+};
+int bwd_bf16_block_m(int d);
+size_t bwd_bf16_smem_bytes(int d);
+cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t s);
+
+// Backward pre-pass: D = rowsum(dO ⊙ O), LSE in base 2, zero dQ accumulator.
+cudaError_t launch_bwd_prep_bf16(const __nv_bfloat16* o, const __nv_bfloat16* dO, const float* lse,
+                                 float* dvec, float* lse2, float* dqacc, long long rows, int d,
+                                 cudaStream_t s);
+// dQ = scale · accumulator, rounded to bf16.
+cudaError_t launch_dq_finish_bf16(const float* dqacc, __nv_bfloat16* dq, long long elems, float scale,
+                                  cudaStream_t s);
+
+// ---------------------------------------------------------------- fp32 SIMT path
+
+cudaError_t launch_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int BH, int N,
+                           int d, float scale, int causal, cudaStream_t s);
+cudaError_t launch_bwd_prep_f32(const float* o, const float* dO, const float* lse, float* dvec, float* lse_copy,
+                                long long rows, int d, cudaStream_t s);
+cudaError_t launch_bwd_f32(const float* q, const float* k, const float* v, const float* dO, const float* lse,
+                           const float* dvec, float* dq, float* dk, float* dv, int BH, int N, int d, float scale,
+                           int causal, cudaStream_t s);
+
+}  // namespace fa

@@ -1,0 +1,149 @@
+/*
+ * fa.h — C ABI of the exact tiled attention library (libfa.so) for GB300 (sm_103a).
+ *
+ * What is computed (pages cited by title and section):
+ *   Forward  — "Flash Attention" tutorial, 1.FlashAttention 整体结构 一 and
+ *              2.Online Softmax §4.2: O = softmax(scale · Q Kᵀ) V computed one
+ *              K/V tile at a time with the online (m, ℓ) rescaling of §3.1 and
+ *              §4.1, normalised once at the end; the N×N score matrix never
+ *              reaches global memory.  The per-row statistic is the one of
+ *              3.Recomputation 三: LSE_i = m_i + ln ℓ_i.
+ *   Backward — same tutorial, 3.Recomputation 四 and 4.附录A
+ *              "反向传播的公式推导" 五-六: only O and LSE are kept; each tile of
+ *              P is rebuilt as exp(S - LSE); D = rowsum(dO ⊙ O);
+ *              dV = Pᵀ dO, dP = dO Vᵀ, dS = P ⊙ (dP - D), dQ = scale · dS K,
+ *              dK = scale · dSᵀ Q (the factor scale = 1/sqrt(d_k) on dQ and dK
+ *              as on the coreui.cn page "FlashAttention 反向传播").
+ *
+ * Conventions shared by every entry point:
+ *   Layout      Q, K, V, O, dO, dQ, dK, dV are dense row-major [B, H, N, d]
+ *               (d innermost, no padding).  LSE is dense [B, H, N] float32,
+ *               the natural-log log-sum-exp of row i of scale · Q Kᵀ over the
+ *               visible keys.  All pointers are DEVICE pointers.
+ *   dtype       FA_DTYPE_BF16: every [B,H,N,d] tensor is bfloat16; arithmetic
+ *               is fp32 accumulation on the tensor cores, P and dS are rounded
+ *               to bf16 before their products.  Supported: d ∈ {64, 128},
+ *               N a multiple of 128, base pointers 16-byte aligned.
+ *               FA_DTYPE_FP32: every tensor is float32 and computed with
+ *               fp32 arithmetic (no tensor cores); any N ≥ 1, 1 ≤ d ≤ 128.
+ *   causal      0: every key visible.  1: key j visible to query i iff j ≤ i
+ *               (square, top-left aligned; no row is ever empty).
+ *   scale       finite and > 0; callers usually pass 1/sqrt(d).
+ *   Empty       B, H or N equal to 0 is a valid empty problem: FA_OK, nothing
+ *               launched, pointers may be NULL.
+ *   Ownership   the caller owns every buffer.  The library allocates no device
+ *               or host memory.
+ *   Streams     every call only enqueues work on `stream` (NULL = legacy
+ *               default stream) and returns without synchronising.  Outputs
+ *               are fully overwritten.  Calls on different streams must not
+ *               share output or workspace buffers.
+ *   Errors      argument checks happen on the host before anything is
+ *               enqueued and return FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED,
+ *               FA_ERR_MISALIGNED or FA_ERR_WORKSPACE with no side effects.
+ *               A launch failure returns FA_ERR_CUDA.  Kernels never trap: a
+ *               pipeline wait that runs past its time limit records a fault
+ *               word and the kernel exits; fa_sync_status() reports it as
+ *               FA_ERR_TIMEOUT.  No exception crosses the ABI; nothing is
+ *               printed.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle; identical to cudaStream_t / CUstream. */
+typedef struct CUstream_st* fa_stream_t;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad scale/causal/dtype */
+  FA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (bf16 d∉{64,128}, N%128≠0, fp32 d>128) */
+  FA_ERR_MISALIGNED = 3,   /* bf16 base pointer not 16-byte aligned */
+  FA_ERR_WORKSPACE = 4,    /* workspace NULL, misaligned (256 B) or too small */
+  FA_ERR_CUDA = 5,         /* a CUDA runtime/driver call or launch failed */
+  FA_ERR_TIMEOUT = 6       /* a kernel abandoned a pipeline wait (see fa_sync_status) */
+} fa_status;
+
+typedef enum { FA_DTYPE_BF16 = 0, FA_DTYPE_FP32 = 1 } fa_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* fa_status_string(fa_status s);
+
+/* Library ABI version (major*100 + minor). */
+int fa_version(void);
+
+/*
+ * Forward.  Reads q, k, v; writes o [B,H,N,d] and lse [B,H,N] (float32).
+ * Cited: "Flash Attention" tutorial, 2.Online Softmax §4.2 (one pass over
+ * K/V tiles, deferred normalisation) and 3.Recomputation 三 (the saved L).
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, float scale, int causal,
+                 fa_dtype dtype, fa_stream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for this problem (0 for an empty
+ * one).  BF16: D and the base-2 LSE (4·B·H·N bytes each) plus a float32 dQ
+ * accumulator (4·B·H·N·d bytes), each part padded to 256 bytes.  FP32: D only.
+ * Pure host arithmetic; returns 0 for invalid arguments.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d, fa_dtype dtype);
+
+/*
+ * Backward.  Reads q, k, v, o, dO and the forward's lse; writes dq, dk, dv
+ * (same dtype and layout as q).  `workspace` is caller-owned device memory of
+ * at least fa_bwd_workspace_size() bytes, 256-byte aligned; its contents on
+ * entry do not matter and are clobbered.  The bf16 path accumulates dQ in
+ * float32 with reductions whose order varies, so dQ is not bitwise
+ * reproducible run to run; O, LSE, dK and dV are.
+ * Cited: "Flash Attention" tutorial, 4.附录A "反向传播的公式推导" 六 (tiled
+ * backward with the D precompute; here K/V tiles are the outer loop).
+ * Equivalent to fa_bwd_prep + fa_bwd_tiles + fa_bwd_dq_finish on one stream.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
+                 const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                 int B, int H, int N, int d, float scale, int causal,
+                 fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                 fa_stream_t stream);
+
+/*
+ * The three stages of fa_bwd, exposed so each can be timed on its own.  They
+ * must run in this order on one stream with the same workspace and sizes.
+ *   fa_bwd_prep      — "反向传播的公式推导" 五 (预处理): D_i = Σ_k dO_ik O_ik in
+ *                      float32, LSE converted to base 2, dQ accumulator zeroed.
+ *   fa_bwd_tiles     — the tiled loop of 六: recompute S and P per tile, then
+ *                      dV += Pᵀ dO, dP = dO Vᵀ, dS = P ⊙ (dP - D), dK += dSᵀ Q
+ *                      and dQ += dS K (into the accumulator); writes dk, dv.
+ *   fa_bwd_dq_finish — dQ = scale · accumulator, rounded to the output dtype.
+ * For FA_DTYPE_FP32, fa_bwd_tiles writes dq directly and fa_bwd_dq_finish is
+ * a no-op.
+ */
+fa_status fa_bwd_prep(const void* o, const void* dO, const float* lse,
+                      int B, int H, int N, int d, fa_dtype dtype,
+                      void* workspace, size_t workspace_bytes, fa_stream_t stream);
+fa_status fa_bwd_tiles(const void* q, const void* k, const void* v, const void* dO,
+                       void* dq, void* dk, void* dv,
+                       int B, int H, int N, int d, float scale, int causal,
+                       fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                       fa_stream_t stream);
+fa_status fa_bwd_dq_finish(void* dq, int B, int H, int N, int d, float scale,
+                           fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                           fa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reports and clears the kernels' fault words on
+ * the current device: FA_ERR_TIMEOUT if any kernel abandoned a pipeline wait
+ * since the last call, FA_ERR_CUDA if the stream reports an error, else FA_OK.
+ * The only entry point that blocks the host.
+ */
+fa_status fa_sync_status(fa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

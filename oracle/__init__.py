@@ -9,6 +9,7 @@ package imports nothing from the product package.
 from .attention import (  # noqa: F401
     attention_backward,
     attention_backward_head,
+    attention_backward_rows,
     attention_forward,
     attention_forward_head,
     attention_forward_rows,

@@ -260,6 +260,32 @@ def attention_backward_head(q, k, v, do, scale, causal=False, return_intermediat
     return dq, dk, dv
 
 
+def attention_backward_rows(q, k, v, do, rows, scale, causal=False):
+    """The backward restricted to a block of query rows of one head.
+
+    The loss Σ dO ⊙ O is a sum over query rows, so each row's contribution to
+    the gradients can be formed on its own with the same three steps as
+    ``attention_backward_head``: for the rows R, dV_R = P_Rᵀ dO_R and
+    dK_R = scale · dS_Rᵀ Q_R are those rows' (additive) shares of dV and dK,
+    and dQ_R = scale · dS_R K is exact.  Returns (dQ_R, dK_R, dV_R).  Used to
+    time a bounded sample of a large workload.
+    """
+    rows = np.asarray(rows)
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    qr, dor = q[rows], do[rows]
+    s = scale * (qr @ k.T)
+    if causal:
+        s = np.where(np.arange(k.shape[0])[None, :] <= rows[:, None], s, -np.inf)
+    p, _, _ = softmax_3pass(s)
+    dp, dv = matmul_backward(p, v, dor)
+    ds = softmax_backward(p, dp)
+    dq_u, dkt_u = matmul_backward(qr, k.T, ds)
+    return scale * dq_u, scale * dkt_u.T, dv
+
+
 # --------------------------------------------------------------------------
 # Batched wrappers over [B, H, N, d]
 # --------------------------------------------------------------------------

@@ -1,0 +1,69 @@
+"""Shared helpers for the parity tests: run the library, run the oracle, compare."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+# Tolerances (per tensor):
+#   fp32 dtype: every output within 1e-5 max abs of the fp64 oracle.
+#   bf16 dtype (fp32 accumulation): O max abs ≤ 1e-2, LSE max abs ≤ 1e-3,
+#   dQ / dK / dV relative Frobenius error ≤ 2e-2; no inf or NaN anywhere.
+FP32_ATOL = 1e-5
+BF16_O_ATOL = 1e-2
+BF16_LSE_ATOL = 1e-3
+BF16_GRAD_RTOL_FRO = 2e-2
+
+
+def to64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def run_library(q, k, v, do, causal, scale=None):
+    """fwd + bwd through the library on the inputs' device; returns CPU fp64 arrays."""
+    import exact_tiled_attention_12_gb300 as fa
+
+    o, lse = fa.fwd(q, k, v, scale=scale, causal=causal)
+    dq, dk, dv = fa.bwd(q, k, v, o, do, lse, scale=scale, causal=causal)
+    assert fa.sync_status(q.device) == 0
+    return {"O": to64(o), "LSE": to64(lse), "dQ": to64(dq), "dK": to64(dk), "dV": to64(dv)}
+
+
+def run_oracle_heads(q, k, v, do, causal, scale, heads):
+    """Oracle on the listed (b, h) heads; inputs are the exact values the GPU saw."""
+    out = {key: [] for key in ("O", "LSE", "dQ", "dK", "dV")}
+    for b, h in heads:
+        qh, kh, vh, doh = (to64(t[b, h]) for t in (q, k, v, do))
+        o, lse = oracle.attention_forward_head(qh, kh, vh, scale, causal)
+        dq, dk, dv = oracle.attention_backward_head(qh, kh, vh, doh, scale, causal)
+        for key, val in zip(("O", "LSE", "dQ", "dK", "dV"), (o, lse, dq, dk, dv)):
+            out[key].append(val)
+    return {key: np.stack(val) for key, val in out.items()}
+
+
+def select_heads(res, heads):
+    return {key: np.stack([val[b, h] for b, h in heads]) for key, val in res.items()}
+
+
+def rel_fro(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def compare(gpu, ref, dtype):
+    """Asserts the stated tolerances; returns the measured errors."""
+    errs = {}
+    for key in ("O", "LSE", "dQ", "dK", "dV"):
+        assert np.all(np.isfinite(gpu[key])), f"{key} has inf/NaN"
+        errs[key] = float(np.max(np.abs(gpu[key] - ref[key]))) if gpu[key].size else 0.0
+    if dtype == "fp32":
+        for key, e in errs.items():
+            assert e <= FP32_ATOL, (key, e)
+    else:
+        assert errs["O"] <= BF16_O_ATOL, errs
+        assert errs["LSE"] <= BF16_LSE_ATOL, errs
+        for key in ("dQ", "dK", "dV"):
+            errs[key + "_relfro"] = rel_fro(gpu[key], ref[key])
+            assert errs[key + "_relfro"] <= BF16_GRAD_RTOL_FRO, (key, errs)
+    return errs

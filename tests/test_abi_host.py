@@ -1,0 +1,91 @@
+"""Host-side checks of the C ABI: the library builds and loads, exports every
+function include/fa.h declares with the documented signatures, and rejects
+invalid arguments before touching the GPU (these calls need no device)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import exact_tiled_attention_12_gb300 as fa
+
+    return fa.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text))
+
+
+def test_header_declares_the_expected_entry_points():
+    assert _declared() >= {"fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_status_string", "fa_version",
+                           "fa_bwd_prep", "fa_bwd_tiles", "fa_bwd_dq_finish", "fa_sync_status"}
+
+
+def test_library_exports_every_declared_symbol(L):
+    from exact_tiled_attention_12_gb300.binding import SIGNATURES
+
+    for name in _declared():
+        assert hasattr(L, name), name
+        assert name in SIGNATURES, name
+
+
+def test_status_strings(L):
+    for code in range(7):
+        s = L.fa_status_string(code).decode()
+        assert s.startswith("FA_")
+    assert L.fa_version() == 100
+
+
+def test_workspace_size(L):
+    # bf16: D and LSE2 (4 bytes per row each, padded to 256) + fp32 dQ accumulator
+    rows, elems = 4 * 32 * 2048, 4 * 32 * 2048 * 128
+    assert L.fa_bwd_workspace_size(4, 32, 2048, 128, 0) == 2 * rows * 4 + elems * 4
+    assert L.fa_bwd_workspace_size(1, 1, 3, 64, 1) == 2 * 256
+    assert L.fa_bwd_workspace_size(0, 1, 128, 64, 0) == 0
+    assert L.fa_bwd_workspace_size(-1, 1, 128, 64, 0) == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)       # 16-byte aligned, never dereferenced
+ODD = ctypes.c_void_p(0x10008)        # 8-byte aligned only
+
+
+def _fwd(L, ptr=FAKE, B=1, H=1, N=128, d=128, scale=0.1, causal=0, dtype=0):
+    return L.fa_fwd(ptr, FAKE, FAKE, FAKE, FAKE, B, H, N, d, scale, causal, dtype, None)
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(B=-1), 1), (dict(N=-5), 1), (dict(d=0), 1), (dict(scale=0.0), 1), (dict(scale=-1.0), 1),
+    (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1), (dict(causal=2), 1), (dict(dtype=7), 1),
+    (dict(ptr=ctypes.c_void_p(0)), 1),
+    (dict(N=200), 2), (dict(d=96), 2), (dict(d=256, dtype=1), 2),
+    (dict(ptr=ODD), 3),
+    (dict(N=0), 0), (dict(B=0, ptr=ctypes.c_void_p(0)), 0),
+])
+def test_forward_argument_checks(L, kwargs, code):
+    assert _fwd(L, **kwargs) == code
+
+
+def test_backward_argument_checks(L):
+    args = [FAKE] * 9 + [1, 1, 128, 64, 0.125, 0, 0]
+    # workspace missing, misaligned, too small
+    assert L.fa_bwd(*args, None, 0, None) == 4
+    assert L.fa_bwd(*args, ctypes.c_void_p(0x10010), 1 << 20, None) == 4
+    assert L.fa_bwd(*args, ctypes.c_void_p(0x10000), 16, None) == 4
+    # misaligned input checked before the workspace
+    bad = [ODD] + [FAKE] * 8 + [1, 1, 128, 64, 0.125, 0, 0]
+    assert L.fa_bwd(*bad, None, 0, None) == 3
+    # stage entry points share the same checks
+    assert L.fa_bwd_prep(FAKE, FAKE, FAKE, 1, 1, 128, 64, 0, None, 0, None) == 4
+    assert L.fa_bwd_tiles(*([FAKE] * 7), 1, 1, 128, 64, 0.125, 0, 0, None, 0, None) == 4
+    assert L.fa_bwd_dq_finish(FAKE, 1, 1, 100, 64, 0.125, 0, None, 0, None) == 2

@@ -1,0 +1,177 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Shapes span several tiles, an odd number of 128-row tiles (a half-empty
+two-tile CTA), single-tile heads and both masks; the fp32 dtype also covers
+ragged N and d.  Tolerances are in tests/_helpers.py.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from exact_tiled_attention_12_gb300.synthetic import WORKLOADS, make_inputs, make_workload_inputs
+
+from ._helpers import compare, run_library, run_oracle_heads, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+
+def _all_heads(B, H):
+    return [(b, h) for b in range(B) for h in range(H)]
+
+
+def _check(B, H, N, d, causal, dtype, dist="normal", seed=7):
+    q, k, v, do = make_inputs(B, H, N, d, dtype, dist, seed, device="cuda")
+    scale = d ** -0.5
+    gpu = run_library(q, k, v, do, causal, scale)
+    heads = _all_heads(B, H)
+    ref = run_oracle_heads(q, k, v, do, causal, scale, heads)
+    flat = {key: val.reshape((-1,) + val.shape[2:]) for key, val in gpu.items()}
+    return compare(flat, ref, dtype)
+
+
+# ------------------------------------------------------------------ fp32 dtype
+
+
+def test_tiny_fp32_workload():
+    """The tiny fp32 workload (1 x 1 x 256 x 64, non-causal) within 1e-5."""
+    w = WORKLOADS["tiny_fp32"]
+    q, k, v, do = make_workload_inputs(w, device="cuda")
+    gpu = run_library(q, k, v, do, w.causal, w.scale)
+    ref = run_oracle_heads(q, k, v, do, w.causal, w.scale, [(0, 0)])
+    compare({key: val[0:1, 0] for key, val in gpu.items()}, ref, "fp32")
+
+
+@pytest.mark.parametrize("B,H,N,d", [(1, 1, 256, 64), (2, 3, 77, 40), (1, 2, 200, 128), (1, 1, 1, 1), (1, 1, 33, 127)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp32_parity(B, H, N, d, causal):
+    _check(B, H, N, d, causal, "fp32", seed=B * 1000 + N + d)
+
+
+# ------------------------------------------------------------------ bf16 dtype (tensor cores)
+
+BF16_SHAPES = [
+    (1, 2, 256, 128),   # one two-tile CTA per head
+    (2, 3, 384, 64),    # three tiles: the second CTA's upper tile is past N
+    (1, 1, 128, 128),   # a single tile
+    (1, 1, 128, 64),
+    (1, 2, 1024, 128),  # several K/V stages and ring wrap-around
+    (3, 2, 640, 64),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d", BF16_SHAPES)
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_parity(B, H, N, d, causal):
+    _check(B, H, N, d, causal, "bf16", seed=B * 1000 + N + d + int(causal))
+
+
+def test_bf16_stress_small():
+    """Scores scaled to magnitudes in the hundreds (Q, K drawn ×8, d = 64)."""
+    errs = _check(2, 2, 512, 64, False, "bf16", dist="stress", seed=5)
+    assert errs["O"] <= 1e-2
+
+
+# ------------------------------------------------------------------ closed forms on the GPU
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_constant_v(d, causal):
+    """Rows of P sum to one: V_j = c gives O_i = c to within one bf16 ulp of |c|."""
+    import exact_tiled_attention_12_gb300 as fa
+
+    q, k, _, _ = make_inputs(1, 2, 512, d, "bf16", "normal", 11, device="cuda")
+    c = torch.linspace(-3, 3, d, dtype=torch.float32).to(torch.bfloat16)
+    v = c.view(1, 1, 1, d).expand(1, 2, 512, d).contiguous().cuda()
+    o, _ = fa.fwd(q, k, v, causal=causal)
+    cf = c.double().abs()
+    ulp = torch.where(cf > 0, torch.exp2(torch.floor(torch.log2(cf.clamp_min(1e-30))) - 7), torch.zeros_like(cf))
+    err = (o.double().cpu() - c.double().view(1, 1, 1, d)).abs()
+    assert bool((err <= ulp.view(1, 1, 1, d) + 1e-12).all()), float(err.max())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_identical_keys(causal):
+    """K_j = k for all j: P is uniform over visible keys, O_i = mean of visible V_j."""
+    import exact_tiled_attention_12_gb300 as fa
+
+    q, _, v, _ = make_inputs(1, 1, 384, 128, "bf16", "normal", 12, device="cuda")
+    k = make_inputs(1, 1, 1, 128, "bf16", "normal", 13, device="cuda")[0].expand(1, 1, 384, 128).contiguous()
+    o, lse = fa.fwd(q, k, v, causal=causal)
+    vv = to64(v[0, 0])
+    want = np.cumsum(vv, axis=0) / np.arange(1, 385)[:, None] if causal else np.tile(vv.mean(axis=0), (384, 1))
+    assert np.max(np.abs(to64(o[0, 0]) - want)) <= 1e-2
+
+
+def test_bf16_gradient_invariants():
+    """Σ_j dK_j = 0 and Σ_j dV_j = Σ_i dO_i, relative to the gradients' size."""
+    q, k, v, do = make_inputs(2, 2, 512, 128, "bf16", "normal", 14, device="cuda")
+    for causal in (False, True):
+        g = run_library(q, k, v, do, causal)
+        for b in range(2):
+            for h in range(2):
+                dk, dv, dov = g["dK"][b, h], g["dV"][b, h], to64(do[b, h])
+                assert np.linalg.norm(dk.sum(axis=0)) <= 2e-2 * np.linalg.norm(dk)
+                assert np.linalg.norm(dv.sum(axis=0) - dov.sum(axis=0)) <= 2e-2 * np.linalg.norm(dv)
+
+
+# ------------------------------------------------------------------ API behaviour
+
+
+def test_bf16_forward_and_dkdv_are_deterministic():
+    import exact_tiled_attention_12_gb300 as fa
+
+    q, k, v, do = make_inputs(1, 2, 512, 128, "bf16", "normal", 15, device="cuda")
+    o1, l1 = fa.fwd(q, k, v)
+    o2, l2 = fa.fwd(q, k, v)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    g1 = fa.bwd(q, k, v, o1, do, l1)
+    g2 = fa.bwd(q, k, v, o1, do, l1)
+    assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
+    assert float((g1[0].float() - g2[0].float()).abs().max()) <= 1e-2
+
+
+def test_stage_api_matches_fa_bwd():
+    import exact_tiled_attention_12_gb300 as fa
+
+    q, k, v, do = make_inputs(1, 2, 512, 64, "bf16", "normal", 16, device="cuda")
+    o, lse = fa.fwd(q, k, v, causal=True)
+    dq, dk, dv = fa.bwd(q, k, v, o, do, lse, causal=True)
+    ws = torch.empty(fa.bwd_workspace_size(1, 2, 512, 64), dtype=torch.uint8, device="cuda")
+    dq2, dk2, dv2 = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    fa.bwd_stages(q, k, v, o, do, lse, dq2, dk2, dv2, ws, causal=True)
+    assert fa.sync_status() == 0
+    assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    assert float((dq.float() - dq2.float()).abs().max()) <= 1e-2
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_empty_problems(dtype):
+    import exact_tiled_attention_12_gb300 as fa
+
+    for shape in [(1, 1, 0, 64), (0, 2, 128, 64), (1, 0, 128, 64)]:
+        q, k, v, do = make_inputs(*shape, dtype, "normal", 1, device="cuda")
+        o, lse = fa.fwd(q, k, v)
+        dq, dk, dv = fa.bwd(q, k, v, o, do, lse)
+        assert o.shape == q.shape and lse.shape == shape[:3] and dq.shape == q.shape
+    assert fa.sync_status() == 0
+
+
+def test_unsupported_shapes_raise():
+    import exact_tiled_attention_12_gb300 as fa
+
+    for shape in [(1, 1, 200, 128), (1, 1, 256, 96)]:
+        q, k, v, _ = make_inputs(*shape, "bf16", "normal", 1, device="cuda")
+        with pytest.raises(fa.FaError) as e:
+            fa.fwd(q, k, v)
+        assert e.value.code == 2

@@ -17,6 +17,7 @@ import pytest
 
 from oracle import (
     attention_backward_head,
+    attention_backward_rows,
     attention_forward_head,
     attention_forward_rows,
     causal_mask,
@@ -381,3 +382,21 @@ def test_finite_difference_gradients(causal, n):
                 fd[i, t] = (up - dn) / (2 * h)
         err = np.linalg.norm(fd - g) / max(np.linalg.norm(g), 1e-30)
         assert err <= 1e-6, (which, err)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_block_backward_sums_to_full(causal):
+    """Row blocks of the backward: dQ rows are exact and the dK, dV shares of a
+    partition of the rows add up to the full gradients."""
+    rng = _rng(27)
+    n, d = 48, 8
+    q, k, v, do = (rng.normal(size=(n, d)) for _ in range(4))
+    dq, dk, dv = attention_backward_head(q, k, v, do, 0.4, causal)
+    dk_sum, dv_sum = np.zeros_like(dk), np.zeros_like(dv)
+    for block in (np.arange(0, 5), np.arange(5, 31), np.arange(31, 48)):
+        dq_r, dk_r, dv_r = attention_backward_rows(q, k, v, do, block, 0.4, causal)
+        np.testing.assert_allclose(dq_r, dq[block], atol=1e-14, rtol=0)
+        dk_sum += dk_r
+        dv_sum += dv_r
+    np.testing.assert_allclose(dk_sum, dk, atol=1e-13, rtol=0)
+    np.testing.assert_allclose(dv_sum, dv, atol=1e-13, rtol=0)

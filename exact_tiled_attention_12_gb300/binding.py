@@ -34,6 +34,7 @@ SIGNATURES = {
     "fa_bwd_tiles": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P, _Z, _P]),
     "fa_bwd_dq_finish": (_I, [_P, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
     "fa_sync_status": (_I, [_P]),
+    "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P]),
 }
 
 

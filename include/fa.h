@@ -142,6 +142,37 @@ fa_status fa_bwd_dq_finish(void* dq, int B, int H, int N, int d, float scale,
  */
 fa_status fa_sync_status(fa_stream_t stream);
 
+/*
+ * Size of the scratch array compiled into libfa.so for fa_bwd_noalloc:
+ * 32 MiB, held on every GPU that loads the library until the process exits.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * Backward without a workspace argument.  The pages have no counterpart to
+ * this entry point; it exists for callers that cannot allocate device memory
+ * (for example a runtime that forbids allocation after start-up, or a plug-in
+ * whose host owns every device allocation).  Same arguments, results and
+ * errors as fa_bwd, except that the scratch comes from a fixed array inside
+ * the library instead of the caller:
+ *   - nothing is allocated, by this call or by anything it calls;
+ *   - problems whose fa_bwd_workspace_size() exceeds FA_NOALLOC_SCRATCH_BYTES
+ *     are rejected with FA_ERR_WORKSPACE before anything is enqueued (for
+ *     bf16 that is 4·B·H·N·(d + 2) bytes plus padding, e.g. B·H·N up to
+ *     about 64,000 rows at d = 128);
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current and caches it; make
+ *     that first call before any stream capture begins;
+ *   - every call on a device shares the one array and it keeps the last
+ *     call's contents (the pre-pass rewrites what must start at zero), so
+ *     calls whose work can overlap on the GPU — on different streams, or from
+ *     different host threads — race and must not be issued.
+ */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                         int B, int H, int N, int d, float scale, int causal,
+                         fa_dtype dtype, fa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

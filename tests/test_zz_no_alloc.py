@@ -1,0 +1,78 @@
+"""fa_bwd_noalloc: the backward for callers that cannot allocate device memory.
+
+Such callers (a runtime that forbids allocation after start-up, a plug-in whose
+host owns every device allocation) cannot hand fa_bwd a workspace, so this
+entry point uses a fixed scratch array compiled into the library.  The test
+calls it through the C ABI twice in a row, with different inputs, and checks
+each result against fa_bwd with a caller-provided workspace, within the
+tolerances the other tests use: dK and dV are reproducible bit for bit, dQ
+(float32 reductions in varying order) within 1e-2.  It also checks that a
+problem larger than the built-in scratch is refused.  This file sorts last so
+that a run stopping at the first failure has already run every other test.
+"""
+
+import ctypes
+
+import pytest
+import torch
+
+from exact_tiled_attention_12_gb300.synthetic import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+SCRATCH_BYTES = 32 << 20   # FA_NOALLOC_SCRATCH_BYTES in include/fa.h
+
+
+@pytest.fixture(scope="module")
+def fa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import exact_tiled_attention_12_gb300 as fa
+
+    return fa
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _noalloc(fa, q, k, v, o, do, lse, causal):
+    B, H, N, d = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    code = 0 if q.dtype == torch.bfloat16 else 1
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    st = fa.lib().fa_bwd_noalloc(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(dq), _p(dk), _p(dv),
+                                 B, H, N, d, d ** -0.5, int(causal), code, stream)
+    assert st == 0, fa.status_string(st)
+    assert fa.sync_status() == 0
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("dtype,shape,causal", [
+    ("bf16", (1, 2, 512, 128), True),
+    ("bf16", (2, 2, 384, 64), False),
+    ("fp32", (1, 2, 200, 64), True),
+])
+def test_noalloc_matches_fa_bwd_twice(fa, dtype, shape, causal):
+    for seed in (21, 22):   # two calls in a row; the second sees the first's leftovers
+        q, k, v, do = make_inputs(*shape, dtype, "normal", seed, device="cuda")
+        o, lse = fa.fwd(q, k, v, causal=causal)
+        want = fa.bwd(q, k, v, o, do, lse, causal=causal)
+        got = _noalloc(fa, q, k, v, o, do, lse, causal)
+        if dtype == "bf16":
+            assert torch.equal(got[1], want[1]) and torch.equal(got[2], want[2])
+            assert float((got[0].float() - want[0].float()).abs().max()) <= 1e-2
+        else:
+            for g, w_ in zip(got, want):
+                assert float((g - w_).abs().max()) <= 1e-5
+
+
+def test_noalloc_rejects_problems_beyond_the_scratch(fa):
+    B, H, N, d = 1, 16, 4096, 128
+    assert fa.bwd_workspace_size(B, H, N, d) > SCRATCH_BYTES
+    fake = ctypes.c_void_p(0x10000)
+    st = fa.lib().fa_bwd_noalloc(*([fake] * 9), B, H, N, d, d ** -0.5, 0, 0, None)
+    assert st == 4   # FA_ERR_WORKSPACE, returned before anything is enqueued

@@ -188,9 +188,10 @@ def run_ours(args, w, rank, world):
 
     # End to end through the public API: pinned host inputs copied in, results
     # (O, LSE, dQ, dK, dV) copied back, every step.
-    hq, hk, hv, hdo = (t.to("cpu").pin_memory() for t in (q, k, v, do))
-    ho, hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(4))
-    hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    hq, hk, hv, hdo = (t.to("cpu").pin_memory() for t in (q, k, v, do)) if not args.no_e2e else (q, k, v, do)
+    pin = (lambda t: t.pin_memory()) if not args.no_e2e else (lambda t: t)
+    ho, hdq, hdk, hdv = (pin(torch.empty(q.shape, dtype=q.dtype)) for _ in range(4))
+    hlse = pin(torch.empty(lse.shape, dtype=torch.float32))
     dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
 
     def e2e_step():
@@ -206,7 +207,9 @@ def run_ours(args, w, rank, world):
             h_.copy_(t_, non_blocking=True)
 
     n_e2e = max(3, min(args.steps, 10))
-    e2e_step()
+    if args.no_e2e:
+        n_e2e = 0
+    e2e_step() if n_e2e else None
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -214,7 +217,7 @@ def run_ours(args, w, rank, world):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    e2e_ms = e0.elapsed_time(e1) / max(n_e2e, 1) if n_e2e else float("nan")
     elem_bytes = q.numel() * q.element_size()
     e2e = {"value": round(world * (flops_fwd + flops_bwd) / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
            "h2d_bytes_per_step": 4 * elem_bytes, "d2h_bytes_per_step": 4 * elem_bytes + lse.numel() * 4,
@@ -331,6 +334,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

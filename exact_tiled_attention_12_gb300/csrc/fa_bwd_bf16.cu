@@ -7,22 +7,30 @@
 // dK += dSᵀ Q and dQ += dS K.  The scale of the scores multiplies dQ and dK
 // (coreui.cn page "FlashAttention 反向传播", dQ = dS K / sqrt(d_k)).
 //
-// Loop order differs from the page's pseudocode (query tiles outermost): here
-// a CTA owns one 128-row K/V tile and walks the query tiles, so dK and dV
+// Loop order differs from the page's pseudocode (query tiles outermost): a CTA
+// owns one 128-row K/V tile and walks the 128-row query tiles, so dK and dV
 // accumulate in tensor memory and only dQ is shared between CTAs (fp32
-// reductions into a workspace accumulator).  The sums are the same.
+// vector reductions into a workspace accumulator).  The sums are the same.
 //
-// Everything is computed transposed relative to the page (rows = keys):
-//   Sᵀ = K Qᵀ, dPᵀ = V dOᵀ   (tcgen05, M = 128 keys, N = BM queries)
-//   Pᵀ = exp2(Sᵀ·scale·log2e - LSE2), dSᵀ = Pᵀ ⊙ (dPᵀ - D)   (one thread per key row)
-//   dV += Pᵀ dO, dK += dSᵀ Q   (A = Pᵀ / dSᵀ from shared memory, M = 128 keys)
-//   d = 128: dQᵀ = Kᵀ dSᵀ (M = 128 head dims, N = 64 queries)
-//   d = 64:  dQ  = dS K   (M = 128 queries, N = 64 head dims)
+// Per query tile (rows = keys for the first four, rows = queries for dQ):
+//   Sᵀ  = K Qᵀ        tcgen05, A = K (smem), B = Q (smem), both K-major
+//   dPᵀ = V dOᵀ       same with V and dO
+//   Pᵀ  = exp2(Sᵀ·scale·log2e − LSE₂), dSᵀ = Pᵀ ⊙ (dPᵀ − D)   one thread per key row
+//   dV += Pᵀ dO       A = Pᵀ from tensor memory (written over Sᵀ), B = dO (MN-major)
+//   dK += dSᵀ Q       A = dSᵀ (smem, K-major over queries), B = Q (MN-major)
+//   dQ                d = 128: dQᵀ = Kᵀ dSᵀ (M = head dims, N = queries);
+//                     d = 64:  dQ = dS K (M = queries, N = head dims);
+//                     both read the dSᵀ tile and K MN-major from smem
+// Every product is M = 128 with N ≥ 64 (N = 128 except dV, dK, dQ at d = 64).
 //
-// CTA: 14 warps.  Warps 0-7 compute Pᵀ/dSᵀ (warp w owns key rows 32(w%4).. and
-// half w/4 of the query columns), warps 8-11 drain dQ from tensor memory into
-// the fp32 accumulator with vector reductions, warp 12 issues TMA, warp 13
-// issues the MMAs and owns tensor memory.
+// Tensor memory (512 columns): dV [0, d), dK [d, 2d), Sᵀ/Pᵀ [2d, 2d+128),
+// dPᵀ/dQ [2d+128, 2d+256).  dQ reuses the dPᵀ columns once the compute warps
+// have read dPᵀ; the next dPᵀ waits until dQ has been drained.
+//
+// CTA: 10 warps.  Warps 0-7 compute Pᵀ/dSᵀ (warp w owns key rows 32(w%4)..+31
+// and query columns 64(w/4)..+63) and then drain that tile's dQ from tensor
+// memory into the fp32 accumulator; warp 8 issues TMA, warp 9 issues the MMAs and
+// owns tensor memory.  The grid is head-major (K/V tile fastest).
 #include "fa_kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -30,61 +38,65 @@ namespace fa {
 namespace {
 
 constexpr int kBN = 128;            // keys per CTA
-constexpr int kThreads = 448;
+constexpr int kBM = 128;            // queries per step
+constexpr int kThreads = 320;
 constexpr int kComputeWarps = 8;
-constexpr int kDrainWarp0 = 8;
-constexpr int kTmaWarp = 12;
-constexpr int kMmaWarp = 13;
-constexpr int kBox = 16384;         // 128 rows × 128 bytes
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kBox = 16384;         // one TMA box: 128 rows × 128 bytes
 
 template <int D>
 struct BwdCfg {
-  static constexpr int BM = D == 128 ? 64 : 128;  // queries per step
-  static constexpr int NDP = D == 128 ? 2 : 1;    // dPᵀ buffers in tensor memory
-  // shared memory
-  static constexpr int kKV = kBN * D * 2;          // one K (or V) tile
-  static constexpr int kQT = BM * D * 2;           // one Q (or dO) tile
-  static constexpr int kQBox = BM * 128;           // one 64-column box of a Q tile
-  static constexpr int kPT = kBN * BM * 2;         // one Pᵀ (or dSᵀ) tile
+  // shared memory (offsets from a 1024-byte aligned base)
+  static constexpr int kTile = 128 * D * 2;        // one 128 × D bf16 tile (D/64 boxes)
   static constexpr int kK = 0;
-  static constexpr int kV = kK + kKV;
-  static constexpr int kQ = kV + kKV;              // 2 stages
-  static constexpr int kDO = kQ + 2 * kQT;         // 2 stages
-  static constexpr int kP = kDO + 2 * kQT;         // 2 buffers
-  static constexpr int kDS = kP + 2 * kPT;         // 2 buffers
-  static constexpr int kLSE = kDS + 2 * kPT;       // 2 stages of BM floats
-  static constexpr int kDV = kLSE + 2 * BM * 4;    // 2 stages of BM floats
-  static constexpr int kBar = kDV + 2 * BM * 4;
+  static constexpr int kV = kK + kTile;
+  static constexpr int kQ = kV + kTile;            // 2 stages
+  static constexpr int kDO = kQ + 2 * kTile;       // 2 stages
+  static constexpr int kDS = kDO + 2 * kTile;      // dSᵀ [128 keys][128 queries] bf16: 2 boxes
+  static constexpr int kLSE = kDS + 2 * kBox;      // 2 stages of 128 floats
+  static constexpr int kDV = kLSE + 2 * kBM * 4;   // 2 stages of 128 floats
+  static constexpr int kBar = kDV + 2 * kBM * 4;
   static constexpr int kBytes = kBar + 256;
   // tensor memory columns
   static constexpr uint32_t kColDV = 0;
   static constexpr uint32_t kColDK = D;
-  static constexpr uint32_t col_s(int b) { return 2 * D + b * BM; }
-  static constexpr uint32_t col_dp(int b) { return 2 * D + 2 * BM + (b % NDP) * BM; }
+  static constexpr uint32_t kColS = 2 * D;
+  static constexpr uint32_t kColDP = 2 * D + 128;
 };
 
 enum BwdBar : int {
   kKVFull = 0,
-  kQFull = 1,       // +stage
-  kQEmpty = 3,      // +stage
-  kSFull = 5,       // +buffer
-  kDPFull = 7,      // +buffer
-  kTmUsed = 9,      // +buffer: compute threads have read Sᵀ and dPᵀ
-  kPdsFull = 11,    // +buffer
-  kPdsEmpty = 13,   // +buffer
-  kDqFull = 15,     // +buffer
-  kDqDrained = 17,  // +buffer
-  kDKVFull = 19,
-  kMmaDone = 20,
-  kNumBars = 21,
+  kQFull = 1,      // +stage
+  kQEmpty = 3,     // +stage
+  kSFull = 5,
+  kDPFull = 6,
+  kPdsFull = 7,
+  kDqFull = 8,
+  kDqDrained = 9,
+  kDKVFull = 10,
+  kMmaDone = 11,
+  kNumBars = 12,
 };
 
 __device__ __forceinline__ uint32_t site(int s) { return 0x0200u | (uint32_t)s; }
 
+// Barrier among the two compute warps that share a TMEM lane quarter, with an
+// AND over their `ok` flags so both take the same branch.
+__device__ __forceinline__ bool pair_sync_and(int id, bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n bar.red.and.pred q, %2, 64, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)ok), "r"(id)
+      : "memory");
+  return r != 0;
+}
+
 template <int D, bool CAUSAL>
+// 10 warps: at most 3 per SM sub-partition, so up to 168 registers a thread.
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_constant__ BwdArgs a) {
   using C = BwdCfg<D>;
-  constexpr int BM = C::BM;
   // Dynamic shared memory starts on a 1024-byte boundary (no static shared
   // memory is declared); 128-byte swizzled tiles need that alignment.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -103,26 +115,27 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int N = a.N;
-  const int bh = blockIdx.x;
-  const int jt = blockIdx.y;                 // K/V tile; small jt = most work when causal
+  // Non-causal: head-major grid (K/V tile fastest), so a wave touches few
+  // heads' Q, dO and dQ accumulator and they stay in L2.  Causal: batch·head
+  // fastest, so the heaviest tiles (small jt) of every head go first.
+  const int jt = CAUSAL ? (int)blockIdx.y : (int)blockIdx.x;
+  const int bh = CAUSAL ? (int)blockIdx.x : (int)blockIdx.y;
   const int kv0 = jt * kBN;
   const int row0 = bh * N;
-  const int i0 = CAUSAL ? kv0 / BM : 0;      // first query tile with a visible query
-  const int n = N / BM - i0;                 // query tiles visited
+  const int i0 = CAUSAL ? jt : 0;            // first query tile with a visible query (kBM == kBN)
+  const int n = N / kBM - i0;                // query tiles visited
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kKVFull), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kQFull + s), 1);
       mbar_init(bar(kQEmpty + s), 1 + 32 * kComputeWarps);
-      mbar_init(bar(kSFull + s), 1);
-      mbar_init(bar(kDPFull + s), 1);
-      mbar_init(bar(kTmUsed + s), 32 * kComputeWarps);
-      mbar_init(bar(kPdsFull + s), 32 * kComputeWarps);
-      mbar_init(bar(kPdsEmpty + s), 1);
-      mbar_init(bar(kDqFull + s), 1);
-      mbar_init(bar(kDqDrained + s), 128);
     }
+    mbar_init(bar(kSFull), 1);
+    mbar_init(bar(kDPFull), 1);
+    mbar_init(bar(kPdsFull), 32 * kComputeWarps);
+    mbar_init(bar(kDqFull), 1);
+    mbar_init(bar(kDqDrained), 32 * kComputeWarps);
     mbar_init(bar(kDKVFull), 1);
     mbar_init(bar(kMmaDone), 1);
     *abort_flag = 0;
@@ -140,66 +153,125 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
   if (warp < kComputeWarps) {
     // ------------------------------------------------------------ Pᵀ, dSᵀ
     const int g = warp & 3;
-    const int h = warp >> 2;                       // query-column half
+    const int h = warp >> 2;                       // query columns [64h, 64h + 64)
     const int r = g * 32 + lane;                   // key row within the tile = TMEM lane
     const int kv = kv0 + r;
     const uint32_t lane_off = (uint32_t)(g * 32) << 16;
-    constexpr int CW = BM / 2;                     // query columns per thread
     const float sl2 = a.scale_log2;
+    const uint32_t ds_tile = sbase + C::kDS;
     bool ok = true;
     for (int i = 0; i < n; ++i) {
-      const int b = i & 1;
-      const uint32_t par = (uint32_t)((i >> 1) & 1);
-      const int q0 = (i0 + i) * BM;
-      ok = mbar_wait(bar(kSFull + b), par, wc, site(1)) && mbar_wait(bar(kDPFull + b), par, wc, site(2)) &&
-           mbar_wait(bar(kQFull + b), par, wc, site(3)) &&
-           (i < 2 || mbar_wait(bar(kPdsEmpty + b), (uint32_t)(((i >> 1) - 1) & 1), wc, site(4)));
+      const int st = i & 1;
+      const uint32_t par = (uint32_t)(i & 1);
+      const int q0 = (i0 + i) * kBM;
+      ok = mbar_wait(bar(kSFull), par, wc, site(1)) && mbar_wait(bar(kDPFull), par, wc, site(2)) &&
+           mbar_wait(bar(kQFull + st), (uint32_t)((i >> 1) & 1), wc, site(3));
+      ok = __all_sync(kFull, ok);
+      const float* lse2 = reinterpret_cast<const float*>(sgen + C::kLSE + st * kBM * 4);
+      const float* dvec = reinterpret_cast<const float*>(sgen + C::kDV + st * kBM * 4);
+      const bool masked = CAUSAL && i == 0;        // the diagonal tile (q0 == kv0)
+      float p[64];
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          const int c0 = h * 64 + ch * 32;
+          uint32_t s[32];
+          tmem_ld_x32(tmem + lane_off + C::kColS + (uint32_t)c0, s);
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c0 + e);
+            p[ch * 32 + e + 0] = ex2(fmaf(u2f(s[e + 0]), sl2, -l4.x));
+            p[ch * 32 + e + 1] = ex2(fmaf(u2f(s[e + 1]), sl2, -l4.y));
+            p[ch * 32 + e + 2] = ex2(fmaf(u2f(s[e + 2]), sl2, -l4.z));
+            p[ch * 32 + e + 3] = ex2(fmaf(u2f(s[e + 3]), sl2, -l4.w));
+          }
+          if (masked) {
+            // key kv is visible to query q iff kv ≤ q
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (r > c0 + e) p[ch * 32 + e] = 0.f;
+          }
+        }
+      }
+      // Both warps of the lane quarter have read their Sᵀ columns; Pᵀ may now
+      // be written over the first 64 of them.
+      ok = pair_sync_and(1 + g, ok);
+      if (!ok) break;
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
+        uint32_t lo[16], hi[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          lo[e] = pk[e];
+          hi[e] = pk[16 + e];
+        }
+        tmem_st_x16(tmem + lane_off + C::kColS + (uint32_t)(h * 32), lo);
+        tmem_st_x16(tmem + lane_off + C::kColS + (uint32_t)(h * 32 + 16), hi);
+      }
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c0 = h * 64 + ch * 32;
+        uint32_t dp[32];
+        tmem_ld_x32(tmem + lane_off + C::kColDP + (uint32_t)c0, dp);
+        uint32_t dk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(dvec + c0 + e);
+          const float d0 = p[ch * 32 + e + 0] * (u2f(dp[e + 0]) - d4.x);
+          const float d1 = p[ch * 32 + e + 1] * (u2f(dp[e + 1]) - d4.y);
+          const float d2 = p[ch * 32 + e + 2] * (u2f(dp[e + 2]) - d4.z);
+          const float d3 = p[ch * 32 + e + 3] * (u2f(dp[e + 3]) - d4.w);
+          dk[(e >> 1) + 0] = pack_bf16x2(d0, d1);
+          dk[(e >> 1) + 1] = pack_bf16x2(d2, d3);
+        }
+        // 32 query columns = four 16-byte chunks of this key row, in box h
+        // (queries 64h..64h+63), placed with the 128-byte swizzle.
+        const uint32_t row_addr = ds_tile + (uint32_t)(h * kBox + r * 128);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int chunk = ch * 4 + u;
+          st_shared_v4(row_addr + (uint32_t)(((chunk ^ (r & 7)) & 7) * 16), dk[4 * u], dk[4 * u + 1], dk[4 * u + 2],
+                       dk[4 * u + 3]);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      fence_proxy_async_smem();
+      mbar_arrive(bar(kPdsFull));
+      mbar_arrive(bar(kQEmpty + st));
+
+      // dQ of this tile: the MMA thread issues it first after Pᵀ/dSᵀ, and the
+      // next Sᵀ/dPᵀ arrive only after dQ, dV and dK, so these warps are free
+      // to drain it.  Each thread reads its share into registers, releases the
+      // columns, then adds into the fp32 accumulator with global reductions.
+      ok = mbar_wait(bar(kDqFull), par, wc, site(6));
       ok = __all_sync(kFull, ok);
       if (!ok) break;
       tc_fence_after();
-      const float* lse2 = reinterpret_cast<const float*>(sgen + C::kLSE + b * BM * 4);
-      const float* dvec = reinterpret_cast<const float*>(sgen + C::kDV + b * BM * 4);
-      const bool masked = CAUSAL && q0 < kv0 + kBN;   // tile straddles the diagonal
-      const uint32_t p_tile = sbase + C::kP + b * C::kPT;
-      const uint32_t ds_tile = sbase + C::kDS + b * C::kPT;
+      if constexpr (D == 128) {
+        // dQᵀ: lane = head dim, columns = queries [64h, 64h + 64); a warp's
+        // reduction covers 32 consecutive floats of one accumulator row.
+        uint32_t v[64];
+        tmem_ld_x64(tmem + lane_off + C::kColDP + (uint32_t)(64 * h), v);
+        tc_fence_before();
+        mbar_arrive(bar(kDqDrained));
+        float* base = a.dqacc + ((size_t)row0 + (size_t)q0 + (size_t)(64 * h)) * D + (size_t)r;
 #pragma unroll
-      for (int ch = 0; ch < CW / 32; ++ch) {
-        const int c0 = h * CW + ch * 32;           // first query column of this chunk
-        uint32_t s[32], dp[32];
-        tmem_ld_x32(tmem + lane_off + C::col_s(b) + (uint32_t)c0, s);
-        tmem_ld_x32(tmem + lane_off + C::col_dp(b) + (uint32_t)c0, dp);
-        uint32_t pk[16], dk[16];
+        for (int c = 0; c < 64; ++c) red_add_f32(base + (size_t)c * D, u2f(v[c]));
+      } else {
+        // dQ: lane = query row, columns = head dims [32h, 32h + 32); 16-byte
+        // vector reductions along the row.
+        uint32_t v[32];
+        tmem_ld_x32(tmem + lane_off + C::kColDP + (uint32_t)(32 * h), v);
+        tc_fence_before();
+        mbar_arrive(bar(kDqDrained));
+        float* base = a.dqacc + ((size_t)row0 + (size_t)q0 + (size_t)r) * D + (size_t)(32 * h);
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2(fmaf(u2f(s[e]), sl2, -lse2[c0 + e]));
-          float p1 = ex2(fmaf(u2f(s[e + 1]), sl2, -lse2[c0 + e + 1]));
-          if (masked) {
-            // key kv is visible to query q iff kv ≤ q
-            if (kv > q0 + c0 + e) p0 = 0.f;
-            if (kv > q0 + c0 + e + 1) p1 = 0.f;
-          }
-          const float d0 = p0 * (u2f(dp[e]) - dvec[c0 + e]);
-          const float d1 = p1 * (u2f(dp[e + 1]) - dvec[c0 + e + 1]);
-          pk[e >> 1] = pack_bf16x2(p0, p1);
-          dk[e >> 1] = pack_bf16x2(d0, d1);
-        }
-        // 32 query columns = 64 bytes = four 16-byte chunks of this key row,
-        // placed with the 128-byte swizzle (chunk index XOR row % 8).
-        const int box = c0 >> 6;
-        const uint32_t row_addr = (uint32_t)(box * kBox + r * 128);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int chunk = ((c0 & 63) >> 3) + u;
-          const uint32_t off = row_addr + (uint32_t)(((chunk ^ (r & 7)) & 7) * 16);
-          st_shared_v4(p_tile + off, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-          st_shared_v4(ds_tile + off, dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
-        }
+        for (int c = 0; c < 32; c += 4) red_add_v4_f32(base + c, u2f(v[c]), u2f(v[c + 1]), u2f(v[c + 2]), u2f(v[c + 3]));
       }
-      tc_fence_before();
-      mbar_arrive(bar(kTmUsed + b));
-      fence_proxy_async_smem();
-      mbar_arrive(bar(kPdsFull + b));
-      mbar_arrive(bar(kQEmpty + b));
     }
     // ------------------------------------------------------------ dK, dV epilogue
     if (ok) {
@@ -223,33 +295,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
           st_global_v4(dst + 32 * cc + 8 * u, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       }
     }
-  } else if (warp < kTmaWarp) {
-    // ------------------------------------------------------------ dQ drain
-    const int g = warp - kDrainWarp0;
-    const uint32_t lane_off = (uint32_t)(g * 32) << 16;
-    for (int i = 0; i < n; ++i) {
-      const int b = i & 1;
-      bool ok = mbar_wait(bar(kDqFull + b), (uint32_t)((i >> 1) & 1), wc, site(6));
-      ok = __all_sync(kFull, ok);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t v[64];
-      tmem_ld_x64(tmem + lane_off + C::col_s(b), v);
-      tc_fence_before();
-      mbar_arrive(bar(kDqDrained + b));
-      const int q0 = (i0 + i) * BM;
-      if constexpr (D == 128) {
-        // lane = head dim, columns = 64 queries
-        float* base = a.dqacc + ((size_t)row0 + (size_t)q0) * D + (size_t)(g * 32 + lane);
-#pragma unroll
-        for (int c = 0; c < 64; ++c) red_add_f32(base + (size_t)c * D, u2f(v[c]));
-      } else {
-        // lane = query row, columns = 64 head dims
-        float* base = a.dqacc + ((size_t)row0 + (size_t)q0 + (size_t)(g * 32 + lane)) * D;
-#pragma unroll
-        for (int c = 0; c < 64; c += 4) red_add_v4_f32(base + c, u2f(v[c]), u2f(v[c + 1]), u2f(v[c + 2]), u2f(v[c + 3]));
-      }
-    }
   } else if (warp == kTmaWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -257,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       prefetch_tmap(&a.tm_k);
       prefetch_tmap(&a.tm_v);
       prefetch_tmap(&a.tm_do);
-      mbar_arrive_expect_tx(bar(kKVFull), 2u * C::kKV);
+      mbar_arrive_expect_tx(bar(kKVFull), 2u * C::kTile);
       for (int bx = 0; bx < D / 64; ++bx) {
         tma_load_2d(sbase + C::kK + bx * kBox, &a.tm_k, bar(kKVFull), 64 * bx, row0 + kv0);
         tma_load_2d(sbase + C::kV + bx * kBox, &a.tm_v, bar(kKVFull), 64 * bx, row0 + kv0);
@@ -266,15 +311,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       for (int i = 0; i < n; ++i) {
         const int s = i & 1;
         if (i >= 2 && !mbar_wait(bar(kQEmpty + s), (uint32_t)(((i >> 1) - 1) & 1), wc, site(7))) break;
-        const int q0 = (i0 + i) * BM;
-        mbar_arrive_expect_tx(bar(kQFull + s), 2u * C::kQT + 2u * BM * 4);
+        const int q0 = (i0 + i) * kBM;
+        mbar_arrive_expect_tx(bar(kQFull + s), 2u * C::kTile + 2u * kBM * 4);
         for (int bx = 0; bx < D / 64; ++bx) {
-          tma_load_2d(sbase + C::kQ + s * C::kQT + bx * C::kQBox, &a.tm_q, bar(kQFull + s), 64 * bx, row0 + q0);
-          tma_load_2d(sbase + C::kDO + s * C::kQT + bx * C::kQBox, &a.tm_do, bar(kQFull + s), 64 * bx,
-                      row0 + q0);
+          tma_load_2d(sbase + C::kQ + s * C::kTile + bx * kBox, &a.tm_q, bar(kQFull + s), 64 * bx, row0 + q0);
+          tma_load_2d(sbase + C::kDO + s * C::kTile + bx * kBox, &a.tm_do, bar(kQFull + s), 64 * bx, row0 + q0);
         }
-        bulk_load(sbase + C::kLSE + s * BM * 4, a.lse2 + row0 + q0, BM * 4, bar(kQFull + s));
-        bulk_load(sbase + C::kDV + s * BM * 4, a.dvec + row0 + q0, BM * 4, bar(kQFull + s));
+        bulk_load(sbase + C::kLSE + s * kBM * 4, a.lse2 + row0 + q0, kBM * 4, bar(kQFull + s));
+        bulk_load(sbase + C::kDV + s * kBM * 4, a.dvec + row0 + q0, kBM * 4, bar(kQFull + s));
         ++issued[s];
       }
       mbar_wait_drain(bar(kKVFull), 0, wc, site(8));
@@ -284,89 +328,78 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
   } else {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, BM, false, false);  // Sᵀ = K Qᵀ, dPᵀ = V dOᵀ
-      constexpr uint32_t kIdKV = idesc_bf16(128, D, false, true);   // dV += Pᵀ dO, dK += dSᵀ Q
-      // dQᵀ = Kᵀ dSᵀ (d = 128) or dQ = dS K (d = 64): both operands MN-major
-      constexpr uint32_t kIdQ = idesc_bf16(128, 64, true, true);
-      bool ok = mbar_wait(bar(kKVFull), 0, wc, site(9));
-      auto issue_sdp = [&](int i) -> bool {
-        const int b = i & 1;
-        if (!mbar_wait(bar(kQFull + b), (uint32_t)((i >> 1) & 1), wc, site(10))) return false;
-        if (i >= 2 && !mbar_wait(bar(kDqDrained + b), (uint32_t)(((i >> 1) - 1) & 1), wc, site(11))) return false;
-        tc_fence_after();
-        const uint32_t qb = sbase + C::kQ + b * C::kQT;
-        const uint32_t ob = sbase + C::kDO + b * C::kQT;
+      constexpr uint32_t kIdS = idesc_bf16(128, kBM, false, false);  // Sᵀ = K Qᵀ, dPᵀ = V dOᵀ
+      constexpr uint32_t kIdKV = idesc_bf16(128, D, false, true);    // dV += Pᵀ dO, dK += dSᵀ Q
+      // d = 128: dQᵀ = Kᵀ dSᵀ (M = head dims, N = 128 queries); d = 64: dQ = dS K (M = queries, N = 64)
+      constexpr uint32_t kIdQ = D == 128 ? idesc_bf16(128, kBM, true, true) : idesc_bf16(128, D, true, true);
+      auto issue_sd = [&](int i, uint32_t col, uint32_t a_tile) {    // Sᵀ (A = K) or dPᵀ (A = V)
+        const int st = i & 1;
+        const uint32_t b_tile = (a_tile == sbase + C::kK ? sbase + C::kQ : sbase + C::kDO) + st * C::kTile;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t ok_ = (uint32_t)((ks >> 2) * kBox + (ks & 3) * 32);
-          const uint32_t oq = (uint32_t)((ks >> 2) * C::kQBox + (ks & 3) * 32);
-          mma_ss(tmem + C::col_s(b), sdesc_sw128(sbase + C::kK + ok_, 16, 1024), sdesc_sw128(qb + oq, 16, 1024),
-                 kIdS, ks > 0 ? 1u : 0u);
+          const uint32_t off = (uint32_t)((ks >> 2) * kBox + (ks & 3) * 32);
+          mma_ss(tmem + col, sdesc_sw128(a_tile + off, 16, 1024), sdesc_sw128(b_tile + off, 16, 1024), kIdS,
+                 ks > 0 ? 1u : 0u);
         }
-        tc_commit(bar(kSFull + b));
-        // The dPᵀ buffer must have been read by the compute threads.
-        if (C::NDP == 2) {
-          if (i >= 2 && !mbar_wait(bar(kTmUsed + b), (uint32_t)(((i >> 1) - 1) & 1), wc, site(12))) return false;
-        } else {
-          if (i >= 1 && !mbar_wait(bar(kTmUsed + ((i - 1) & 1)), (uint32_t)(((i - 1) >> 1) & 1), wc, site(12)))
-            return false;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t ok_ = (uint32_t)((ks >> 2) * kBox + (ks & 3) * 32);
-          const uint32_t oq = (uint32_t)((ks >> 2) * C::kQBox + (ks & 3) * 32);
-          mma_ss(tmem + C::col_dp(b), sdesc_sw128(sbase + C::kV + ok_, 16, 1024), sdesc_sw128(ob + oq, 16, 1024),
-                 kIdS, ks > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(kDPFull + b));
-        return true;
       };
-      if (ok && n > 0) ok = issue_sdp(0);
-      if (ok && n > 1) ok = issue_sdp(1);
+      bool ok = mbar_wait(bar(kKVFull), 0, wc, site(9)) && mbar_wait(bar(kQFull), 0, wc, site(10));
+      if (ok && n > 0) {
+        tc_fence_after();
+        issue_sd(0, C::kColS, sbase + C::kK);
+        tc_commit(bar(kSFull));
+        issue_sd(0, C::kColDP, sbase + C::kV);
+        tc_commit(bar(kDPFull));
+      }
       for (int i = 0; ok && i < n; ++i) {
-        const int b = i & 1;
-        if (!mbar_wait(bar(kPdsFull + b), (uint32_t)((i >> 1) & 1), wc, site(13))) {
+        const int st = i & 1;
+        if (!mbar_wait(bar(kPdsFull), (uint32_t)(i & 1), wc, site(11))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t pt = sbase + C::kP + b * C::kPT;
-        const uint32_t dst = sbase + C::kDS + b * C::kPT;
-        const uint32_t qb = sbase + C::kQ + b * C::kQT;
-        const uint32_t ob = sbase + C::kDO + b * C::kQT;
-        // dQ first, so that its drain overlaps the dV / dK products.
+        const uint32_t ds = sbase + C::kDS;
+        const uint32_t qb = sbase + C::kQ + st * C::kTile;
+        const uint32_t ob = sbase + C::kDO + st * C::kTile;
+        // dQ into the dPᵀ columns first, so its drain overlaps dV and dK.
+        // Both operands are read MN-major, dSᵀ [keys][queries] and K [keys][dims].
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint32_t kst = (uint32_t)(ks * 2048);   // 16 key rows
-          uint64_t da, db;
-          if constexpr (D == 128) {
-            da = sdesc_sw128(sbase + C::kK + kst, kBox, 1024);   // Kᵀ: M = head dims (two 64-wide blocks)
-            db = sdesc_sw128(dst + kst, kBox, 1024);             // dSᵀ: N = 64 queries
-          } else {
-            da = sdesc_sw128(dst + kst, kBox, 1024);             // dS: M = 128 queries (two 64-wide blocks)
-            db = sdesc_sw128(sbase + C::kK + kst, kBox, 1024);   // K: N = 64 head dims
+          const uint64_t dsd = sdesc_sw128(ds + (uint32_t)(ks * 2048), kBox, 1024);
+          const uint64_t kd = sdesc_sw128(sbase + C::kK + (uint32_t)(ks * 2048), kBox, 1024);
+          if constexpr (D == 128)
+            mma_ss(tmem + C::kColDP, kd, dsd, kIdQ, ks > 0 ? 1u : 0u);
+          else
+            mma_ss(tmem + C::kColDP, dsd, kd, kIdQ, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(kDqFull));
+        // dV += Pᵀ dO, Pᵀ from tensor memory
+#pragma unroll
+        for (int ks = 0; ks < kBM / 16; ++ks)
+          mma_ts(tmem + C::kColDV, tmem + C::kColS + (uint32_t)(8 * ks),
+                 sdesc_sw128(ob + (uint32_t)(ks * 2048), kBox, 1024), kIdKV, (i > 0 || ks > 0) ? 1u : 0u);
+        // dK += dSᵀ Q
+#pragma unroll
+        for (int ks = 0; ks < kBM / 16; ++ks)
+          mma_ss(tmem + C::kColDK, sdesc_sw128(ds + (uint32_t)((ks >> 2) * kBox + (ks & 3) * 32), 16, 1024),
+                 sdesc_sw128(qb + (uint32_t)(ks * 2048), kBox, 1024), kIdKV, (i > 0 || ks > 0) ? 1u : 0u);
+        tc_commit(bar(kQEmpty + st));
+        if (i + 1 < n) {
+          // Sᵀ of the next tile overwrites Pᵀ: issued after dV, which reads it.
+          if (!mbar_wait(bar(kQFull + ((i + 1) & 1)), (uint32_t)(((i + 1) >> 1) & 1), wc, site(12))) {
+            ok = false;
+            break;
           }
-          mma_ss(tmem + C::col_s(b), da, db, kIdQ, ks > 0 ? 1u : 0u);
+          tc_fence_after();
+          issue_sd(i + 1, C::kColS, sbase + C::kK);
+          tc_commit(bar(kSFull));
+          if (!mbar_wait(bar(kDqDrained), (uint32_t)(i & 1), wc, site(13))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_sd(i + 1, C::kColDP, sbase + C::kV);
+          tc_commit(bar(kDPFull));
         }
-        tc_commit(bar(kDqFull + b));
-#pragma unroll
-        for (int ks = 0; ks < BM / 16; ++ks) {
-          const uint32_t oa = (uint32_t)((ks >> 2) * kBox + (ks & 3) * 32);   // Pᵀ / dSᵀ, K-major over queries
-          const uint32_t ob2 = (uint32_t)(ks * 2048);                         // dO / Q, MN-major, 16 query rows
-          mma_ss(tmem + C::kColDV, sdesc_sw128(pt + oa, 16, 1024), sdesc_sw128(ob + ob2, C::kQBox, 1024), kIdKV,
-                 (i > 0 || ks > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int ks = 0; ks < BM / 16; ++ks) {
-          const uint32_t oa = (uint32_t)((ks >> 2) * kBox + (ks & 3) * 32);
-          const uint32_t ob2 = (uint32_t)(ks * 2048);
-          mma_ss(tmem + C::kColDK, sdesc_sw128(dst + oa, 16, 1024), sdesc_sw128(qb + ob2, C::kQBox, 1024), kIdKV,
-                 (i > 0 || ks > 0) ? 1u : 0u);
-        }
-        tc_commit(bar(kQEmpty + b));
-        tc_commit(bar(kPdsEmpty + b));
-        if (i + 2 < n) ok = issue_sdp(i + 2);
       }
       if (ok) tc_commit(bar(kDKVFull));
       tc_commit(bar(kMmaDone));
@@ -388,7 +421,8 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t s) {
   const size_t smem = BwdCfg<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(a.B * a.H), (unsigned)(a.N / kBN));
+  const unsigned tiles = (unsigned)(a.N / kBN), heads = (unsigned)(a.B * a.H);
+  const dim3 grid = CAUSAL ? dim3(heads, tiles) : dim3(tiles, heads);
   kern<<<grid, kThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
@@ -448,11 +482,9 @@ __global__ void __launch_bounds__(256) dq_finish_kernel(const float* __restrict_
 
 }  // namespace
 
-int bwd_bf16_block_m(int d) { return d == 128 ? BwdCfg<128>::BM : BwdCfg<64>::BM; }
+int bwd_bf16_block_m(int) { return kBM; }
 
-size_t bwd_bf16_smem_bytes(int d) {
-  return d == 64 ? BwdCfg<64>::kBytes : BwdCfg<128>::kBytes;
-}
+size_t bwd_bf16_smem_bytes(int d) { return d == 64 ? BwdCfg<64>::kBytes : BwdCfg<128>::kBytes; }
 
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t s) {
   if (a.d == 128) return a.causal ? launch_impl<128, true>(a, s) : launch_impl<128, false>(a, s);

@@ -86,8 +86,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int N = a.N;
-  const int bh = blockIdx.x;
-  const int pair = (int)gridDim.y - 1 - (int)blockIdx.y;   // heaviest query tiles first
+  // Non-causal: head-major grid (pair fastest), so a wave touches few heads'
+  // K/V and they stay in L2.  Causal: batch·head fastest with the heaviest
+  // pairs first across the whole grid (longest tiles scheduled first).
+  const int pair = CAUSAL ? (int)gridDim.y - 1 - (int)blockIdx.y : (int)blockIdx.x;
+  const int bh = CAUSAL ? (int)blockIdx.x : (int)blockIdx.y;
   const int q0 = pair * 2 * kBM;
   const int row0 = bh * N;                                 // first row of this head in the [B·H·N, d] view
   const int n_kv = N / kBN;
@@ -334,7 +337,8 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t s) {
   const size_t smem = FwdLayout<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(a.B * a.H), (unsigned)((a.N + 2 * kBM - 1) / (2 * kBM)));
+  const unsigned pairs = (unsigned)((a.N + 2 * kBM - 1) / (2 * kBM)), heads = (unsigned)(a.B * a.H);
+  const dim3 grid = CAUSAL ? dim3(heads, pairs) : dim3(pairs, heads);
   kern<<<grid, kThreads, smem, s>>>(a);
   return cudaGetLastError();
 }

@@ -44,6 +44,9 @@ constexpr int kComputeWarps = 8;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kBox = 16384;         // one TMA box: 128 rows × 128 bytes
+// Exponential pairs per FMA-pipe exponential (0 = all on MUFU); measured on
+// GB300 the split makes no difference here, so all stay on MUFU.
+constexpr int kPolyEvery = 0;
 
 template <int D>
 struct BwdCfg {
@@ -80,6 +83,34 @@ enum BwdBar : int {
 };
 
 __device__ __forceinline__ uint32_t site(int s) { return 0x0200u | (uint32_t)s; }
+
+// Pᵀ for 32 query columns of one key row: p = 2^(s·scale·log2e − LSE₂) as
+// packed pairs, from Sᵀ (32 TMEM words) and −LSE₂ (16 pairs).  With MASKED,
+// columns whose query precedes the key (column index < `row_minus_col0`) are
+// zero.  With POLY_EVERY > 0 one pair in POLY_EVERY takes its exponentials on
+// the FMA pipe.
+template <bool MASKED, int POLY_EVERY>
+__device__ __forceinline__ void p_chunk(const uint32_t (&s)[32], uint64_t sl2x2, const uint64_t* nlse,
+                                        int row_minus_col0, uint64_t* p) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const uint64_t x = f2_fma(f2_pack(u2f(s[2 * e]), u2f(s[2 * e + 1])), sl2x2, nlse[e]);
+    float x0, x1, e0, e1;
+    f2_unpack(x, x0, x1);
+    if (POLY_EVERY > 0 && e % (POLY_EVERY > 0 ? POLY_EVERY : 1) == POLY_EVERY - 1) {
+      exp2_fma_x2(x0, x1, e0, e1);
+    } else {
+      e0 = ex2(x0);
+      e1 = ex2(x1);
+    }
+    if (MASKED) {
+      // key kv is visible to query q iff kv ≤ q
+      e0 = row_minus_col0 > 2 * e ? 0.f : e0;
+      e1 = row_minus_col0 > 2 * e + 1 ? 0.f : e1;
+    }
+    p[e] = f2_pack(e0, e1);
+  }
+}
 
 // Barrier among the two compute warps that share a TMEM lane quarter, with an
 // AND over their `ok` flags so both take the same branch.
@@ -167,10 +198,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       ok = mbar_wait(bar(kSFull), par, wc, site(1)) && mbar_wait(bar(kDPFull), par, wc, site(2)) &&
            mbar_wait(bar(kQFull + st), (uint32_t)((i >> 1) & 1), wc, site(3));
       ok = __all_sync(kFull, ok);
-      const float* lse2 = reinterpret_cast<const float*>(sgen + C::kLSE + st * kBM * 4);
-      const float* dvec = reinterpret_cast<const float*>(sgen + C::kDV + st * kBM * 4);
+      // The pre-pass stored −LSE·log2(e) and −D, so each pair of columns is
+      // one packed FMA (the exponent) and one packed add/multiply (dS).
+      const uint64_t* nlse = reinterpret_cast<const uint64_t*>(sgen + C::kLSE + st * kBM * 4);
+      const uint64_t* ndv = reinterpret_cast<const uint64_t*>(sgen + C::kDV + st * kBM * 4);
       const bool masked = CAUSAL && i == 0;        // the diagonal tile (q0 == kv0)
-      float p[64];
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
+      uint64_t p[32];                              // P for query columns 64h + 2e, 2e + 1
       if (ok) {
         tc_fence_after();
 #pragma unroll
@@ -178,38 +212,26 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
           const int c0 = h * 64 + ch * 32;
           uint32_t s[32];
           tmem_ld_x32(tmem + lane_off + C::kColS + (uint32_t)c0, s);
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c0 + e);
-            p[ch * 32 + e + 0] = ex2(fmaf(u2f(s[e + 0]), sl2, -l4.x));
-            p[ch * 32 + e + 1] = ex2(fmaf(u2f(s[e + 1]), sl2, -l4.y));
-            p[ch * 32 + e + 2] = ex2(fmaf(u2f(s[e + 2]), sl2, -l4.z));
-            p[ch * 32 + e + 3] = ex2(fmaf(u2f(s[e + 3]), sl2, -l4.w));
-          }
-          if (masked) {
-            // key kv is visible to query q iff kv ≤ q
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (r > c0 + e) p[ch * 32 + e] = 0.f;
-          }
+          if (masked)
+            p_chunk<true, kPolyEvery>(s, sl2x2, nlse + (c0 >> 1), r - c0, p + ch * 16);
+          else
+            p_chunk<false, kPolyEvery>(s, sl2x2, nlse + (c0 >> 1), r - c0, p + ch * 16);
         }
       }
       // Both warps of the lane quarter have read their Sᵀ columns; Pᵀ may now
       // be written over the first 64 of them.
       ok = pair_sync_and(1 + g, ok);
       if (!ok) break;
-      {
-        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
-        uint32_t lo[16], hi[16];
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          lo[e] = pk[e];
-          hi[e] = pk[16 + e];
+          float a0, a1;
+          f2_unpack(p[half * 16 + e], a0, a1);
+          pk[e] = pack_bf16x2(a0, a1);
         }
-        tmem_st_x16(tmem + lane_off + C::kColS + (uint32_t)(h * 32), lo);
-        tmem_st_x16(tmem + lane_off + C::kColS + (uint32_t)(h * 32 + 16), hi);
+        tmem_st_x16(tmem + lane_off + C::kColS + (uint32_t)(h * 32 + 16 * half), pk);
       }
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
@@ -218,14 +240,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         tmem_ld_x32(tmem + lane_off + C::kColDP + (uint32_t)c0, dp);
         uint32_t dk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(dvec + c0 + e);
-          const float d0 = p[ch * 32 + e + 0] * (u2f(dp[e + 0]) - d4.x);
-          const float d1 = p[ch * 32 + e + 1] * (u2f(dp[e + 1]) - d4.y);
-          const float d2 = p[ch * 32 + e + 2] * (u2f(dp[e + 2]) - d4.z);
-          const float d3 = p[ch * 32 + e + 3] * (u2f(dp[e + 3]) - d4.w);
-          dk[(e >> 1) + 0] = pack_bf16x2(d0, d1);
-          dk[(e >> 1) + 1] = pack_bf16x2(d2, d3);
+        for (int e = 0; e < 16; ++e) {
+          const uint64_t ds = f2_mul(p[ch * 16 + e], f2_add(f2_pack(u2f(dp[2 * e]), u2f(dp[2 * e + 1])), ndv[(c0 >> 1) + e]));
+          float d0, d1;
+          f2_unpack(ds, d0, d1);
+          dk[e] = pack_bf16x2(d0, d1);
         }
         // 32 query columns = four 16-byte chunks of this key row, in box h
         // (queries 64h..64h+63), placed with the 128-byte swizzle.
@@ -461,8 +480,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
 #pragma unroll
   for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
   if (row < rows && part == 0) {
-    dvec[row] = acc;
-    lse2[row] = lse[row] * 1.4426950408889634074f;
+    // Stored negated: the tiled kernel adds them with packed f32x2 operations.
+    dvec[row] = -acc;
+    lse2[row] = -lse[row] * 1.4426950408889634074f;
   }
 }
 

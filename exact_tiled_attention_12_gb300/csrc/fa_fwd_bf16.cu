@@ -36,6 +36,10 @@ constexpr int kThreads = 320;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kBoxBytes = 128 * 128;   // one TMA box: 128 rows × 128 bytes
+// Exponential pairs per FMA-pipe exponential (0 = all on MUFU).  Measured on
+// GB300: moving 1/8, 1/4 or 1/2 of them to the FMA pipe slows the softmax
+// (it is issue-bound, not MUFU-bound), so all stay on MUFU.
+constexpr int kPolyEvery = 0;
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 template <int D>
@@ -64,6 +68,44 @@ enum FwdBar : int {
 
 // Fault codes recorded when a wait runs out of time (kernel id 1 in the high byte).
 __device__ __forceinline__ uint32_t site(int s) { return 0x0100u | (uint32_t)s; }
+
+// P = 2^(s·scale·log2e − m) for one 128-column row of S, rounded to bf16 and
+// stored over the row's first 64 tensor-memory columns; returns Σ P in fp32.
+// The scale-and-subtract and the sum run as packed f32x2 operations; with
+// POLY_EVERY > 0, one pair of exponentials in POLY_EVERY runs on the FMA pipe
+// (exp2_fma_x2), the others on MUFU.
+template <int POLY_EVERY>
+__device__ __forceinline__ float exp_tile_to_p(const uint32_t (&s)[128], float sl2, float m_ref, uint32_t p_addr) {
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
+  const uint64_t negx2 = f2_pack(-m_ref, -m_ref);
+  uint64_t lsum0 = f2_pack(0.f, 0.f), lsum1 = lsum0;
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    uint32_t p[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint64_t x = f2_fma(f2_pack(u2f(s[32 * cc + 2 * i]), u2f(s[32 * cc + 2 * i + 1])), sl2x2, negx2);
+      float x0, x1, e0, e1;
+      f2_unpack(x, x0, x1);
+      if (POLY_EVERY > 0 && i % (POLY_EVERY > 0 ? POLY_EVERY : 1) == POLY_EVERY - 1) {
+        exp2_fma_x2(x0, x1, e0, e1);
+      } else {
+        e0 = ex2(x0);
+        e1 = ex2(x1);
+      }
+      if (i & 1)
+        lsum1 = f2_add(lsum1, f2_pack(e0, e1));
+      else
+        lsum0 = f2_add(lsum0, f2_pack(e0, e1));
+      p[i] = pack_bf16x2(e0, e1);
+    }
+    tmem_st_x16(p_addr + 16 * cc, p);
+  }
+  float la, lb, lc, ld;
+  f2_unpack(lsum0, la, lb);
+  f2_unpack(lsum1, lc, ld);
+  return (la + lb) + (lc + ld);
+}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_constant__ FwdArgs a) {
@@ -153,13 +195,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
         for (int c = 0; c < 128; ++c)
           if (c > r) s[c] = f2u(-INFINITY);
       }
+      // Row max: four independent chains of 3-input maxima.
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, u2f(s[c]));
-        mx1 = fmaxf(mx1, u2f(s[c + 1]));
-        mx2 = fmaxf(mx2, u2f(s[c + 2]));
-        mx3 = fmaxf(mx3, u2f(s[c + 3]));
+      for (int c = 0; c < 128; c += 8) {
+        mx0 = max3(mx0, u2f(s[c]), u2f(s[c + 1]));
+        mx1 = max3(mx1, u2f(s[c + 2]), u2f(s[c + 3]));
+        mx2 = max3(mx2, u2f(s[c + 4]), u2f(s[c + 5]));
+        mx3 = max3(mx3, u2f(s[c + 6]), u2f(s[c + 7]));
       }
       const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
       const bool move = mx > m_ref + 8.0f;                 // always true on the first tile
@@ -180,22 +223,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
       }
       ell *= alpha;
       m_ref = m_new;
-      const float neg = -m_ref;
-      float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t p[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float e0 = ex2(fmaf(u2f(s[32 * cc + 2 * i]), sl2, neg));
-          const float e1 = ex2(fmaf(u2f(s[32 * cc + 2 * i + 1]), sl2, neg));
-          l0 += e0;
-          l1 += e1;
-          p[i] = pack_bf16x2(e0, e1);
-        }
-        tmem_st_x16(tmem + lane_off + s_col(t) + 16 * cc, p);
-      }
-      ell += l0 + l1;
+      // The causal diagonal tile takes every exponential on MUFU, so masked
+      // scores give exactly 0.
+      const uint32_t p_addr = tmem + lane_off + s_col(t);
+      if (CAUSAL && j == nt - 1)
+        ell += exp_tile_to_p<0>(s, sl2, m_ref, p_addr);
+      else
+        ell += exp_tile_to_p<kPolyEvery>(s, sl2, m_ref, p_addr);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kPFull + t));

@@ -30,8 +30,8 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s);
 // of BM rows (BM = 64 for d = 128, 128 for d = 64).
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
-  const float* lse2;      // workspace: LSE · log2(e), [B·H·N]
-  const float* dvec;      // workspace: D = rowsum(dO ⊙ O), [B·H·N]
+  const float* lse2;      // workspace: −LSE · log2(e), [B·H·N]
+  const float* dvec;      // workspace: −D = −rowsum(dO ⊙ O), [B·H·N]
   float* dqacc;           // workspace: fp32 dQ accumulator, [B·H·N, d]
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;

@@ -234,6 +234,62 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 
+// ---- packed fp32 pairs (one f32x2 instruction does two lanes of work)
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// 2^x for two values on the FMA/ALU pipes, leaving the MUFU pipe to the other
+// exponentials of a tile.  Cody–Waite range reduction (Cody & Waite, "Software
+// Manual for the Elementary Functions", 1980): n = round(x) by adding 1.5·2^23,
+// f = x − n in [−1/2, 1/2]; 2^f by a cubic fitted for this library
+// (max relative error 7.5e-5 on [−1/2, 1/2], well under bf16's 2^-9); the
+// result's exponent field is then raised by n.  Inputs are clamped to
+// [−125, 126]; callers that need an exact 0 for −∞ (masked scores) must not
+// use it for those elements.
+__device__ __forceinline__ void exp2_fma_x2(float x0, float x1, float& y0, float& y1) {
+  constexpr float kShift = 12582912.0f;   // 1.5 · 2^23
+  x0 = fminf(fmaxf(x0, -125.0f), 126.0f);
+  x1 = fminf(fmaxf(x1, -125.0f), 126.0f);
+  const uint64_t x = f2_pack(x0, x1);
+  const uint64_t t = f2_add(x, f2_pack(kShift, kShift));             // n in the low mantissa bits
+  const uint64_t nf = f2_add(t, f2_pack(-kShift, -kShift));          // n as a float
+  const uint64_t f = f2_fma(nf, f2_pack(-1.0f, -1.0f), x);           // x − n
+  uint64_t p = f2_fma(f, f2_pack(0.055171653f, 0.055171653f), f2_pack(0.24261113f, 0.24261113f));
+  p = f2_fma(p, f, f2_pack(0.69326097f, 0.69326097f));
+  p = f2_fma(p, f, f2_pack(0.99992806f, 0.99992806f));
+  float p0, p1, t0, t1;
+  f2_unpack(p, p0, p1);
+  f2_unpack(t, t0, t1);
+  y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
+  y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
+}
+
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }

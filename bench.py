@@ -130,8 +130,12 @@ def run_ours(args, w, rank, world):
     sp = ctypes.c_void_p(stream.cuda_stream)
     P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
 
+    fws_n = fa.fwd_workspace_size(B, H, N, d, w.causal, q.dtype)
+    fws = torch.empty(max(fws_n, 1), dtype=torch.uint8, device=dev)
+
     def fwd():
-        st = L.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, w.scale, int(w.causal), 0, sp)
+        st = L.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, w.scale, int(w.causal), 0,
+                      P(fws) if fws_n else None, fws_n, sp)
         assert st == 0, fa.status_string(st)
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]

@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     bwd_stages,
     bwd_workspace_size,
     fwd,
+    fwd_workspace_size,
     lib,
     library_path,
     status_string,

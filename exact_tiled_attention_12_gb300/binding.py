@@ -27,7 +27,8 @@ _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_version": (_I, []),
-    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "fa_fwd_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
+    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P, _Z, _P]),
     "fa_bwd_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P, _Z, _P]),
     "fa_bwd_prep": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
@@ -108,16 +109,30 @@ def _check_qkv(*ts):
             raise ValueError("tensors must be contiguous [B, H, N, d]")
 
 
-def fwd(q, k, v, scale=None, causal=False):
-    """Attention forward.  Returns (o [B,H,N,d] in q's dtype, lse [B,H,N] float32)."""
+def fwd_workspace_size(B, H, N, d, causal=False, dtype=torch.bfloat16) -> int:
+    code = FA_DTYPE_BF16 if dtype == torch.bfloat16 else FA_DTYPE_FP32
+    return int(lib().fa_fwd_workspace_size(B, H, N, d, int(bool(causal)), code))
+
+
+def fwd(q, k, v, scale=None, causal=False, workspace=None):
+    """Attention forward.  Returns (o [B,H,N,d] in q's dtype, lse [B,H,N] float32).
+
+    ``workspace``: None allocates the optional load-balancing workspace with
+    torch when the library asks for one; a uint8 CUDA tensor is used as given;
+    False runs without one.
+    """
     _check_qkv(q, k, v)
     B, H, N, d = q.shape
     scale = float(d ** -0.5 if scale is None else scale)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     with torch.cuda.device(q.device):
+        if workspace is None:
+            n = fwd_workspace_size(B, H, N, d, causal, q.dtype)
+            workspace = torch.empty(n, dtype=torch.uint8, device=q.device) if n else False
+        ws, n = (None, 0) if workspace is False else (workspace, workspace.numel())
         _check("fa_fwd", lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
-                                      int(bool(causal)), _dtype_code(q), _stream(q)))
+                                      int(bool(causal)), _dtype_code(q), _ptr(ws), n, _stream(q)))
     return o, lse
 
 

@@ -137,6 +137,37 @@ fa_status carve_workspace(const Shape& s, fa_dtype dtype, void* ws, size_t bytes
 
 inline fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
+// SM count of the current device (0 if it cannot be queried), cached per device.
+int sm_count_current_device() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+  cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+struct FwdPlan {
+  int n_full, splits;
+  size_t opart_bytes;
+};
+
+// Workspace the forward's load balancing needs on the current device (0 when
+// it does not split: causal, fp32, or no partial last wave worth splitting).
+size_t fwd_workspace_bytes(const Shape& s, int causal, fa_dtype dtype, FwdPlan* plan) {
+  if (s.empty() || causal || dtype != FA_DTYPE_BF16) return 0;
+  const int units = fa::fwd_units((int)s.B, (int)s.H, (int)s.N);
+  int n_full, splits;
+  fa::fwd_split_plan(units, sm_count_current_device(), (int)(s.N / 128), &n_full, &splits);
+  if (splits <= 1 || n_full >= units) return 0;
+  const size_t rows = (size_t)(units - n_full) * (size_t)splits * 256;
+  const size_t opart = pad256(rows * (size_t)s.d * 4);
+  if (plan) *plan = FwdPlan{n_full, splits, opart};
+  return opart + pad256(rows * 4);
+}
+
 constexpr float kLog2e = 1.4426950408889634074f;
 
 }  // namespace
@@ -158,8 +189,15 @@ const char* fa_status_string(fa_status s) {
 
 int fa_version(void) { return 100; }
 
+size_t fa_fwd_workspace_size(int B, int H, int N, int d, int causal, fa_dtype dtype) {
+  Shape s;
+  if (check_shape(B, H, N, d, dtype, &s) != FA_OK || (causal != 0 && causal != 1)) return 0;
+  return fwd_workspace_bytes(s, causal, dtype, nullptr);
+}
+
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-                 float scale, int causal, fa_dtype dtype, fa_stream_t stream) {
+                 float scale, int causal, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                 fa_stream_t stream) {
   Shape s;
   fa_status st = check_shape(B, H, N, d, dtype, &s);
   if (st != FA_OK) return st;
@@ -167,6 +205,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (s.empty()) return FA_OK;
   if ((st = check_ptrs({q, k, v, o, lse}, dtype)) != FA_OK) return st;
+  if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_WORKSPACE;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   unsigned int* fault = fault_word_for_current_device();
   if (!fault) return FA_ERR_CUDA;
@@ -188,6 +227,20 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   a.scale_log2 = scale * kLog2e;
   a.causal = causal;
   a.fault = fault;
+  // Load balancing needs the workspace; without one (NULL) every unit runs whole.
+  FwdPlan plan;
+  const size_t need = fwd_workspace_bytes(s, causal, dtype, &plan);
+  a.n_full = fa::fwd_units(B, H, N);
+  a.splits = 1;
+  a.opart = nullptr;
+  a.lpart = nullptr;
+  if (need > 0 && workspace != nullptr) {
+    if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+    a.n_full = plan.n_full;
+    a.splits = plan.splits;
+    a.opart = static_cast<float*>(workspace);
+    a.lpart = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.opart_bytes);
+  }
   return from_cuda(fa::launch_fwd_bf16(a, cs));
 }
 

@@ -128,14 +128,32 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int N = a.N;
-  // Non-causal: head-major grid (pair fastest), so a wave touches few heads'
-  // K/V and they stay in L2.  Causal: batch·head fastest with the heaviest
-  // pairs first across the whole grid (longest tiles scheduled first).
-  const int pair = CAUSAL ? (int)gridDim.y - 1 - (int)blockIdx.y : (int)blockIdx.x;
-  const int bh = CAUSAL ? (int)blockIdx.x : (int)blockIdx.y;
+  const int pairs = (N + 2 * kBM - 1) / (2 * kBM);       // two-tile units per head
+  // Work of this CTA (1-D grid).  Causal: batch·head fastest with the
+  // heaviest pairs first across the whole grid (longest tiles scheduled
+  // first).  Non-causal: head-major (pair fastest), so a wave touches few
+  // heads' K/V and they stay in L2; the last `tail` units are split into
+  // `splits` CTAs over equal K/V sub-ranges, each writing a partial result
+  // (normalised O and LSE of its keys) that fwd_combine merges.
+  int bh, pair, kv_begin = 0, n_kv = N / kBN, part_slot = -1;
+  const int idx = (int)blockIdx.x;
+  if (CAUSAL) {
+    bh = idx % (a.B * a.H);
+    pair = pairs - 1 - idx / (a.B * a.H);
+  } else if (idx < a.n_full) {
+    bh = idx / pairs;
+    pair = idx % pairs;
+  } else {
+    part_slot = idx - a.n_full;                            // = tail unit · splits + part
+    const int unit = a.n_full + part_slot / a.splits;
+    const int part = part_slot % a.splits;
+    bh = unit / pairs;
+    pair = unit % pairs;
+    kv_begin = part * n_kv / a.splits;
+    n_kv = (part + 1) * n_kv / a.splits - kv_begin;
+  }
   const int q0 = pair * 2 * kBM;
   const int row0 = bh * N;                                 // first row of this head in the [B·H·N, d] view
-  const int n_kv = N / kBN;
 
   // Number of K/V tiles each query tile visits (0 if the tile is past N).
   int n_t[2];
@@ -241,20 +259,37 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
         tc_fence_after();
         const int q = q0 + t * kBM + r;
         const float inv = 1.0f / ell;
-        __nv_bfloat16* orow = a.o + ((size_t)row0 + (size_t)q) * D;
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld_x32(tmem + lane_off + o_col(t) + 32 * cc, o);
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            st_global_v4(orow + 32 * cc + 8 * v4, pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-        }
         // LSE in natural log of the scaled scores: (m + log2 ℓ) · ln 2.
-        a.lse[(size_t)row0 + (size_t)q] = (m_ref + log2f(ell)) * 0.69314718055994530942f;
+        const float lse = (m_ref + log2f(ell)) * 0.69314718055994530942f;
+        if (part_slot < 0) {
+          __nv_bfloat16* orow = a.o + ((size_t)row0 + (size_t)q) * D;
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld_x32(tmem + lane_off + o_col(t) + 32 * cc, o);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              st_global_v4(orow + 32 * cc + 8 * v4, pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
+          a.lse[(size_t)row0 + (size_t)q] = lse;
+        } else {
+          // Partial over this CTA's keys: normalised O and LSE in fp32.
+          const size_t prow = (size_t)part_slot * (2 * kBM) + (size_t)(t * kBM + r);
+          float* orow = a.opart + prow * D;
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld_x32(tmem + lane_off + o_col(t) + 32 * cc, o);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              st_global_v4(orow + 32 * cc + 4 * v4, f2u(u2f(o[4 * v4]) * inv), f2u(u2f(o[4 * v4 + 1]) * inv),
+                           f2u(u2f(o[4 * v4 + 2]) * inv), f2u(u2f(o[4 * v4 + 3]) * inv));
+          }
+          a.lpart[prow] = lse;
+        }
       }
     }
   } else if (warp == kTmaWarp) {
@@ -281,13 +316,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
         mbar_arrive_expect_tx(bar(kKFull + s), tile);
         for (int b = 0; b < D / 64; ++b)
           tma_load_2d(sbase + L::kK + s * L::kTile + b * kBoxBytes, &a.tm_k, bar(kKFull + s), 64 * b,
-                      row0 + j * kBN);
+                      row0 + (kv_begin + j) * kBN);
         ++issued_k[s];
         if (j >= 2 && !mbar_wait(bar(kVEmpty + s), (uint32_t)(((j >> 1) - 1) & 1), wc, site(4))) break;
         mbar_arrive_expect_tx(bar(kVFull + s), tile);
         for (int b = 0; b < D / 64; ++b)
           tma_load_2d(sbase + L::kV + s * L::kTile + b * kBoxBytes, &a.tm_v, bar(kVFull + s), 64 * b,
-                      row0 + j * kBN);
+                      row0 + (kv_begin + j) * kBN);
         ++issued_v[s];
       }
       // Never leave the CTA with copies in flight: wait for the last load of
@@ -365,19 +400,91 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
   }
 }
 
+template <int D>
+cudaError_t launch_combine(const FwdArgs& a, int tail, cudaStream_t s);
+
 template <int D, bool CAUSAL>
 cudaError_t launch_impl(const FwdArgs& a, cudaStream_t s) {
   auto kern = fa_fwd_bf16_kernel<D, CAUSAL>;
   const size_t smem = FwdLayout<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const unsigned pairs = (unsigned)((a.N + 2 * kBM - 1) / (2 * kBM)), heads = (unsigned)(a.B * a.H);
-  const dim3 grid = CAUSAL ? dim3(heads, pairs) : dim3(pairs, heads);
-  kern<<<grid, kThreads, smem, s>>>(a);
+  const long long units = (long long)fwd_units(a.B, a.H, a.N);
+  const long long ctas = CAUSAL ? units : a.n_full + (units - a.n_full) * a.splits;
+  kern<<<(unsigned)ctas, kThreads, smem, s>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || CAUSAL || a.splits <= 1 || a.n_full >= units) return e;
+  return launch_combine<D>(a, (int)(units - a.n_full), s);
+}
+
+// Merge of the split partials, "Flash Attention" tutorial, 2.Online Softmax
+// §3.1/§4.1 and §七 (the merge is log-sum-exp): for one query row with
+// partials (O_k, L_k) over disjoint key ranges, L = ln Σ_k e^{L_k} and
+// O = Σ_k e^{L_k − L} O_k.  One warp per row; lanes over the head dims.
+template <int D>
+__global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restrict__ opart,
+                                                          const float* __restrict__ lpart, __nv_bfloat16* __restrict__ o,
+                                                          float* __restrict__ lse, int N, int n_full, int splits,
+                                                          int tail) {
+  constexpr int V = D / 32;   // floats per lane
+  const int row = (int)(blockIdx.x * 8 + (threadIdx.x >> 5));
+  const int lane = threadIdx.x & 31;
+  if (row >= tail * 2 * kBM) return;
+  const int u = row / (2 * kBM), rr = row % (2 * kBM);
+  const int pairs = (N + 2 * kBM - 1) / (2 * kBM);
+  const int unit = n_full + u;
+  const int q = (unit % pairs) * 2 * kBM + rr;
+  if (q >= N) return;
+  const size_t orow = (size_t)(unit / pairs) * N + (size_t)q;
+  float mx = -INFINITY;
+  for (int k = 0; k < splits; ++k) mx = fmaxf(mx, lpart[(size_t)(u * splits + k) * 2 * kBM + rr]);
+  float sum = 0.f;
+  for (int k = 0; k < splits; ++k) sum += expf(lpart[(size_t)(u * splits + k) * 2 * kBM + rr] - mx);
+  const float total = mx + logf(sum);
+  float acc[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc[v] = 0.f;
+  for (int k = 0; k < splits; ++k) {
+    const size_t pr = (size_t)(u * splits + k) * 2 * kBM + rr;
+    const float w = expf(lpart[pr] - total);
+    const float* src = opart + pr * D + lane * V;
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] = fmaf(w, src[v], acc[v]);
+  }
+  __nv_bfloat16* dst = o + orow * D + lane * V;
+#pragma unroll
+  for (int v = 0; v < V; v += 2) reinterpret_cast<uint32_t*>(dst)[v / 2] = pack_bf16x2(acc[v], acc[v + 1]);
+  if (lane == 0) lse[orow] = total;
+}
+
+template <int D>
+cudaError_t launch_combine(const FwdArgs& a, int tail, cudaStream_t s) {
+  const int rows = tail * 2 * kBM;
+  fwd_combine_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a.opart, a.lpart, a.o, a.lse, a.N, a.n_full,
+                                                                   a.splits, tail);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+int fwd_units(int B, int H, int N) { return B * H * ((N + 2 * kBM - 1) / (2 * kBM)); }
+
+void fwd_split_plan(int units, int num_sms, int n_kv, int* n_full, int* splits) {
+  *n_full = units;
+  *splits = 1;
+  if (num_sms <= 0 || units <= 0) return;
+  const int tail = units % num_sms;
+  if (tail == 0) return;
+  int s = num_sms / tail;         // CTAs per tail unit that still fit in one wave
+  if (s > 4) s = 4;
+  // Each part must keep at least 8 K/V tiles: shorter parts cost more in
+  // per-CTA start-up, fp32 partial writes and the merge than they save
+  // (measured on GB300 with 8 tiles per unit split in two).
+  while (s > 1 && n_kv / s < 8) --s;
+  if (s < 2) return;
+  *splits = s;
+  *n_full = units - tail;
+}
 
 size_t fwd_bf16_smem_bytes(int d) {
   return d == 64 ? FwdLayout<64>::kBytes : FwdLayout<128>::kBytes;

@@ -22,7 +22,19 @@ struct FwdArgs {
   float scale_log2;       // scale · log2(e): scores are handled in base 2
   int causal;
   unsigned int* fault;
+  // Non-causal load balancing: two-tile units [0, n_full) run whole; each of
+  // the remaining units runs as `splits` CTAs over K/V sub-ranges writing
+  // fp32 partials (opart [slots·256, d], lpart [slots·256]) that a combine
+  // kernel merges.  splits = 1 (or n_full = all units) disables it.
+  int n_full, splits;
+  float* opart;
+  float* lpart;
 };
+// Two-tile (256-query) work units of the forward.
+int fwd_units(int B, int H, int N);
+// Split plan for `units` equal units of `n_kv` K/V tiles on `num_sms` SMs: the
+// units of the last, partial wave are split when that fills the GPU better.
+void fwd_split_plan(int units, int num_sms, int n_kv, int* n_full, int* splits);
 size_t fwd_bf16_smem_bytes(int d);
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s);
 

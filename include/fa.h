@@ -77,18 +77,36 @@ const char* fa_status_string(fa_status s);
 int fa_version(void);
 
 /*
+ * Bytes of optional device workspace that lets fa_fwd balance its last wave
+ * of work across the GPU (0 when it would not: causal masks, FA_DTYPE_FP32,
+ * or no partial last wave).  Depends on the current device's SM count (one
+ * CUDA attribute query, cached); returns 0 for invalid arguments or when no
+ * device is available.
+ */
+size_t fa_fwd_workspace_size(int B, int H, int N, int d, int causal, fa_dtype dtype);
+
+/*
  * Forward.  Reads q, k, v; writes o [B,H,N,d] and lse [B,H,N] (float32).
  * Cited: "Flash Attention" tutorial, 2.Online Softmax §4.2 (one pass over
  * K/V tiles, deferred normalisation) and 3.Recomputation 三 (the saved L).
+ * `workspace` is optional: NULL runs every 256-query unit of work in one CTA.
+ * With at least fa_fwd_workspace_size() bytes (256-byte aligned) the units of
+ * the last, partial wave are split over K/V ranges whose partial results are
+ * merged on the device with the log-sum-exp form of the two-block merge
+ * (2.Online Softmax §3.1, §七); results differ from the unsplit run only by
+ * floating-point rounding.  A non-NULL workspace that is misaligned or too
+ * small returns FA_ERR_WORKSPACE.
  */
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                  int B, int H, int N, int d, float scale, int causal,
-                 fa_dtype dtype, fa_stream_t stream);
+                 fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                 fa_stream_t stream);
 
 /*
  * Bytes of device workspace fa_bwd needs for this problem (0 for an empty
  * one).  BF16: D and the base-2 LSE (4·B·H·N bytes each) plus a float32 dQ
- * accumulator (4·B·H·N·d bytes), each part padded to 256 bytes.  FP32: D only.
+ * accumulator (4·B·H·N·d bytes), each part padded to 256 bytes.  FP32: D and
+ * a copy of LSE (4·B·H·N bytes each, padded to 256).
  * Pure host arithmetic; returns 0 for invalid arguments.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d, fa_dtype dtype);
@@ -114,7 +132,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
  * The three stages of fa_bwd, exposed so each can be timed on its own.  They
  * must run in this order on one stream with the same workspace and sizes.
  *   fa_bwd_prep      — "反向传播的公式推导" 五 (预处理): D_i = Σ_k dO_ik O_ik in
- *                      float32, LSE converted to base 2, dQ accumulator zeroed.
+ *                      float32 and a copy of LSE (bf16 stores −D and
+ *                      −LSE·log2(e) for the tiled stage), dQ accumulator zeroed.
  *   fa_bwd_tiles     — the tiled loop of 六: recompute S and P per tile, then
  *                      dV += Pᵀ dO, dP = dO Vᵀ, dS = P ⊙ (dP - D), dK += dSᵀ Q
  *                      and dQ += dS K (into the accumulator); writes dk, dv.

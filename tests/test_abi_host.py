@@ -60,8 +60,8 @@ FAKE = ctypes.c_void_p(0x10000)       # 16-byte aligned, never dereferenced
 ODD = ctypes.c_void_p(0x10008)        # 8-byte aligned only
 
 
-def _fwd(L, ptr=FAKE, B=1, H=1, N=128, d=128, scale=0.1, causal=0, dtype=0):
-    return L.fa_fwd(ptr, FAKE, FAKE, FAKE, FAKE, B, H, N, d, scale, causal, dtype, None)
+def _fwd(L, ptr=FAKE, B=1, H=1, N=128, d=128, scale=0.1, causal=0, dtype=0, ws=None):
+    return L.fa_fwd(ptr, FAKE, FAKE, FAKE, FAKE, B, H, N, d, scale, causal, dtype, ws, 0 if ws is None else 1, None)
 
 
 @pytest.mark.parametrize("kwargs,code", [
@@ -70,6 +70,7 @@ def _fwd(L, ptr=FAKE, B=1, H=1, N=128, d=128, scale=0.1, causal=0, dtype=0):
     (dict(ptr=ctypes.c_void_p(0)), 1),
     (dict(N=200), 2), (dict(d=96), 2), (dict(d=256, dtype=1), 2),
     (dict(ptr=ODD), 3),
+    (dict(ws=ctypes.c_void_p(0x10010)), 4),
     (dict(N=0), 0), (dict(B=0, ptr=ctypes.c_void_p(0)), 0),
 ])
 def test_forward_argument_checks(L, kwargs, code):

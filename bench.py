@@ -129,6 +129,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ ranks
+
+
+def max_over_ranks(ms, device, world):
+    """The slowest rank's timed region (every rank returns the same value)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step_per_rank, steps, slowest_ms, world):
+    """Whole-job throughput: every rank runs its own batch (weak scaling), so
+    the job does world × steps × flops in the slowest rank's time."""
+    return world * flops_per_step_per_rank * steps / (slowest_ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ GPU arm
 
 
@@ -201,13 +219,10 @@ def run_ours(args, w, rank, world):
     t_bwd = [ev[i][1].elapsed_time(ev[i][4]) for i in range(args.steps)]
     t_tiles = [ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps)]
     total_ms = sum(t_step)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, dev, world)
     ms_per_step = total_ms / args.steps
     flops_fwd, flops_bwd = w.flops_fwd(), w.flops_bwd()
-    value = world * (flops_fwd + flops_bwd) * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_tflops(flops_fwd + flops_bwd, args.steps, total_ms, world)
     fwd_tflops = flops_fwd / (statistics.mean(t_fwd) * 1e-3) / 1e12
     bwd_tflops = flops_bwd / (statistics.mean(t_bwd) * 1e-3) / 1e12
     tiles_tflops = flops_bwd / (statistics.mean(t_tiles) * 1e-3) / 1e12

@@ -18,3 +18,4 @@ from .binding import (  # noqa: F401
     status_string,
     sync_status,
 )
+from .autograd import attention  # noqa: F401,E402

@@ -46,16 +46,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return f;
 }
 
-// 2-D map over a [rows, d] bf16 row-major matrix; boxes of 64 columns
-// (128 bytes) × box_rows rows, 128-byte swizzle.
-bool encode_bf16_rows(CUtensorMap* m, const void* base, unsigned long long rows, int d, int box_rows) {
+// 3-D map over a [B·H, N, d] bf16 tensor; boxes of 64 columns (128 bytes) ×
+// box_rows rows of one head, 128-byte swizzle.  Rows past N read as zero, so
+// a tile at the end of a head never picks up the next head's rows.
+bool encode_bf16_heads(CUtensorMap* m, const void* base, long long heads, long long N, int d, int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * (cuuint64_t)d * 2};
+  cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -69,6 +70,9 @@ struct Shape {
   long long B, H, N, d;
   long long rows() const { return B * H * N; }
   long long elems() const { return B * H * N * d; }
+  // bf16 per-row workspace arrays are padded to whole 128-row tiles per head
+  long long n_pad() const { return (N + 127) / 128 * 128; }
+  long long rows_pad() const { return B * H * n_pad(); }
   bool empty() const { return B == 0 || H == 0 || N == 0; }
 };
 
@@ -80,8 +84,7 @@ fa_status check_shape(int B, int H, int N, int d, fa_dtype dtype, Shape* out) {
   if (!s.empty()) {
     if (dtype == FA_DTYPE_BF16) {
       if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-      if (N % 128 != 0) return FA_ERR_UNSUPPORTED;
-      if (s.rows() >= (1ll << 31) || N / 128 > 65535) return FA_ERR_UNSUPPORTED;
+      if (s.rows_pad() >= (1ll << 31) || s.n_pad() / 128 > 65535 || s.B * s.H > 65535) return FA_ERR_UNSUPPORTED;
     } else {
       if (d > 128) return FA_ERR_UNSUPPORTED;
       if (s.B * s.H > 65535 || s.rows() >= (1ll << 31)) return FA_ERR_UNSUPPORTED;
@@ -110,13 +113,14 @@ fa_status check_ptrs(std::initializer_list<const void*> ptrs, fa_dtype dtype) {
 
 size_t workspace_bytes_for(const Shape& s, fa_dtype dtype) {
   if (s.empty()) return 0;
-  const size_t rows = (size_t)s.rows();
-  if (dtype == FA_DTYPE_FP32) return 2 * pad256(rows * 4);
-  return 2 * pad256(rows * 4) + pad256((size_t)s.elems() * 4);
+  if (dtype == FA_DTYPE_FP32) return 2 * pad256((size_t)s.rows() * 4);
+  const size_t rows = (size_t)s.rows_pad();
+  return 2 * pad256(rows * 4) + pad256(rows * (size_t)s.d * 4);
 }
 
 // Workspace parts: D (float32 per row), the forward's LSE per row (base 2 for
 // bf16, natural-log copy for fp32), and for bf16 the float32 dQ accumulator.
+// The bf16 parts hold whole 128-row tiles per head (rows_pad rows).
 struct Workspace {
   float* dvec;
   float* lse2;
@@ -128,7 +132,7 @@ fa_status carve_workspace(const Shape& s, fa_dtype dtype, void* ws, size_t bytes
   if (need == 0) return FA_OK;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || bytes < need) return FA_ERR_WORKSPACE;
   char* p = static_cast<char*>(ws);
-  const size_t rows = (size_t)s.rows();
+  const size_t rows = dtype == FA_DTYPE_FP32 ? (size_t)s.rows() : (size_t)s.rows_pad();
   w->dvec = reinterpret_cast<float*>(p);
   w->lse2 = reinterpret_cast<float*>(p + pad256(rows * 4));
   w->dqacc = dtype == FA_DTYPE_FP32 ? nullptr : reinterpret_cast<float*>(p + 2 * pad256(rows * 4));
@@ -160,7 +164,7 @@ size_t fwd_workspace_bytes(const Shape& s, int causal, fa_dtype dtype, FwdPlan* 
   if (s.empty() || causal || dtype != FA_DTYPE_BF16) return 0;
   const int units = fa::fwd_units((int)s.B, (int)s.H, (int)s.N);
   int n_full, splits;
-  fa::fwd_split_plan(units, sm_count_current_device(), (int)(s.N / 128), &n_full, &splits);
+  fa::fwd_split_plan(units, sm_count_current_device(), (int)(s.n_pad() / 128), &n_full, &splits);
   if (splits <= 1 || n_full >= units) return 0;
   const size_t rows = (size_t)(units - n_full) * (size_t)splits * 256;
   const size_t opart = pad256(rows * (size_t)s.d * 4);
@@ -214,9 +218,9 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                                         static_cast<const float*>(v), static_cast<float*>(o), lse, (int)(s.B * s.H),
                                         N, d, scale, causal, cs));
   fa::FwdArgs a;
-  if (!encode_bf16_rows(&a.tm_q, q, (unsigned long long)s.rows(), d, 128) ||
-      !encode_bf16_rows(&a.tm_k, k, (unsigned long long)s.rows(), d, 128) ||
-      !encode_bf16_rows(&a.tm_v, v, (unsigned long long)s.rows(), d, 128))
+  const long long heads = s.B * s.H;
+  if (!encode_bf16_heads(&a.tm_q, q, heads, N, d, 128) || !encode_bf16_heads(&a.tm_k, k, heads, N, d, 128) ||
+      !encode_bf16_heads(&a.tm_v, v, heads, N, d, 128))
     return FA_ERR_CUDA;
   a.o = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
@@ -265,11 +269,12 @@ fa_status fa_bwd_prep(const void* o, const void* dO, const float* lse, int B, in
                                              w.lse2, s.rows(), d, cs));
   return from_cuda(fa::launch_bwd_prep_bf16(static_cast<const __nv_bfloat16*>(o),
                                             static_cast<const __nv_bfloat16*>(dO), lse, w.dvec, w.lse2, w.dqacc,
-                                            s.rows(), d, cs));
+                                            s.B * s.H, N, (int)s.n_pad(), d, cs));
 }
 
-fa_status fa_bwd_tiles(const void* q, const void* k, const void* v, const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
-                                fa_dtype dtype, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+fa_status fa_bwd_tiles(const void* q, const void* k, const void* v, const void* dO, void* dq, void* dk, void* dv,
+                       int B, int H, int N, int d, float scale, int causal, fa_dtype dtype, void* workspace,
+                       size_t workspace_bytes, fa_stream_t stream) {
   Shape s;
   fa_status st = check_shape(B, H, N, d, dtype, &s);
   if (st != FA_OK) return st;
@@ -290,9 +295,9 @@ fa_status fa_bwd_tiles(const void* q, const void* k, const void* v, const void* 
   if (!fault) return FA_ERR_CUDA;
   fa::BwdArgs a;
   const int bm = fa::bwd_bf16_block_m(d);
-  const unsigned long long rows = (unsigned long long)s.rows();
-  if (!encode_bf16_rows(&a.tm_q, q, rows, d, bm) || !encode_bf16_rows(&a.tm_k, k, rows, d, 128) ||
-      !encode_bf16_rows(&a.tm_v, v, rows, d, 128) || !encode_bf16_rows(&a.tm_do, dO, rows, d, bm))
+  const long long heads = s.B * s.H;
+  if (!encode_bf16_heads(&a.tm_q, q, heads, N, d, bm) || !encode_bf16_heads(&a.tm_k, k, heads, N, d, 128) ||
+      !encode_bf16_heads(&a.tm_v, v, heads, N, d, 128) || !encode_bf16_heads(&a.tm_do, dO, heads, N, d, bm))
     return FA_ERR_CUDA;
   a.lse2 = w.lse2;
   a.dvec = w.dvec;
@@ -320,8 +325,8 @@ fa_status fa_bwd_dq_finish(void* dq, int B, int H, int N, int d, float scale, fa
   if ((st = check_ptrs({dq}, dtype)) != FA_OK) return st;
   Workspace w;
   if ((st = carve_workspace(s, dtype, workspace, workspace_bytes, &w)) != FA_OK) return st;
-  return from_cuda(fa::launch_dq_finish_bf16(w.dqacc, static_cast<__nv_bfloat16*>(dq), s.elems(), scale,
-                                             reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(fa::launch_dq_finish_bf16(w.dqacc, static_cast<__nv_bfloat16*>(dq), s.B * s.H, N,
+                                             (int)s.n_pad(), d, scale, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,

@@ -152,9 +152,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
   const int jt = CAUSAL ? (int)blockIdx.y : (int)blockIdx.x;
   const int bh = CAUSAL ? (int)blockIdx.x : (int)blockIdx.y;
   const int kv0 = jt * kBN;
-  const int row0 = bh * N;
+  const int row0 = bh * N;                   // first row of this head in O, dK, dV
+  const int n_tiles = (N + kBM - 1) / kBM;   // tiles per head; the last may be ragged
+  const long long wrow0 = (long long)bh * n_tiles * kBM;   // first row of this head in the workspace
   const int i0 = CAUSAL ? jt : 0;            // first query tile with a visible query (kBM == kBN)
-  const int n = N / kBM - i0;                // query tiles visited
+  const int n = n_tiles - i0;                // query tiles visited
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kKVFull), 1);
@@ -187,6 +189,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
     const int h = warp >> 2;                       // query columns [64h, 64h + 64)
     const int r = g * 32 + lane;                   // key row within the tile = TMEM lane
     const int kv = kv0 + r;
+    // A key past N (last tile of a ragged head) reads as a zero row, so its
+    // score is 0 and 2^(−LSE·log2 e) could overflow; its Pᵀ and dSᵀ are set
+    // to 0 so that dQ never sees it.  Queries past N need nothing: their
+    // −LSE is −∞ and their dO row is zero.
+    const bool dead_key = kv >= N;
     const uint32_t lane_off = (uint32_t)(g * 32) << 16;
     const float sl2 = a.scale_log2;
     const uint32_t ds_tile = sbase + C::kDS;
@@ -216,6 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
             p_chunk<true, kPolyEvery>(s, sl2x2, nlse + (c0 >> 1), r - c0, p + ch * 16);
           else
             p_chunk<false, kPolyEvery>(s, sl2x2, nlse + (c0 >> 1), r - c0, p + ch * 16);
+        }
+        if (dead_key) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) p[e] = 0ull;
         }
       }
       // Both warps of the lane quarter have read their Sᵀ columns; Pᵀ may now
@@ -277,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         tmem_ld_x64(tmem + lane_off + C::kColDP + (uint32_t)(64 * h), v);
         tc_fence_before();
         mbar_arrive(bar(kDqDrained));
-        float* base = a.dqacc + ((size_t)row0 + (size_t)q0 + (size_t)(64 * h)) * D + (size_t)r;
+        float* base = a.dqacc + ((size_t)wrow0 + (size_t)q0 + (size_t)(64 * h)) * D + (size_t)r;
 #pragma unroll
         for (int c = 0; c < 64; ++c) red_add_f32(base + (size_t)c * D, u2f(v[c]));
       } else {
@@ -287,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         tmem_ld_x32(tmem + lane_off + C::kColDP + (uint32_t)(32 * h), v);
         tc_fence_before();
         mbar_arrive(bar(kDqDrained));
-        float* base = a.dqacc + ((size_t)row0 + (size_t)q0 + (size_t)r) * D + (size_t)(32 * h);
+        float* base = a.dqacc + ((size_t)wrow0 + (size_t)q0 + (size_t)r) * D + (size_t)(32 * h);
 #pragma unroll
         for (int c = 0; c < 32; c += 4) red_add_v4_f32(base + c, u2f(v[c]), u2f(v[c + 1]), u2f(v[c + 2]), u2f(v[c + 3]));
       }
@@ -305,13 +316,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t v[32];
-        tmem_ld_x32(tmem + lane_off + col + 32 * cc, v);
+        tmem_ld_x32(tmem + lane_off + col + 32 * cc, v);   // warp-collective: every lane loads
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(v[2 * e]) * mul, u2f(v[2 * e + 1]) * mul);
+        if (!dead_key) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          st_global_v4(dst + 32 * cc + 8 * u, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          for (int u = 0; u < 4; ++u)
+            st_global_v4(dst + 32 * cc + 8 * u, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
       }
     }
   } else if (warp == kTmaWarp) {
@@ -323,8 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       prefetch_tmap(&a.tm_do);
       mbar_arrive_expect_tx(bar(kKVFull), 2u * C::kTile);
       for (int bx = 0; bx < D / 64; ++bx) {
-        tma_load_2d(sbase + C::kK + bx * kBox, &a.tm_k, bar(kKVFull), 64 * bx, row0 + kv0);
-        tma_load_2d(sbase + C::kV + bx * kBox, &a.tm_v, bar(kKVFull), 64 * bx, row0 + kv0);
+        tma_load_3d(sbase + C::kK + bx * kBox, &a.tm_k, bar(kKVFull), 64 * bx, kv0, bh);
+        tma_load_3d(sbase + C::kV + bx * kBox, &a.tm_v, bar(kKVFull), 64 * bx, kv0, bh);
       }
       int issued[2] = {0, 0};
       for (int i = 0; i < n; ++i) {
@@ -333,11 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         const int q0 = (i0 + i) * kBM;
         mbar_arrive_expect_tx(bar(kQFull + s), 2u * C::kTile + 2u * kBM * 4);
         for (int bx = 0; bx < D / 64; ++bx) {
-          tma_load_2d(sbase + C::kQ + s * C::kTile + bx * kBox, &a.tm_q, bar(kQFull + s), 64 * bx, row0 + q0);
-          tma_load_2d(sbase + C::kDO + s * C::kTile + bx * kBox, &a.tm_do, bar(kQFull + s), 64 * bx, row0 + q0);
+          tma_load_3d(sbase + C::kQ + s * C::kTile + bx * kBox, &a.tm_q, bar(kQFull + s), 64 * bx, q0, bh);
+          tma_load_3d(sbase + C::kDO + s * C::kTile + bx * kBox, &a.tm_do, bar(kQFull + s), 64 * bx, q0, bh);
         }
-        bulk_load(sbase + C::kLSE + s * kBM * 4, a.lse2 + row0 + q0, kBM * 4, bar(kQFull + s));
-        bulk_load(sbase + C::kDV + s * kBM * 4, a.dvec + row0 + q0, kBM * 4, bar(kQFull + s));
+        bulk_load(sbase + C::kLSE + s * kBM * 4, a.lse2 + wrow0 + q0, kBM * 4, bar(kQFull + s));
+        bulk_load(sbase + C::kDV + s * kBM * 4, a.dvec + wrow0 + q0, kBM * 4, bar(kQFull + s));
         ++issued[s];
       }
       mbar_wait_drain(bar(kKVFull), 0, wc, site(8));
@@ -440,7 +453,7 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t s) {
   const size_t smem = BwdCfg<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const unsigned tiles = (unsigned)(a.N / kBN), heads = (unsigned)(a.B * a.H);
+  const unsigned tiles = (unsigned)((a.N + kBN - 1) / kBN), heads = (unsigned)(a.B * a.H);
   const dim3 grid = CAUSAL ? dim3(heads, tiles) : dim3(tiles, heads);
   kern<<<grid, kThreads, smem, s>>>(a);
   return cudaGetLastError();
@@ -448,22 +461,32 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t s) {
 
 // ------------------------------------------------------------------ pre-pass and dQ finish
 
-// One group of D/8 threads per row; each thread reads 8 bf16 of O and of dO
-// (16 bytes each), so a warp covers 32·8 contiguous elements.
+// One group of D/8 threads per workspace row (n_pad rows per head); each thread
+// reads 8 bf16 of O and of dO (16 bytes each), so a warp covers 32·8
+// contiguous elements.  Rows past N in a head are padding: D = 0, −LSE = −∞.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                        const __nv_bfloat16* __restrict__ dO,
                                                        const float* __restrict__ lse, float* __restrict__ dvec,
                                                        float* __restrict__ lse2, float* __restrict__ dqacc,
-                                                       long long rows) {
+                                                       long long rows_pad, int N, int n_pad) {
   constexpr int G = D / 8;   // threads per row
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long row = tid / G;
+  const long long row = tid / G;           // workspace row
   const int part = (int)(tid % G);
+  const long long head = row / n_pad;
+  const int pos = (int)(row - head * n_pad);
+  const long long src = head * N + pos;    // row of O, dO and LSE
+  const bool live = row < rows_pad && pos < N;
   float acc = 0.f;
-  if (row < rows) {
-    const uint4 ov = *reinterpret_cast<const uint4*>(o + row * D + part * 8);
-    const uint4 gv = *reinterpret_cast<const uint4*>(dO + row * D + part * 8);
+  if (row < rows_pad) {
+    float4* z = reinterpret_cast<float4*>(dqacc + row * D + part * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (live) {
+    const uint4 ov = *reinterpret_cast<const uint4*>(o + src * D + part * 8);
+    const uint4 gv = *reinterpret_cast<const uint4*>(dO + src * D + part * 8);
     const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(&ov);
     const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(&gv);
 #pragma unroll
@@ -473,25 +496,31 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
       acc = fmaf(a2.x, b2.x, acc);
       acc = fmaf(a2.y, b2.y, acc);
     }
-    float4* z = reinterpret_cast<float4*>(dqacc + row * D + part * 8);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
   for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
-  if (row < rows && part == 0) {
+  if (row < rows_pad && part == 0) {
     // Stored negated: the tiled kernel adds them with packed f32x2 operations.
-    dvec[row] = -acc;
-    lse2[row] = -lse[row] * 1.4426950408889634074f;
+    dvec[row] = live ? -acc : 0.f;
+    lse2[row] = live ? -lse[src] * 1.4426950408889634074f : -INFINITY;
   }
 }
 
+// One thread per 8 consecutive dQ elements of a live row; the accumulator has
+// n_pad rows per head, dQ has N.
+template <int D>
 __global__ void __launch_bounds__(256) dq_finish_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
-                                                        long long n8, float scale) {
+                                                        long long n8, int N, int n_pad, float scale) {
+  constexpr int G = D / 8;
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n8) return;
-  const float4 a0 = reinterpret_cast<const float4*>(acc)[2 * i];
-  const float4 a1 = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+  const long long row = i / G;
+  const int part = (int)(i - row * G);
+  const long long head = row / N;
+  const long long arow = row + head * (long long)(n_pad - N);
+  const float4* a = reinterpret_cast<const float4*>(acc + arow * D + part * 8);
+  const float4 a0 = a[0];
+  const float4 a1 = a[1];
   uint4 out;
   out.x = pack_bf16x2(a0.x * scale, a0.y * scale);
   out.y = pack_bf16x2(a0.z * scale, a0.w * scale);
@@ -513,23 +542,30 @@ cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_bwd_prep_bf16(const __nv_bfloat16* o, const __nv_bfloat16* dO, const float* lse, float* dvec,
-                                 float* lse2, float* dqacc, long long rows, int d, cudaStream_t s) {
-  const long long threads = rows * (d / 8);
+                                 float* lse2, float* dqacc, long long heads, int N, int n_pad, int d,
+                                 cudaStream_t s) {
+  const long long rows_pad = heads * n_pad;
+  const long long threads = rows_pad * (d / 8);
   const unsigned blocks = (unsigned)((threads + 255) / 256);
   if (d == 128)
-    bwd_prep_kernel<128><<<blocks, 256, 0, s>>>(o, dO, lse, dvec, lse2, dqacc, rows);
+    bwd_prep_kernel<128><<<blocks, 256, 0, s>>>(o, dO, lse, dvec, lse2, dqacc, rows_pad, N, n_pad);
   else if (d == 64)
-    bwd_prep_kernel<64><<<blocks, 256, 0, s>>>(o, dO, lse, dvec, lse2, dqacc, rows);
+    bwd_prep_kernel<64><<<blocks, 256, 0, s>>>(o, dO, lse, dvec, lse2, dqacc, rows_pad, N, n_pad);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
-cudaError_t launch_dq_finish_bf16(const float* dqacc, __nv_bfloat16* dq, long long elems, float scale,
-                                  cudaStream_t s) {
-  const long long n8 = elems / 8;
+cudaError_t launch_dq_finish_bf16(const float* dqacc, __nv_bfloat16* dq, long long heads, int N, int n_pad, int d,
+                                  float scale, cudaStream_t s) {
+  const long long n8 = heads * N * (d / 8);
   const unsigned blocks = (unsigned)((n8 + 255) / 256);
-  dq_finish_kernel<<<blocks, 256, 0, s>>>(dqacc, dq, n8, scale);
+  if (d == 128)
+    dq_finish_kernel<128><<<blocks, 256, 0, s>>>(dqacc, dq, n8, N, n_pad, scale);
+  else if (d == 64)
+    dq_finish_kernel<64><<<blocks, 256, 0, s>>>(dqacc, dq, n8, N, n_pad, scale);
+  else
+    return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 

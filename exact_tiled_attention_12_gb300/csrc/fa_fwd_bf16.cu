@@ -135,7 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
   // heads' K/V and they stay in L2; the last `tail` units are split into
   // `splits` CTAs over equal K/V sub-ranges, each writing a partial result
   // (normalised O and LSE of its keys) that fwd_combine merges.
-  int bh, pair, kv_begin = 0, n_kv = N / kBN, part_slot = -1;
+  const int n_kv_all = (N + kBN - 1) / kBN;
+  int bh, pair, kv_begin = 0, n_kv = n_kv_all, part_slot = -1;
   const int idx = (int)blockIdx.x;
   if (CAUSAL) {
     bh = idx % (a.B * a.H);
@@ -154,6 +155,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
   }
   const int q0 = pair * 2 * kBM;
   const int row0 = bh * N;                                 // first row of this head in the [B·H·N, d] view
+  // Keys of the head's last K/V tile that exist (128 unless N is ragged).
+  // Non-causal rows must not see the zero-filled keys past N; causal rows
+  // never do, since those keys lie above the diagonal of every real query.
+  const int kv_tail = N - (n_kv_all - 1) * kBN;
+  const bool ragged_last = !CAUSAL && kv_tail < kBN && kv_begin + n_kv == n_kv_all;
 
   // Number of K/V tiles each query tile visits (0 if the tile is past N).
   int n_t[2];
@@ -213,6 +219,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
         for (int c = 0; c < 128; ++c)
           if (c > r) s[c] = f2u(-INFINITY);
       }
+      if (!CAUSAL && ragged_last && j == nt - 1) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c >= kv_tail) s[c] = f2u(-INFINITY);
+      }
       // Row max: four independent chains of 3-input maxima.
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
@@ -241,10 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
       }
       ell *= alpha;
       m_ref = m_new;
-      // The causal diagonal tile takes every exponential on MUFU, so masked
-      // scores give exactly 0.
+      // Masked tiles take every exponential on MUFU, so masked scores give
+      // exactly 0.
       const uint32_t p_addr = tmem + lane_off + s_col(t);
-      if (CAUSAL && j == nt - 1)
+      if ((CAUSAL || ragged_last) && j == nt - 1)
         ell += exp_tile_to_p<0>(s, sl2, m_ref, p_addr);
       else
         ell += exp_tile_to_p<kPolyEvery>(s, sl2, m_ref, p_addr);
@@ -262,6 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
         // LSE in natural log of the scaled scores: (m + log2 ℓ) · ln 2.
         const float lse = (m_ref + log2f(ell)) * 0.69314718055994530942f;
         if (part_slot < 0) {
+          // tcgen05.ld is warp-collective: every lane loads, and only rows
+          // below N (the last tile of a ragged head) are stored.
+          const bool live = q < N;
           __nv_bfloat16* orow = a.o + ((size_t)row0 + (size_t)q) * D;
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
@@ -270,11 +284,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
+            if (live) {
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              st_global_v4(orow + 32 * cc + 8 * v4, pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+              for (int v4 = 0; v4 < 4; ++v4)
+                st_global_v4(orow + 32 * cc + 8 * v4, pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+            }
           }
-          a.lse[(size_t)row0 + (size_t)q] = lse;
+          if (live) a.lse[(size_t)row0 + (size_t)q] = lse;
         } else {
           // Partial over this CTA's keys: normalised O and LSE in fp32.
           const size_t prow = (size_t)part_slot * (2 * kBM) + (size_t)(t * kBM + r);
@@ -307,22 +323,22 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
         for (int t = 0; t < 2; ++t)
           if (n_t[t] > 0)
             for (int b = 0; b < D / 64; ++b)
-              tma_load_2d(sbase + L::kQ + t * L::kTile + b * kBoxBytes, &a.tm_q, bar(kQFull), 64 * b,
-                          row0 + q0 + t * kBM);
+              tma_load_3d(sbase + L::kQ + t * L::kTile + b * kBoxBytes, &a.tm_q, bar(kQFull), 64 * b,
+                          q0 + t * kBM, bh);
       }
       for (int j = 0; j < J; ++j) {
         const int s = j & 1;
         if (j >= 2 && !mbar_wait(bar(kKEmpty + s), (uint32_t)(((j >> 1) - 1) & 1), wc, site(3))) break;
         mbar_arrive_expect_tx(bar(kKFull + s), tile);
         for (int b = 0; b < D / 64; ++b)
-          tma_load_2d(sbase + L::kK + s * L::kTile + b * kBoxBytes, &a.tm_k, bar(kKFull + s), 64 * b,
-                      row0 + (kv_begin + j) * kBN);
+          tma_load_3d(sbase + L::kK + s * L::kTile + b * kBoxBytes, &a.tm_k, bar(kKFull + s), 64 * b,
+                      (kv_begin + j) * kBN, bh);
         ++issued_k[s];
         if (j >= 2 && !mbar_wait(bar(kVEmpty + s), (uint32_t)(((j >> 1) - 1) & 1), wc, site(4))) break;
         mbar_arrive_expect_tx(bar(kVFull + s), tile);
         for (int b = 0; b < D / 64; ++b)
-          tma_load_2d(sbase + L::kV + s * L::kTile + b * kBoxBytes, &a.tm_v, bar(kVFull + s), 64 * b,
-                      row0 + (kv_begin + j) * kBN);
+          tma_load_3d(sbase + L::kV + s * L::kTile + b * kBoxBytes, &a.tm_v, bar(kVFull + s), 64 * b,
+                      (kv_begin + j) * kBN, bh);
         ++issued_v[s];
       }
       // Never leave the CTA with copies in flight: wait for the last load of

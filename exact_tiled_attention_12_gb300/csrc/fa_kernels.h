@@ -12,8 +12,9 @@ namespace fa {
 
 // ---------------------------------------------------------------- bf16 tensor-core path
 
-// Forward: 2-D tensor maps over the [B·H·N, d] bf16 row view of Q, K, V with
-// 64-column (128-byte) boxes of 128 rows and 128-byte swizzle.
+// Forward: 3-D tensor maps over the [B·H, N, d] bf16 view of Q, K, V with
+// boxes of 64 columns (128 bytes) × 128 rows of one head and 128-byte swizzle;
+// rows past N read as zero, so N need not be a multiple of 128.
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v;
   __nv_bfloat16* o;
@@ -38,13 +39,13 @@ void fwd_split_plan(int units, int num_sms, int n_kv, int* n_full, int* splits);
 size_t fwd_bf16_smem_bytes(int d);
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s);
 
-// Backward tiled loop.  tm_k / tm_v: boxes of 128 rows; tm_q / tm_do: boxes
-// of BM rows (BM = 64 for d = 128, 128 for d = 64).
+// Backward tiled loop.  Tensor maps as in the forward (3-D, 128-row boxes).
+// The workspace arrays hold n_pad = 128·⌈N/128⌉ rows per head.
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
-  const float* lse2;      // workspace: −LSE · log2(e), [B·H·N]
-  const float* dvec;      // workspace: −D = −rowsum(dO ⊙ O), [B·H·N]
-  float* dqacc;           // workspace: fp32 dQ accumulator, [B·H·N, d]
+  const float* lse2;      // workspace: −LSE · log2(e), [B·H·n_pad]
+  const float* dvec;      // workspace: −D = −rowsum(dO ⊙ O), [B·H·n_pad]
+  float* dqacc;           // workspace: fp32 dQ accumulator, [B·H·n_pad, d]
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int B, H, N, d;
@@ -57,13 +58,15 @@ int bwd_bf16_block_m(int d);
 size_t bwd_bf16_smem_bytes(int d);
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t s);
 
-// Backward pre-pass: D = rowsum(dO ⊙ O), LSE in base 2, zero dQ accumulator.
+// Backward pre-pass: −D = −rowsum(dO ⊙ O) and −LSE·log2(e) per row, dQ
+// accumulator zeroed.  The workspace arrays hold n_pad ≥ N rows per head
+// (whole 128-row tiles); padding rows get −LSE = −∞ (so P = 0) and D = 0.
 cudaError_t launch_bwd_prep_bf16(const __nv_bfloat16* o, const __nv_bfloat16* dO, const float* lse,
-                                 float* dvec, float* lse2, float* dqacc, long long rows, int d,
+                                 float* dvec, float* lse2, float* dqacc, long long heads, int N, int n_pad, int d,
                                  cudaStream_t s);
-// dQ = scale · accumulator, rounded to bf16.
-cudaError_t launch_dq_finish_bf16(const float* dqacc, __nv_bfloat16* dq, long long elems, float scale,
-                                  cudaStream_t s);
+// dQ = scale · accumulator (n_pad rows per head), rounded to bf16 [heads, N, d].
+cudaError_t launch_dq_finish_bf16(const float* dqacc, __nv_bfloat16* dq, long long heads, int N, int n_pad, int d,
+                                  float scale, cudaStream_t s);
 
 // ---------------------------------------------------------------- fp32 SIMT path
 

@@ -23,7 +23,9 @@
  *   dtype       FA_DTYPE_BF16: every [B,H,N,d] tensor is bfloat16; arithmetic
  *               is fp32 accumulation on the tensor cores, P and dS are rounded
  *               to bf16 before their products.  Supported: d ∈ {64, 128},
- *               N a multiple of 128, base pointers 16-byte aligned.
+ *               any N ≥ 1 (tiles of 128 rows; a ragged last tile reads zero
+ *               rows past N and masks those keys), base pointers 16-byte
+ *               aligned.
  *               FA_DTYPE_FP32: every tensor is float32 and computed with
  *               fp32 arithmetic (no tensor cores); any N ≥ 1, 1 ≤ d ≤ 128.
  *   causal      0: every key visible.  1: key j visible to query i iff j ≤ i
@@ -61,7 +63,7 @@ typedef struct CUstream_st* fa_stream_t;
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad scale/causal/dtype */
-  FA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (bf16 d∉{64,128}, N%128≠0, fp32 d>128) */
+  FA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (bf16 d∉{64,128}, fp32 d>128, sizes past the grid limits) */
   FA_ERR_MISALIGNED = 3,   /* bf16 base pointer not 16-byte aligned */
   FA_ERR_WORKSPACE = 4,    /* workspace NULL, misaligned (256 B) or too small */
   FA_ERR_CUDA = 5,         /* a CUDA runtime/driver call or launch failed */
@@ -104,8 +106,9 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 
 /*
  * Bytes of device workspace fa_bwd needs for this problem (0 for an empty
- * one).  BF16: D and the base-2 LSE (4·B·H·N bytes each) plus a float32 dQ
- * accumulator (4·B·H·N·d bytes), each part padded to 256 bytes.  FP32: D and
+ * one).  BF16: D and the base-2 LSE (4·B·H·Np bytes each) plus a float32 dQ
+ * accumulator (4·B·H·Np·d bytes), Np = 128·⌈N/128⌉ (whole tiles per head),
+ * each part padded to 256 bytes.  FP32: D and
  * a copy of LSE (4·B·H·N bytes each, padded to 256).
  * Pure host arithmetic; returns 0 for invalid arguments.
  */
@@ -177,7 +180,7 @@ fa_status fa_sync_status(fa_stream_t stream);
  *   - nothing is allocated, by this call or by anything it calls;
  *   - problems whose fa_bwd_workspace_size() exceeds FA_NOALLOC_SCRATCH_BYTES
  *     are rejected with FA_ERR_WORKSPACE before anything is enqueued (for
- *     bf16 that is 4·B·H·N·(d + 2) bytes plus padding, e.g. B·H·N up to
+ *     bf16 that is 4·B·H·Np·(d + 2) bytes plus padding, e.g. B·H·Np up to
  *     about 64,000 rows at d = 128);
  *   - the first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current and caches it; make

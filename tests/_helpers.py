@@ -10,7 +10,9 @@ import oracle
 # Tolerances (per tensor):
 #   fp32 dtype: every output within 1e-5 max abs of the fp64 oracle.
 #   bf16 dtype (fp32 accumulation): O max abs ≤ 1e-2, LSE max abs ≤ 1e-3,
-#   dQ / dK / dV relative Frobenius error ≤ 2e-2; no inf or NaN anywhere.
+#   dQ / dK / dV relative Frobenius error ≤ 2e-2 (a gradient that is zero by
+#   the closed form — one visible key per row — max abs ≤ 1e-2 instead);
+#   no inf or NaN anywhere.
 FP32_ATOL = 1e-5
 BF16_O_ATOL = 1e-2
 BF16_LSE_ATOL = 1e-3
@@ -64,6 +66,13 @@ def compare(gpu, ref, dtype):
         assert errs["O"] <= BF16_O_ATOL, errs
         assert errs["LSE"] <= BF16_LSE_ATOL, errs
         for key in ("dQ", "dK", "dV"):
+            if np.linalg.norm(ref[key]) <= 1e-9 * np.linalg.norm(ref["dV"]):
+                # Zero by the closed form (every row sees one key: P = 1 and
+                # dS = P ⊙ (dP − D) = 0), so a relative error is undefined;
+                # the rounding noise must stay below the O tolerance instead.
+                errs[key + "_abs_zero"] = errs[key]
+                assert errs[key] <= BF16_O_ATOL, (key, errs)
+                continue
             errs[key + "_relfro"] = rel_fro(gpu[key], ref[key])
             assert errs[key + "_relfro"] <= BF16_GRAD_RTOL_FRO, (key, errs)
     return errs

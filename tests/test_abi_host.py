@@ -52,6 +52,8 @@ def test_workspace_size(L):
     rows, elems = 4 * 32 * 2048, 4 * 32 * 2048 * 128
     assert L.fa_bwd_workspace_size(4, 32, 2048, 128, 0) == 2 * rows * 4 + elems * 4
     assert L.fa_bwd_workspace_size(1, 1, 3, 64, 1) == 2 * 256
+    # bf16 ragged N: whole 128-row tiles per head (200 -> 256 rows)
+    assert L.fa_bwd_workspace_size(2, 1, 200, 64, 0) == 2 * (2 * 256 * 4) + 2 * 256 * 64 * 4
     assert L.fa_bwd_workspace_size(0, 1, 128, 64, 0) == 0
     assert L.fa_bwd_workspace_size(-1, 1, 128, 64, 0) == 0
 
@@ -68,10 +70,11 @@ def _fwd(L, ptr=FAKE, B=1, H=1, N=128, d=128, scale=0.1, causal=0, dtype=0, ws=N
     (dict(B=-1), 1), (dict(N=-5), 1), (dict(d=0), 1), (dict(scale=0.0), 1), (dict(scale=-1.0), 1),
     (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1), (dict(causal=2), 1), (dict(dtype=7), 1),
     (dict(ptr=ctypes.c_void_p(0)), 1),
-    (dict(N=200), 2), (dict(d=96), 2), (dict(d=256, dtype=1), 2),
+    (dict(d=96), 2), (dict(d=256, dtype=1), 2), (dict(B=300, H=300), 2), (dict(N=65535 * 128 + 1), 2),
     (dict(ptr=ODD), 3),
     (dict(ws=ctypes.c_void_p(0x10010)), 4),
     (dict(N=0), 0), (dict(B=0, ptr=ctypes.c_void_p(0)), 0),
+    (dict(N=200, ws=ctypes.c_void_p(0x10010)), 4),   # ragged N passes the shape check
 ])
 def test_forward_argument_checks(L, kwargs, code):
     assert _fwd(L, **kwargs) == code
@@ -89,4 +92,5 @@ def test_backward_argument_checks(L):
     # stage entry points share the same checks
     assert L.fa_bwd_prep(FAKE, FAKE, FAKE, 1, 1, 128, 64, 0, None, 0, None) == 4
     assert L.fa_bwd_tiles(*([FAKE] * 7), 1, 1, 128, 64, 0.125, 0, 0, None, 0, None) == 4
-    assert L.fa_bwd_dq_finish(FAKE, 1, 1, 100, 64, 0.125, 0, None, 0, None) == 2
+    assert L.fa_bwd_dq_finish(FAKE, 1, 1, 100, 64, 0.125, 0, None, 0, None) == 4
+    assert L.fa_bwd_dq_finish(FAKE, 1, 1, 100, 96, 0.125, 0, None, 0, None) == 2

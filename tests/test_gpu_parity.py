@@ -1,8 +1,9 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
 
 Shapes span several tiles, an odd number of 128-row tiles (a half-empty
-two-tile CTA), single-tile heads and both masks; the fp32 dtype also covers
-ragged N and d.  Tolerances are in tests/_helpers.py.
+two-tile CTA), single-tile heads, ragged N (a last tile partly past N) and
+both masks; the fp32 dtype also covers ragged d.  Tolerances are in
+tests/_helpers.py.
 """
 
 import numpy as np
@@ -66,6 +67,11 @@ BF16_SHAPES = [
     (1, 1, 128, 64),
     (1, 2, 1024, 128),  # several K/V stages and ring wrap-around
     (3, 2, 640, 64),
+    (1, 2, 200, 128),   # ragged: one two-tile CTA, the second tile holds 72 rows
+    (2, 1, 333, 64),    # ragged: three tiles, 77 rows in the last
+    (1, 1, 1, 128),     # a single row
+    (1, 1, 127, 64),
+    (2, 2, 1000, 128),  # ragged with several K/V stages
 ]
 
 
@@ -75,7 +81,7 @@ def test_bf16_parity(B, H, N, d, causal):
     _check(B, H, N, d, causal, "bf16", seed=B * 1000 + N + d + int(causal))
 
 
-@pytest.mark.parametrize("B,H,N,d", [(1, 1, 2048, 128), (1, 2, 4096, 64), (2, 1, 2176, 128)])
+@pytest.mark.parametrize("B,H,N,d", [(1, 1, 2048, 128), (1, 2, 4096, 64), (2, 1, 2176, 128), (1, 1, 2100, 128)])
 def test_bf16_split_forward(B, H, N, d):
     """The load-balanced forward (last-wave units split over K/V ranges and
     merged on the device) against the oracle and against the unsplit run."""
@@ -101,6 +107,14 @@ def test_bf16_stress_small():
     """Scores scaled to magnitudes in the hundreds (Q, K drawn ×8, d = 64)."""
     errs = _check(2, 2, 512, 64, False, "bf16", dist="stress", seed=5)
     assert errs["O"] <= 1e-2
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_stress_ragged(causal):
+    """Large scores with a ragged last tile: the zero-filled keys past N score
+    0, far above rows whose scores are all very negative; they must neither
+    enter the softmax nor turn dQ into inf · 0."""
+    _check(2, 1, 300, 64, causal, "bf16", dist="stress", seed=6)
 
 
 # ------------------------------------------------------------------ closed forms on the GPU
@@ -192,8 +206,24 @@ def test_empty_problems(dtype):
 def test_unsupported_shapes_raise():
     import exact_tiled_attention_12_gb300 as fa
 
-    for shape in [(1, 1, 200, 128), (1, 1, 256, 96)]:
+    for shape in [(1, 1, 256, 96), (1, 1, 200, 32)]:
         q, k, v, _ = make_inputs(*shape, "bf16", "normal", 1, device="cuda")
         with pytest.raises(fa.FaError) as e:
             fa.fwd(q, k, v)
         assert e.value.code == 2
+
+
+@pytest.mark.parametrize("dtype,causal", [("bf16", False), ("bf16", True), ("fp32", True)])
+def test_autograd_attention_matches_oracle(dtype, causal):
+    """attention() under torch.autograd: O from forward, dQ/dK/dV from .backward()."""
+    import exact_tiled_attention_12_gb300 as fa
+
+    B, H, N, d = 1, 2, 256, 64
+    q, k, v, do = make_inputs(B, H, N, d, dtype, "normal", 41, device="cuda")
+    q, k, v = (t.clone().requires_grad_(True) for t in (q, k, v))
+    o = fa.attention(q, k, v, causal=causal)
+    o.backward(do)
+    ref = run_oracle_heads(q.detach(), k.detach(), v.detach(), do, causal, d ** -0.5, [(0, 0), (0, 1)])
+    gpu = {"O": to64(o.detach()[0]), "LSE": ref["LSE"], "dQ": to64(q.grad[0]), "dK": to64(k.grad[0]),
+           "dV": to64(v.grad[0])}
+    compare(gpu, ref, dtype)

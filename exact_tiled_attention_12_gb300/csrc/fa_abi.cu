@@ -46,19 +46,23 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return f;
 }
 
-// 3-D map over a [B·H, N, d] bf16 tensor; boxes of 64 columns (128 bytes) ×
-// box_rows rows of one head, 128-byte swizzle.  Rows past N read as zero, so
-// a tile at the end of a head never picks up the next head's rows.
+// Tensor map over a [B·H, N, d] bf16 tensor with boxes of 64 columns (128
+// bytes) × box_rows rows and 128-byte swizzle.  N a multiple of 128: a 2-D
+// map over the [B·H·N, d] row view (a tile never straddles two heads).
+// Otherwise a 3-D map whose rows past N read as zero, so the last tile of a
+// head never picks up the next head's rows.  The kernels pick the matching
+// copy form from N.
 bool encode_bf16_heads(CUtensorMap* m, const void* base, long long heads, long long N, int d, int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)heads};
+  const bool rows_view = N % 128 == 0;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)(rows_view ? heads * N : N), (cuuint64_t)heads};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * (cuuint64_t)d * 2};
   cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rows_view ? 2 : 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

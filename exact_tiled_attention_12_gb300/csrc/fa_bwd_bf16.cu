@@ -124,7 +124,10 @@ __device__ __forceinline__ bool pair_sync_and(int id, bool ok) {
   return r != 0;
 }
 
-template <int D, bool CAUSAL>
+// RAGGED (N not a multiple of 128): 3-D per-head tensor maps whose rows past
+// N read as zero, masking of the keys past N and row-predicated dK/dV
+// stores.  Otherwise 2-D maps over the [B·H·N, d] row view and none of that.
+template <int D, bool CAUSAL, bool RAGGED>
 // 10 warps: at most 3 per SM sub-partition, so up to 168 registers a thread.
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_constant__ BwdArgs a) {
   using C = BwdCfg<D>;
@@ -153,9 +156,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
   const int bh = CAUSAL ? (int)blockIdx.x : (int)blockIdx.y;
   const int kv0 = jt * kBN;
   const int row0 = bh * N;                   // first row of this head in O, dK, dV
-  const int n_tiles = (N + kBM - 1) / kBM;   // tiles per head; the last may be ragged
-  const long long wrow0 = (long long)bh * n_tiles * kBM;   // first row of this head in the workspace
+  const int n_tiles = RAGGED ? (N + kBM - 1) / kBM : N / kBM;   // tiles per head; the last may be ragged
+  // First row of this head in the workspace (whole tiles per head; the
+  // workspace has fewer than 2^31 rows).
+  const int wrow0 = RAGGED ? bh * n_tiles * kBM : row0;
   const int i0 = CAUSAL ? jt : 0;            // first query tile with a visible query (kBM == kBN)
+  // Loads rows [pos, pos + 128) of this head.
+  auto load_rows = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar_addr, int x, int pos) {
+    if constexpr (RAGGED)
+      tma_load_3d(dst, map, bar_addr, x, pos, bh);
+    else
+      tma_load_2d(dst, map, bar_addr, x, row0 + pos);
+  };
   const int n = n_tiles - i0;                // query tiles visited
 
   if (threadIdx.x == 0) {
@@ -190,10 +202,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
     const int r = g * 32 + lane;                   // key row within the tile = TMEM lane
     const int kv = kv0 + r;
     // A key past N (last tile of a ragged head) reads as a zero row, so its
-    // score is 0 and 2^(−LSE·log2 e) could overflow; its Pᵀ and dSᵀ are set
-    // to 0 so that dQ never sees it.  Queries past N need nothing: their
-    // −LSE is −∞ and their dO row is zero.
-    const bool dead_key = kv >= N;
+    // score is 0 and 2^(−LSE·log2 e) could overflow; its Pᵀ and dSᵀ are
+    // masked to 0 so that dQ never sees it.  Causal tiles mask it already
+    // (it lies above the diagonal of every real query).  Queries past N need
+    // nothing: their −LSE is −∞ and their dO row is zero.
+    const bool dead_key = RAGGED && kv >= N;
+    [[maybe_unused]] const bool ragged_cta = RAGGED && !CAUSAL && kv0 + kBN > N;   // uniform over the CTA
+    [[maybe_unused]] const int dead_lim = dead_key ? (1 << 30) : -(1 << 30);        // masks all columns or none
     const uint32_t lane_off = (uint32_t)(g * 32) << 16;
     const float sl2 = a.scale_log2;
     const uint32_t ds_tile = sbase + C::kDS;
@@ -221,12 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
           tmem_ld_x32(tmem + lane_off + C::kColS + (uint32_t)c0, s);
           if (masked)
             p_chunk<true, kPolyEvery>(s, sl2x2, nlse + (c0 >> 1), r - c0, p + ch * 16);
+          else if (ragged_cta)
+            p_chunk<true, 0>(s, sl2x2, nlse + (c0 >> 1), dead_lim, p + ch * 16);
           else
             p_chunk<false, kPolyEvery>(s, sl2x2, nlse + (c0 >> 1), r - c0, p + ch * 16);
-        }
-        if (dead_key) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) p[e] = 0ull;
         }
       }
       // Both warps of the lane quarter have read their Sᵀ columns; Pᵀ may now
@@ -336,8 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       prefetch_tmap(&a.tm_do);
       mbar_arrive_expect_tx(bar(kKVFull), 2u * C::kTile);
       for (int bx = 0; bx < D / 64; ++bx) {
-        tma_load_3d(sbase + C::kK + bx * kBox, &a.tm_k, bar(kKVFull), 64 * bx, kv0, bh);
-        tma_load_3d(sbase + C::kV + bx * kBox, &a.tm_v, bar(kKVFull), 64 * bx, kv0, bh);
+        load_rows(sbase + C::kK + bx * kBox, &a.tm_k, bar(kKVFull), 64 * bx, kv0);
+        load_rows(sbase + C::kV + bx * kBox, &a.tm_v, bar(kKVFull), 64 * bx, kv0);
       }
       int issued[2] = {0, 0};
       for (int i = 0; i < n; ++i) {
@@ -346,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         const int q0 = (i0 + i) * kBM;
         mbar_arrive_expect_tx(bar(kQFull + s), 2u * C::kTile + 2u * kBM * 4);
         for (int bx = 0; bx < D / 64; ++bx) {
-          tma_load_3d(sbase + C::kQ + s * C::kTile + bx * kBox, &a.tm_q, bar(kQFull + s), 64 * bx, q0, bh);
-          tma_load_3d(sbase + C::kDO + s * C::kTile + bx * kBox, &a.tm_do, bar(kQFull + s), 64 * bx, q0, bh);
+          load_rows(sbase + C::kQ + s * C::kTile + bx * kBox, &a.tm_q, bar(kQFull + s), 64 * bx, q0);
+          load_rows(sbase + C::kDO + s * C::kTile + bx * kBox, &a.tm_do, bar(kQFull + s), 64 * bx, q0);
         }
         bulk_load(sbase + C::kLSE + s * kBM * 4, a.lse2 + wrow0 + q0, kBM * 4, bar(kQFull + s));
         bulk_load(sbase + C::kDV + s * kBM * 4, a.dvec + wrow0 + q0, kBM * 4, bar(kQFull + s));
@@ -447,9 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool RAGGED>
 cudaError_t launch_impl(const BwdArgs& a, cudaStream_t s) {
-  auto kern = fa_bwd_bf16_kernel<D, CAUSAL>;
+  auto kern = fa_bwd_bf16_kernel<D, CAUSAL, RAGGED>;
   const size_t smem = BwdCfg<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -461,25 +474,26 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t s) {
 
 // ------------------------------------------------------------------ pre-pass and dQ finish
 
-// One group of D/8 threads per workspace row (n_pad rows per head); each thread
-// reads 8 bf16 of O and of dO (16 bytes each), so a warp covers 32·8
+// Grid (n_pad·D/8 / 256, heads): one group of D/8 threads per workspace row
+// (n_pad rows per head, a multiple of 128, so every thread has a row); each
+// thread reads 8 bf16 of O and of dO (16 bytes each), so a warp covers 32·8
 // contiguous elements.  Rows past N in a head are padding: D = 0, −LSE = −∞.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                        const __nv_bfloat16* __restrict__ dO,
                                                        const float* __restrict__ lse, float* __restrict__ dvec,
-                                                       float* __restrict__ lse2, float* __restrict__ dqacc,
-                                                       long long rows_pad, int N, int n_pad) {
+                                                       float* __restrict__ lse2, float* __restrict__ dqacc, int N,
+                                                       int n_pad) {
   constexpr int G = D / 8;   // threads per row
-  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long row = tid / G;           // workspace row
-  const int part = (int)(tid % G);
-  const long long head = row / n_pad;
-  const int pos = (int)(row - head * n_pad);
-  const long long src = head * N + pos;    // row of O, dO and LSE
-  const bool live = row < rows_pad && pos < N;
+  const int tid = (int)(blockIdx.x * blockDim.x + threadIdx.x);
+  const int pos = tid / G;                  // row within the head
+  const int part = tid % G;
+  const long long head = blockIdx.y;
+  const long long row = head * n_pad + pos;   // workspace row
+  const long long src = head * N + pos;       // row of O, dO and LSE
+  const bool live = pos < N;
   float acc = 0.f;
-  if (row < rows_pad) {
+  {
     float4* z = reinterpret_cast<float4*>(dqacc + row * D + part * 8);
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -499,25 +513,26 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   }
 #pragma unroll
   for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
-  if (row < rows_pad && part == 0) {
+  if (part == 0) {
     // Stored negated: the tiled kernel adds them with packed f32x2 operations.
     dvec[row] = live ? -acc : 0.f;
     lse2[row] = live ? -lse[src] * 1.4426950408889634074f : -INFINITY;
   }
 }
 
-// One thread per 8 consecutive dQ elements of a live row; the accumulator has
-// n_pad rows per head, dQ has N.
+// Grid (⌈N·D/8 / 256⌉, heads): one thread per 8 consecutive dQ elements of a
+// row below N; the accumulator has n_pad rows per head, dQ has N.
 template <int D>
 __global__ void __launch_bounds__(256) dq_finish_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
-                                                        long long n8, int N, int n_pad, float scale) {
+                                                        int N, int n_pad, float scale) {
   constexpr int G = D / 8;
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n8) return;
-  const long long row = i / G;
-  const int part = (int)(i - row * G);
-  const long long head = row / N;
-  const long long arow = row + head * (long long)(n_pad - N);
+  const int tid = (int)(blockIdx.x * blockDim.x + threadIdx.x);
+  const int pos = tid / G;
+  if (pos >= N) return;
+  const int part = tid % G;
+  const long long head = blockIdx.y;
+  const long long arow = head * n_pad + pos;
+  const long long i = (head * N + pos) * G + part;   // 16-byte chunk of dQ
   const float4* a = reinterpret_cast<const float4*>(acc + arow * D + part * 8);
   const float4 a0 = a[0];
   const float4 a1 = a[1];
@@ -536,21 +551,27 @@ int bwd_bf16_block_m(int) { return kBM; }
 size_t bwd_bf16_smem_bytes(int d) { return d == 64 ? BwdCfg<64>::kBytes : BwdCfg<128>::kBytes; }
 
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t s) {
-  if (a.d == 128) return a.causal ? launch_impl<128, true>(a, s) : launch_impl<128, false>(a, s);
-  if (a.d == 64) return a.causal ? launch_impl<64, true>(a, s) : launch_impl<64, false>(a, s);
+  const bool ragged = a.N % kBN != 0;
+  if (a.d == 128) {
+    if (ragged) return a.causal ? launch_impl<128, true, true>(a, s) : launch_impl<128, false, true>(a, s);
+    return a.causal ? launch_impl<128, true, false>(a, s) : launch_impl<128, false, false>(a, s);
+  }
+  if (a.d == 64) {
+    if (ragged) return a.causal ? launch_impl<64, true, true>(a, s) : launch_impl<64, false, true>(a, s);
+    return a.causal ? launch_impl<64, true, false>(a, s) : launch_impl<64, false, false>(a, s);
+  }
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_prep_bf16(const __nv_bfloat16* o, const __nv_bfloat16* dO, const float* lse, float* dvec,
                                  float* lse2, float* dqacc, long long heads, int N, int n_pad, int d,
                                  cudaStream_t s) {
-  const long long rows_pad = heads * n_pad;
-  const long long threads = rows_pad * (d / 8);
-  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  if (heads <= 0 || heads > 65535 || n_pad % 128 != 0) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)((long long)n_pad * (d / 8) / 256), (unsigned)heads);
   if (d == 128)
-    bwd_prep_kernel<128><<<blocks, 256, 0, s>>>(o, dO, lse, dvec, lse2, dqacc, rows_pad, N, n_pad);
+    bwd_prep_kernel<128><<<grid, 256, 0, s>>>(o, dO, lse, dvec, lse2, dqacc, N, n_pad);
   else if (d == 64)
-    bwd_prep_kernel<64><<<blocks, 256, 0, s>>>(o, dO, lse, dvec, lse2, dqacc, rows_pad, N, n_pad);
+    bwd_prep_kernel<64><<<grid, 256, 0, s>>>(o, dO, lse, dvec, lse2, dqacc, N, n_pad);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
@@ -558,12 +579,12 @@ cudaError_t launch_bwd_prep_bf16(const __nv_bfloat16* o, const __nv_bfloat16* dO
 
 cudaError_t launch_dq_finish_bf16(const float* dqacc, __nv_bfloat16* dq, long long heads, int N, int n_pad, int d,
                                   float scale, cudaStream_t s) {
-  const long long n8 = heads * N * (d / 8);
-  const unsigned blocks = (unsigned)((n8 + 255) / 256);
+  if (heads <= 0 || heads > 65535) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)(((long long)N * (d / 8) + 255) / 256), (unsigned)heads);
   if (d == 128)
-    dq_finish_kernel<128><<<blocks, 256, 0, s>>>(dqacc, dq, n8, N, n_pad, scale);
+    dq_finish_kernel<128><<<grid, 256, 0, s>>>(dqacc, dq, N, n_pad, scale);
   else if (d == 64)
-    dq_finish_kernel<64><<<blocks, 256, 0, s>>>(dqacc, dq, n8, N, n_pad, scale);
+    dq_finish_kernel<64><<<grid, 256, 0, s>>>(dqacc, dq, N, n_pad, scale);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

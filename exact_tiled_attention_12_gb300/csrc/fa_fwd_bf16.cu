@@ -107,7 +107,10 @@ __device__ __forceinline__ float exp_tile_to_p(const uint32_t (&s)[128], float s
   return (la + lb) + (lc + ld);
 }
 
-template <int D, bool CAUSAL>
+// RAGGED (N not a multiple of 128): 3-D per-head tensor maps whose rows past
+// N read as zero, masking of the missing keys and row-predicated stores.
+// Otherwise 2-D maps over the [B·H·N, d] row view and none of that code.
+template <int D, bool CAUSAL, bool RAGGED>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_constant__ FwdArgs a) {
   using L = FwdLayout<D>;
   // Dynamic shared memory starts on a 1024-byte boundary (no static shared
@@ -159,7 +162,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
   // Non-causal rows must not see the zero-filled keys past N; causal rows
   // never do, since those keys lie above the diagonal of every real query.
   const int kv_tail = N - (n_kv_all - 1) * kBN;
-  const bool ragged_last = !CAUSAL && kv_tail < kBN && kv_begin + n_kv == n_kv_all;
+  const bool ragged_last = RAGGED && !CAUSAL && kv_tail < kBN && kv_begin + n_kv == n_kv_all;
+  // Loads rows [pos, pos + 128) of this head.
+  auto load_rows = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar_addr, int x, int pos) {
+    if constexpr (RAGGED)
+      tma_load_3d(dst, map, bar_addr, x, pos, bh);
+    else
+      tma_load_2d(dst, map, bar_addr, x, row0 + pos);
+  };
 
   // Number of K/V tiles each query tile visits (0 if the tile is past N).
   int n_t[2];
@@ -219,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
         for (int c = 0; c < 128; ++c)
           if (c > r) s[c] = f2u(-INFINITY);
       }
-      if (!CAUSAL && ragged_last && j == nt - 1) {
+      if (ragged_last && j == nt - 1) {
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c >= kv_tail) s[c] = f2u(-INFINITY);
@@ -275,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
         if (part_slot < 0) {
           // tcgen05.ld is warp-collective: every lane loads, and only rows
           // below N (the last tile of a ragged head) are stored.
-          const bool live = q < N;
+          const bool live = !RAGGED || q < N;
           __nv_bfloat16* orow = a.o + ((size_t)row0 + (size_t)q) * D;
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
@@ -323,22 +333,21 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
         for (int t = 0; t < 2; ++t)
           if (n_t[t] > 0)
             for (int b = 0; b < D / 64; ++b)
-              tma_load_3d(sbase + L::kQ + t * L::kTile + b * kBoxBytes, &a.tm_q, bar(kQFull), 64 * b,
-                          q0 + t * kBM, bh);
+              load_rows(sbase + L::kQ + t * L::kTile + b * kBoxBytes, &a.tm_q, bar(kQFull), 64 * b, q0 + t * kBM);
       }
       for (int j = 0; j < J; ++j) {
         const int s = j & 1;
         if (j >= 2 && !mbar_wait(bar(kKEmpty + s), (uint32_t)(((j >> 1) - 1) & 1), wc, site(3))) break;
         mbar_arrive_expect_tx(bar(kKFull + s), tile);
         for (int b = 0; b < D / 64; ++b)
-          tma_load_3d(sbase + L::kK + s * L::kTile + b * kBoxBytes, &a.tm_k, bar(kKFull + s), 64 * b,
-                      (kv_begin + j) * kBN, bh);
+          load_rows(sbase + L::kK + s * L::kTile + b * kBoxBytes, &a.tm_k, bar(kKFull + s), 64 * b,
+                    (kv_begin + j) * kBN);
         ++issued_k[s];
         if (j >= 2 && !mbar_wait(bar(kVEmpty + s), (uint32_t)(((j >> 1) - 1) & 1), wc, site(4))) break;
         mbar_arrive_expect_tx(bar(kVFull + s), tile);
         for (int b = 0; b < D / 64; ++b)
-          tma_load_3d(sbase + L::kV + s * L::kTile + b * kBoxBytes, &a.tm_v, bar(kVFull + s), 64 * b,
-                      (kv_begin + j) * kBN, bh);
+          load_rows(sbase + L::kV + s * L::kTile + b * kBoxBytes, &a.tm_v, bar(kVFull + s), 64 * b,
+                    (kv_begin + j) * kBN);
         ++issued_v[s];
       }
       // Never leave the CTA with copies in flight: wait for the last load of
@@ -419,9 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
 template <int D>
 cudaError_t launch_combine(const FwdArgs& a, int tail, cudaStream_t s);
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool RAGGED>
 cudaError_t launch_impl(const FwdArgs& a, cudaStream_t s) {
-  auto kern = fa_fwd_bf16_kernel<D, CAUSAL>;
+  auto kern = fa_fwd_bf16_kernel<D, CAUSAL, RAGGED>;
   const size_t smem = FwdLayout<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -507,8 +516,15 @@ size_t fwd_bf16_smem_bytes(int d) {
 }
 
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s) {
-  if (a.d == 128) return a.causal ? launch_impl<128, true>(a, s) : launch_impl<128, false>(a, s);
-  if (a.d == 64) return a.causal ? launch_impl<64, true>(a, s) : launch_impl<64, false>(a, s);
+  const bool ragged = a.N % kBN != 0;
+  if (a.d == 128) {
+    if (ragged) return a.causal ? launch_impl<128, true, true>(a, s) : launch_impl<128, false, true>(a, s);
+    return a.causal ? launch_impl<128, true, false>(a, s) : launch_impl<128, false, false>(a, s);
+  }
+  if (a.d == 64) {
+    if (ragged) return a.causal ? launch_impl<64, true, true>(a, s) : launch_impl<64, false, true>(a, s);
+    return a.causal ? launch_impl<64, true, false>(a, s) : launch_impl<64, false, false>(a, s);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -12,9 +12,9 @@ namespace fa {
 
 // ---------------------------------------------------------------- bf16 tensor-core path
 
-// Forward: 3-D tensor maps over the [B·H, N, d] bf16 view of Q, K, V with
-// boxes of 64 columns (128 bytes) × 128 rows of one head and 128-byte swizzle;
-// rows past N read as zero, so N need not be a multiple of 128.
+// Forward: tensor maps over Q, K, V with boxes of 64 columns (128 bytes) ×
+// 128 rows and 128-byte swizzle: 2-D over the [B·H·N, d] row view when N is a
+// multiple of 128, else 3-D over [B·H, N, d] with rows past N read as zero.
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v;
   __nv_bfloat16* o;

@@ -16,6 +16,7 @@ from .attention import (  # noqa: F401
     causal_mask,
     matmul_backward,
     merge_outputs,
+    merge_partials,
     merge_stats,
     naive_softmax,
     online_softmax_steps,

@@ -24,7 +24,12 @@ the repository's design notes):
   ``dQ = scale * dS K`` and ``dK = scale * dSᵀ Q`` (the coreui.cn page divides
   both by sqrt(d_k); the tutorial drops the factor "for brevity");
 * LSE is the natural-log log-sum-exp of the scaled scores of each row;
-* causal means key j is visible to query i iff j <= i (square, top-left).
+* causal means key j is visible to query i iff j <= i (square, top-left);
+  with n_q queries over n_k >= n_q keys the queries are the last n_q positions
+  of the sequence (tokens after a cached prefix, "2.Online Softmax" §七 item 3),
+  so query i sees keys j <= i + (n_k - n_q);
+* normalised partial results (O_k, LSE_k) over disjoint key sets merge with
+  the §3.1/§4.1 merge taking m = LSE_k, ℓ = 1, Õ = O_k for each part.
 
 Every function below has a pin in ``tests/test_oracle_pins.py``; none is
 "parity unpinned".
@@ -123,8 +128,17 @@ def merge_outputs(m_a, l_a, o_a, m_b, l_b, o_b):
 
 
 def causal_mask(n_q, n_k):
-    """Boolean [n_q, n_k] matrix, True where key j is visible to query i (j <= i)."""
-    return np.arange(n_k)[None, :] <= np.arange(n_q)[:, None]
+    """Boolean [n_q, n_k] matrix, True where key j is visible to query i.
+
+    Square: j <= i.  With fewer queries than keys the queries are the last n_q
+    positions of the sequence ("2.Online Softmax" §七 item 3: the softmax state
+    of a prefix is kept and later tokens extend it), so query i is at position
+    i + n_k - n_q and sees j <= i + n_k - n_q.  More queries than keys would
+    leave the first rows with no key at all and is rejected.
+    """
+    if n_q > n_k:
+        raise ValueError("a causal mask with more queries than keys leaves rows with no key")
+    return np.arange(n_k)[None, :] <= np.arange(n_q)[:, None] + (n_k - n_q)
 
 
 def _scores(q, k, scale, causal):
@@ -159,13 +173,14 @@ def attention_forward_rows(q, k, v, rows, scale, causal=False):
     Row i of O depends only on q_i and all of K, V, so a sample of rows can be
     checked at sizes where the full N×N matrix is too large.
     """
+    q_all = q
     q = np.asarray(q, dtype=np.float64)[np.asarray(rows)]
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     s = scale * (q @ k.T)
     if causal:
-        visible = np.arange(k.shape[0])[None, :] <= np.asarray(rows)[:, None]
-        s = np.where(visible, s, -np.inf)
+        n_q = np.shape(q_all)[0]
+        s = np.where(causal_mask(n_q, k.shape[0])[np.asarray(rows)], s, -np.inf)
     p, m, ell = softmax_3pass(s)
     return p @ v, m + np.log(ell)
 
@@ -184,6 +199,7 @@ def tiled_forward_head(q, k, v, scale, block=64, causal=False):
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     n, d = q.shape
+    visible_all = causal_mask(n, k.shape[0]) if causal else None
     m = np.full(n, -np.inf)
     ell = np.zeros(n)
     o = np.zeros((n, v.shape[1]))
@@ -192,8 +208,7 @@ def tiled_forward_head(q, k, v, scale, block=64, causal=False):
         vj = v[j0:j0 + block]
         s = scale * (q @ kj.T)
         if causal:
-            visible = np.arange(j0, j0 + kj.shape[0])[None, :] <= np.arange(n)[:, None]
-            s = np.where(visible, s, -np.inf)
+            s = np.where(visible_all[:, j0:j0 + kj.shape[0]], s, -np.inf)
         m_j = s.max(axis=1)
         # A row whose whole block is masked has m_j = -inf and adds nothing.
         live = np.isfinite(m_j)
@@ -278,12 +293,38 @@ def attention_backward_rows(q, k, v, do, rows, scale, causal=False):
     qr, dor = q[rows], do[rows]
     s = scale * (qr @ k.T)
     if causal:
-        s = np.where(np.arange(k.shape[0])[None, :] <= rows[:, None], s, -np.inf)
+        s = np.where(causal_mask(q.shape[0], k.shape[0])[rows], s, -np.inf)
     p, _, _ = softmax_3pass(s)
     dp, dv = matmul_backward(p, v, dor)
     ds = softmax_backward(p, dp)
     dq_u, dkt_u = matmul_backward(qr, k.T, ds)
     return scale * dq_u, scale * dkt_u.T, dv
+
+
+def merge_partials(o_parts, lse_parts):
+    """Merge normalised partial results over disjoint key sets of the same rows.
+
+    "2.Online Softmax" §3.1 and §4.1 (boxed merges), applied part by part: a
+    part with output O_k and statistic LSE_k is the state m = LSE_k, ℓ = 1,
+    Õ = O_k (since Σ e^{s} over its keys is e^{LSE_k}).  A row a part never
+    saw has LSE_k = -inf and contributes nothing.  Returns (O, LSE) with
+    O = Õ/ℓ and LSE = m + ln ℓ, per row; rows no part saw get O = 0 and
+    LSE = -inf.  Arrays: o_parts [P, rows, d], lse_parts [P, rows].
+    """
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    n_rows = lse_parts.shape[1]
+    o = np.zeros(o_parts.shape[1:])
+    lse = np.full(n_rows, -np.inf)
+    for r in range(n_rows):
+        m, ell, acc = -math.inf, 0.0, np.zeros(o_parts.shape[2])
+        for k in range(o_parts.shape[0]):
+            l_k = 0.0 if lse_parts[k, r] == -math.inf else 1.0
+            m, ell, acc = merge_outputs(m, ell, acc, float(lse_parts[k, r]), l_k, o_parts[k, r])
+        if ell > 0.0:
+            o[r] = acc / ell
+            lse[r] = m + math.log(ell)
+    return o, lse
 
 
 # --------------------------------------------------------------------------

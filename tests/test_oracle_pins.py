@@ -23,6 +23,7 @@ from oracle import (
     causal_mask,
     matmul_backward,
     merge_outputs,
+    merge_partials,
     merge_stats,
     naive_softmax,
     online_softmax_steps,
@@ -223,11 +224,13 @@ def test_causal_mask_direction():
 
 
 def _brute_force_head(q, k, v, scale, causal):
-    """Scalar loops with math.exp; independent of numpy's vectorised path."""
+    """Scalar loops with math.exp; independent of numpy's vectorised path.
+    With fewer queries than keys, query i stands at position i + len(k) - len(q)."""
     n, d = len(q), len(q[0])
+    pos0 = len(k) - n
     o, lse = [], []
     for i in range(n):
-        keys = [j for j in range(len(k)) if (not causal or j <= i)]
+        keys = [j for j in range(len(k)) if (not causal or j <= i + pos0)]
         s = [scale * sum(q[i][t] * k[j][t] for t in range(d)) for j in keys]
         mx = max(s)
         w = [math.exp(x - mx) for x in s]
@@ -400,3 +403,158 @@ def test_row_block_backward_sums_to_full(causal):
         dv_sum += dv_r
     np.testing.assert_allclose(dk_sum, dk, atol=1e-13, rtol=0)
     np.testing.assert_allclose(dv_sum, dv, atol=1e-13, rtol=0)
+
+
+# ---------------------------------------------------------------- fewer queries than keys, merges
+
+
+def test_causal_mask_with_fewer_queries_than_keys():
+    """Queries are the last positions: 3 queries over 5 keys see 3, 4 and 5 keys;
+    the square mask is the lower triangle; more queries than keys is rejected."""
+    assert causal_mask(3, 5).astype(int).tolist() == [[1, 1, 1, 0, 0], [1, 1, 1, 1, 0], [1, 1, 1, 1, 1]]
+    assert np.array_equal(causal_mask(6, 6), np.tril(np.ones((6, 6), dtype=bool)))
+    with pytest.raises(ValueError):
+        causal_mask(4, 3)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fewer_queries_matches_scalar_brute_force(causal):
+    rng = _rng(40)
+    q, k, v = rng.normal(size=(4, 5)), rng.normal(size=(9, 5)), rng.normal(size=(9, 6))
+    o, lse = attention_forward_head(q, k, v, 0.55, causal)
+    ob, lseb = _brute_force_head(q.tolist(), k.tolist(), v.tolist(), 0.55, causal)
+    np.testing.assert_allclose(o, ob, atol=1e-14, rtol=0)
+    np.testing.assert_allclose(lse, lseb, atol=1e-14, rtol=0)
+
+
+def test_suffix_queries_equal_rows_of_the_square_problem():
+    """The last n_q queries of a square causal problem, run alone over all keys,
+    give that problem's last n_q rows of O and LSE; with dO zero on the other
+    rows, its dQ rows and its whole dK, dV as well."""
+    rng = _rng(41)
+    n, n_q, d = 40, 13, 8
+    q, k, v, do = (rng.normal(size=(n, d)) for _ in range(4))
+    do[: n - n_q] = 0.0
+    o, lse = attention_forward_head(q, k, v, 0.4, causal=True)
+    dq, dk, dv = attention_backward_head(q, k, v, do, 0.4, causal=True)
+    o_s, lse_s = attention_forward_head(q[n - n_q:], k, v, 0.4, causal=True)
+    dq_s, dk_s, dv_s = attention_backward_head(q[n - n_q:], k, v, do[n - n_q:], 0.4, causal=True)
+    np.testing.assert_allclose(o_s, o[n - n_q:], atol=1e-14, rtol=0)
+    np.testing.assert_allclose(lse_s, lse[n - n_q:], atol=1e-14, rtol=0)
+    np.testing.assert_allclose(dq_s, dq[n - n_q:], atol=1e-13, rtol=0)
+    np.testing.assert_allclose(dk_s, dk, atol=1e-13, rtol=0)
+    np.testing.assert_allclose(dv_s, dv, atol=1e-13, rtol=0)
+
+
+def test_single_query_causal_sees_every_key():
+    """One query after n_k - 1 cached keys (a decode step) sees all keys."""
+    rng = _rng(42)
+    q, k, v = rng.normal(size=(1, 8)), rng.normal(size=(30, 8)), rng.normal(size=(30, 8))
+    o_c, lse_c = attention_forward_head(q, k, v, 0.3, causal=True)
+    o_n, lse_n = attention_forward_head(q, k, v, 0.3, causal=False)
+    np.testing.assert_allclose(o_c, o_n, atol=0, rtol=0)
+    np.testing.assert_allclose(lse_c, lse_n, atol=0, rtol=0)
+
+
+@pytest.mark.parametrize("block", [1, 6, 32])
+def test_tiled_algorithm_with_fewer_queries(block):
+    rng = _rng(43 + block)
+    q, k, v = rng.normal(size=(21, 8)) * 2, rng.normal(size=(70, 8)) * 2, rng.normal(size=(70, 8))
+    o, lse = attention_forward_head(q, k, v, 8 ** -0.5, causal=True)
+    ot, lset = tiled_forward_head(q, k, v, 8 ** -0.5, block, causal=True)
+    np.testing.assert_allclose(ot, o, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lset, lse, atol=1e-12, rtol=0)
+
+
+def test_row_subsets_with_fewer_queries():
+    rng = _rng(44)
+    q, k, v, do = rng.normal(size=(20, 8)), rng.normal(size=(50, 8)), rng.normal(size=(50, 8)), rng.normal(size=(20, 8))
+    rows = np.array([0, 7, 19])
+    o, lse = attention_forward_head(q, k, v, 0.3, causal=True)
+    orow, lserow = attention_forward_rows(q, k, v, rows, 0.3, causal=True)
+    np.testing.assert_allclose(orow, o[rows], atol=1e-14, rtol=0)
+    np.testing.assert_allclose(lserow, lse[rows], atol=1e-14, rtol=0)
+    dq, dk, dv = attention_backward_head(q, k, v, do, 0.3, causal=True)
+    dk_sum, dv_sum = np.zeros_like(dk), np.zeros_like(dv)
+    for block in (np.arange(0, 9), np.arange(9, 20)):
+        dq_r, dk_r, dv_r = attention_backward_rows(q, k, v, do, block, 0.3, causal=True)
+        np.testing.assert_allclose(dq_r, dq[block], atol=1e-14, rtol=0)
+        dk_sum += dk_r
+        dv_sum += dv_r
+    np.testing.assert_allclose(dk_sum, dk, atol=1e-13, rtol=0)
+    np.testing.assert_allclose(dv_sum, dv, atol=1e-13, rtol=0)
+
+
+def test_finite_difference_gradients_fewer_queries():
+    """Central differences for 3 causal queries over 6 keys (h = 1e-6)."""
+    rng = _rng(45)
+    n_q, n_k, d, scale = 3, 6, 4, 0.7
+    q, do = rng.normal(size=(n_q, d)), rng.normal(size=(n_q, d))
+    k, v = rng.normal(size=(n_k, d)), rng.normal(size=(n_k, d))
+    grads = attention_backward_head(q, k, v, do, scale, causal=True)
+    h = 1e-6
+    for which, g in zip(range(3), grads):
+        fd = np.zeros(g.shape)
+        for i in range(g.shape[0]):
+            for t in range(d):
+                args = [q.copy(), k.copy(), v.copy()]
+                args[which][i, t] += h
+                up = _loss(*args, do, scale, True)
+                args[which][i, t] -= 2 * h
+                dn = _loss(*args, do, scale, True)
+                fd[i, t] = (up - dn) / (2 * h)
+        err = np.linalg.norm(fd - g) / max(np.linalg.norm(g), 1e-30)
+        assert err <= 1e-6, (which, err)
+
+
+def test_merge_partials_over_key_ranges_equals_full():
+    """2.Online Softmax §七: attention over disjoint key sets, merged, is attention
+    over all the keys (contiguous ranges and an interleaved partition)."""
+    rng = _rng(46)
+    q, k, v = rng.normal(size=(9, 6)) * 3, rng.normal(size=(31, 6)) * 3, rng.normal(size=(31, 5))
+    o, lse = attention_forward_head(q, k, v, 0.5)
+    for parts in ([np.arange(0, 10), np.arange(10, 11), np.arange(11, 31)],
+                  [np.arange(0, 31, 3), np.arange(1, 31, 3), np.arange(2, 31, 3)]):
+        outs = [attention_forward_head(q, k[p], v[p], 0.5) for p in parts]
+        om, lsem = merge_partials([x[0] for x in outs], [x[1] for x in outs])
+        np.testing.assert_allclose(om, o, atol=1e-13, rtol=0)
+        np.testing.assert_allclose(lsem, lse, atol=1e-13, rtol=0)
+
+
+def test_merge_partials_streaming_prefix_then_new_keys():
+    """Prefix caching: new causal queries over cached keys (every cached key
+    visible) merged with the same queries over the new keys under the causal
+    mask equal the causal problem over the whole sequence."""
+    rng = _rng(47)
+    n_cache, n_new, d = 25, 7, 8
+    q = rng.normal(size=(n_new, d))
+    k, v = rng.normal(size=(n_cache + n_new, d)), rng.normal(size=(n_cache + n_new, d))
+    o, lse = attention_forward_head(q, k, v, 0.35, causal=True)
+    o_a, lse_a = attention_forward_head(q, k[:n_cache], v[:n_cache], 0.35, causal=False)
+    o_b, lse_b = attention_forward_head(q, k[n_cache:], v[n_cache:], 0.35, causal=True)
+    om, lsem = merge_partials([o_a, o_b], [lse_a, lse_b])
+    np.testing.assert_allclose(om, o, atol=1e-13, rtol=0)
+    np.testing.assert_allclose(lsem, lse, atol=1e-13, rtol=0)
+
+
+def test_merge_partials_ignores_parts_that_saw_nothing():
+    rng = _rng(48)
+    o1, lse1 = rng.normal(size=(3, 4)), rng.normal(size=3)
+    junk = rng.normal(size=(3, 4))
+    lse_none = np.full(3, -np.inf)
+    om, lsem = merge_partials([junk, o1, junk], [lse_none, lse1, lse_none])
+    np.testing.assert_allclose(om, o1, atol=1e-15, rtol=0)
+    np.testing.assert_allclose(lsem, lse1, atol=1e-15, rtol=0)
+    om, lsem = merge_partials([junk, junk], [lse_none, lse_none])
+    assert np.all(om == 0.0) and np.all(lsem == -np.inf)
+
+
+def test_merge_partials_two_parts_closed_form():
+    """Two parts with LSE a and b: weights e^a/(e^a+e^b) and e^b/(e^a+e^b),
+    LSE = ln(e^a + e^b) — written out directly."""
+    o_a, o_b = np.array([[1.0, -2.0]]), np.array([[3.0, 0.5]])
+    a, b = 0.3, -1.1
+    om, lsem = merge_partials([o_a, o_b], [np.array([a]), np.array([b])])
+    wa = math.exp(a) / (math.exp(a) + math.exp(b))
+    np.testing.assert_allclose(om, wa * o_a + (1 - wa) * o_b, atol=1e-15, rtol=0)
+    assert abs(lsem[0] - math.log(math.exp(a) + math.exp(b))) <= 1e-15

@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     fwd_workspace_size,
     lib,
     library_path,
+    merge,
     status_string,
     sync_status,
 )

@@ -36,7 +36,13 @@ SIGNATURES = {
     "fa_bwd_dq_finish": (_I, [_P, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
     "fa_sync_status": (_I, [_P]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "fa_fwd_kv_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
+    "fa_fwd_kv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _Z, _P]),
+    "fa_bwd_kv_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
+    "fa_bwd_kv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _Z, _P]),
+    "fa_merge": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P]),
 }
+MERGE_MAX_PARTS = 16
 
 
 class FaError(RuntimeError):
@@ -96,72 +102,119 @@ def _stream(t: torch.Tensor) -> ctypes.c_void_p:
     return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
 
 
-def _check_qkv(*ts):
-    ref = ts[0]
+def _check_tensors(qside, kside):
+    """q-side tensors (q, o, dO) are [B, H, Nq, d]; k-side (k, v) [B, H, Nk, d]."""
+    ref = qside[0]
     if ref.dim() != 4:
         raise ValueError("tensors must be [B, H, N, d]")
-    for t in ts:
+    for t in qside + kside:
         if not t.is_cuda:
             raise ValueError("tensors must be CUDA tensors")
-        if t.shape != ref.shape or t.dtype != ref.dtype or t.device != ref.device:
-            raise ValueError("q, k, v (and o, dO) must share shape, dtype and device")
+        if t.dim() != 4 or t.dtype != ref.dtype or t.device != ref.device:
+            raise ValueError("q, k, v (and o, dO) must be [B, H, N, d] with one dtype and device")
         if not t.is_contiguous():
             raise ValueError("tensors must be contiguous [B, H, N, d]")
+    for t in qside:
+        if t.shape != ref.shape:
+            raise ValueError("q, o and dO must share one shape [B, H, Nq, d]")
+    kref = kside[0]
+    for t in kside:
+        if t.shape != kref.shape:
+            raise ValueError("k and v must share one shape [B, H, Nk, d]")
+    if kref.shape[:2] != ref.shape[:2] or kref.shape[3] != ref.shape[3]:
+        raise ValueError("q and k must agree on B, H and d")
 
 
-def fwd_workspace_size(B, H, N, d, causal=False, dtype=torch.bfloat16) -> int:
-    code = FA_DTYPE_BF16 if dtype == torch.bfloat16 else FA_DTYPE_FP32
-    return int(lib().fa_fwd_workspace_size(B, H, N, d, int(bool(causal)), code))
+def _code(dtype) -> int:
+    return FA_DTYPE_BF16 if dtype == torch.bfloat16 else FA_DTYPE_FP32
+
+
+def fwd_workspace_size(B, H, N, d, causal=False, dtype=torch.bfloat16, Nk=None) -> int:
+    """Bytes of the forward's optional load-balancing workspace (N queries over Nk keys, Nk = N by default)."""
+    Nk = N if Nk is None else Nk
+    return int(lib().fa_fwd_kv_workspace_size(B, H, N, Nk, d, int(bool(causal)), _code(dtype)))
 
 
 def fwd(q, k, v, scale=None, causal=False, workspace=None):
-    """Attention forward.  Returns (o [B,H,N,d] in q's dtype, lse [B,H,N] float32).
+    """Attention forward.  q [B,H,Nq,d], k and v [B,H,Nk,d]; returns
+    (o [B,H,Nq,d] in q's dtype, lse [B,H,Nq] float32).  Under ``causal`` the
+    queries are the last Nq positions: query i sees keys j <= i + Nk - Nq.
 
     ``workspace``: None allocates the optional load-balancing workspace with
     torch when the library asks for one; a uint8 CUDA tensor is used as given;
     False runs without one.
     """
-    _check_qkv(q, k, v)
-    B, H, N, d = q.shape
+    _check_tensors([q], [k, v])
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
     scale = float(d ** -0.5 if scale is None else scale)
     o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     with torch.cuda.device(q.device):
         if workspace is None:
-            n = fwd_workspace_size(B, H, N, d, causal, q.dtype)
+            n = fwd_workspace_size(B, H, Nq, d, causal, q.dtype, Nk)
             workspace = torch.empty(n, dtype=torch.uint8, device=q.device) if n else False
         ws, n = (None, 0) if workspace is False else (workspace, workspace.numel())
-        _check("fa_fwd", lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
-                                      int(bool(causal)), _dtype_code(q), _ptr(ws), n, _stream(q)))
+        _check("fa_fwd_kv", lib().fa_fwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, scale,
+                                            int(bool(causal)), _dtype_code(q), _ptr(ws), n, _stream(q)))
     return o, lse
 
 
-def bwd_workspace_size(B, H, N, d, dtype=torch.bfloat16) -> int:
-    code = FA_DTYPE_BF16 if dtype == torch.bfloat16 else FA_DTYPE_FP32
-    return int(lib().fa_bwd_workspace_size(B, H, N, d, code))
+def bwd_workspace_size(B, H, N, d, dtype=torch.bfloat16, Nk=None) -> int:
+    """Bytes of the backward's workspace (N queries over Nk keys, Nk = N by default)."""
+    Nk = N if Nk is None else Nk
+    return int(lib().fa_bwd_kv_workspace_size(B, H, N, Nk, d, _code(dtype)))
 
 
-def _workspace(q):
-    B, H, N, d = q.shape
-    n = bwd_workspace_size(B, H, N, d, q.dtype)
+def _workspace(q, k):
+    B, H, Nq, d = q.shape
+    n = bwd_workspace_size(B, H, Nq, d, q.dtype, k.shape[2])
     # torch's caching allocator returns blocks aligned to at least 512 bytes
     return torch.empty(max(n, 1), dtype=torch.uint8, device=q.device), n
 
 
 def bwd(q, k, v, o, do, lse, scale=None, causal=False, workspace=None):
-    """Attention backward.  Returns (dq, dk, dv) in q's dtype."""
-    _check_qkv(q, k, v, o, do)
-    B, H, N, d = q.shape
-    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    """Attention backward.  Returns (dq like q, dk and dv like k)."""
+    _check_tensors([q, o, do], [k, v])
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, Nq] tensor")
     scale = float(d ** -0.5 if scale is None else scale)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    ws, n = _workspace(q) if workspace is None else (workspace, workspace.numel())
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws, n = _workspace(q, k) if workspace is None else (workspace, workspace.numel())
     with torch.cuda.device(q.device):
-        _check("fa_bwd", lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
-                                      _ptr(dv), B, H, N, d, scale, int(bool(causal)), _dtype_code(q), _ptr(ws), n,
-                                      _stream(q)))
+        _check("fa_bwd_kv", lib().fa_bwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                                            _ptr(dk), _ptr(dv), B, H, Nq, Nk, d, scale, int(bool(causal)),
+                                            _dtype_code(q), _ptr(ws), n, _stream(q)))
     return dq, dk, dv
+
+
+def merge(o_parts, lse_parts, out=None):
+    """Merge partial results of the same queries over disjoint key sets.
+
+    o_parts: list of [B,H,N,d] tensors (one dtype); lse_parts: list of
+    [B,H,N] float32 tensors.  Returns (o, lse); ``out`` = (o, lse) writes into
+    given tensors, which may be one of the parts (in-place running state).
+    """
+    if not o_parts or len(o_parts) != len(lse_parts) or len(o_parts) > MERGE_MAX_PARTS:
+        raise ValueError(f"need 1..{MERGE_MAX_PARTS} parts with one LSE each")
+    ref = o_parts[0]
+    for t in o_parts:
+        if not t.is_cuda or t.shape != ref.shape or t.dtype != ref.dtype or not t.is_contiguous():
+            raise ValueError("O parts must be contiguous CUDA tensors of one shape and dtype")
+    B, H, N, d = ref.shape
+    for t in lse_parts:
+        if t.shape != (B, H, N) or t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("LSE parts must be contiguous float32 CUDA tensors [B, H, N]")
+    o, lse = out if out is not None else (torch.empty_like(ref), torch.empty_like(lse_parts[0]))
+    n = len(o_parts)
+    o_arr = (ctypes.c_void_p * n)(*[t.data_ptr() for t in o_parts])
+    l_arr = (ctypes.c_void_p * n)(*[t.data_ptr() for t in lse_parts])
+    with torch.cuda.device(ref.device):
+        _check("fa_merge", lib().fa_merge(ctypes.cast(o_arr, ctypes.c_void_p), ctypes.cast(l_arr, ctypes.c_void_p), n,
+                                          _ptr(o), _ptr(lse), B, H, N, d, _dtype_code(ref), _stream(ref)))
+    return o, lse
 
 
 def bwd_stages(q, k, v, o, do, lse, dq, dk, dv, workspace, scale=None, causal=False, between=None):
@@ -170,7 +223,10 @@ def bwd_stages(q, k, v, o, do, lse, dq, dk, dv, workspace, scale=None, causal=Fa
     ``between`` is an optional pair of callables run just before and just
     after the tiled stage (the bench records CUDA events there).
     """
+    _check_tensors([q, o, do, dq], [k, v, dk, dv])
     B, H, N, d = q.shape
+    if k.shape[2] != N:
+        raise ValueError("the stage entry points take square problems (Nq = Nk)")
     scale = float(d ** -0.5 if scale is None else scale)
     code = _dtype_code(q)
     s = _stream(q)

@@ -47,15 +47,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // Tensor map over a [B·H, N, d] bf16 tensor with boxes of 64 columns (128
-// bytes) × box_rows rows and 128-byte swizzle.  N a multiple of 128: a 2-D
-// map over the [B·H·N, d] row view (a tile never straddles two heads).
-// Otherwise a 3-D map whose rows past N read as zero, so the last tile of a
-// head never picks up the next head's rows.  The kernels pick the matching
-// copy form from N.
-bool encode_bf16_heads(CUtensorMap* m, const void* base, long long heads, long long N, int d, int box_rows) {
+// bytes) × box_rows rows and 128-byte swizzle.  rows_view (every sequence
+// length of the call a multiple of 128): a 2-D map over the [B·H·N, d] row
+// view (a tile never straddles two heads).  Otherwise a 3-D map whose rows
+// past N read as zero, so the last tile of a head never picks up the next
+// head's rows.  The kernels take the matching copy form from the same test.
+bool encode_bf16_heads(CUtensorMap* m, const void* base, long long heads, long long N, int d, int box_rows,
+                       bool rows_view) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
-  const bool rows_view = N % 128 == 0;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)(rows_view ? heads * N : N), (cuuint64_t)heads};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * (cuuint64_t)d * 2};
   cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
@@ -70,29 +70,44 @@ inline size_t pad256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // ------------------------------------------------------------------ validation
 
+// Nq queries over Nk keys per (batch, head).
 struct Shape {
-  long long B, H, N, d;
-  long long rows() const { return B * H * N; }
-  long long elems() const { return B * H * N * d; }
+  long long B, H, Nq, Nk, d;
+  long long heads() const { return B * H; }
+  long long rows() const { return B * H * Nq; }            // query rows
+  long long q_elems() const { return B * H * Nq * d; }
+  long long k_elems() const { return B * H * Nk * d; }
   // bf16 per-row workspace arrays are padded to whole 128-row tiles per head
-  long long n_pad() const { return (N + 127) / 128 * 128; }
-  long long rows_pad() const { return B * H * n_pad(); }
-  bool empty() const { return B == 0 || H == 0 || N == 0; }
+  long long nq_pad() const { return (Nq + 127) / 128 * 128; }
+  long long nk_pad() const { return (Nk + 127) / 128 * 128; }
+  long long rows_pad() const { return B * H * nq_pad(); }
+  bool rows_view() const { return Nq % 128 == 0 && Nk % 128 == 0; }
+  bool no_heads() const { return B == 0 || H == 0; }
+  bool empty() const { return no_heads() || Nq == 0; }    // nothing to compute for any query
 };
 
-fa_status check_shape(int B, int H, int N, int d, fa_dtype dtype, Shape* out) {
-  if (B < 0 || H < 0 || N < 0 || d <= 0) return FA_ERR_INVALID_ARG;
+fa_status check_shape(int B, int H, int Nq, int Nk, int d, fa_dtype dtype, int causal, Shape* out) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP32) return FA_ERR_INVALID_ARG;
-  Shape s{B, H, N, d};
-  if (s.elems() > (1ll << 40)) return FA_ERR_UNSUPPORTED;
-  if (!s.empty()) {
-    if (dtype == FA_DTYPE_BF16) {
-      if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-      if (s.rows_pad() >= (1ll << 31) || s.n_pad() / 128 > 65535 || s.B * s.H > 65535) return FA_ERR_UNSUPPORTED;
-    } else {
-      if (d > 128) return FA_ERR_UNSUPPORTED;
-      if (s.B * s.H > 65535 || s.rows() >= (1ll << 31)) return FA_ERR_UNSUPPORTED;
-    }
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  Shape s{B, H, Nq, Nk, d};
+  if (s.q_elems() > (1ll << 40) || s.k_elems() > (1ll << 40)) return FA_ERR_UNSUPPORTED;
+  if (!s.no_heads() && Nq > 0 && Nk == 0) return FA_ERR_INVALID_ARG;     // queries with no key at all
+  if (s.no_heads() || (Nq == 0 && Nk == 0)) {
+    *out = s;
+    return FA_OK;
+  }
+  // The causal mask aligns the queries with the last Nq keys; more queries
+  // than keys would leave rows with no visible key.
+  if (causal && Nq > Nk) return FA_ERR_UNSUPPORTED;
+  if (s.heads() > 65535) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_DTYPE_BF16) {
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (s.rows_pad() >= (1ll << 31) || s.heads() * s.nk_pad() >= (1ll << 31) || s.nk_pad() / 128 > 65535)
+      return FA_ERR_UNSUPPORTED;
+  } else {
+    if (d > 128) return FA_ERR_UNSUPPORTED;
+    if (s.rows() >= (1ll << 31) || s.heads() * Nk >= (1ll << 31)) return FA_ERR_UNSUPPORTED;
   }
   *out = s;
   return FA_OK;
@@ -122,9 +137,9 @@ size_t workspace_bytes_for(const Shape& s, fa_dtype dtype) {
   return 2 * pad256(rows * 4) + pad256(rows * (size_t)s.d * 4);
 }
 
-// Workspace parts: D (float32 per row), the forward's LSE per row (base 2 for
-// bf16, natural-log copy for fp32), and for bf16 the float32 dQ accumulator.
-// The bf16 parts hold whole 128-row tiles per head (rows_pad rows).
+// Workspace parts: D (float32 per query row), the forward's LSE per row (base
+// 2 for bf16, natural-log copy for fp32), and for bf16 the float32 dQ
+// accumulator.  The bf16 parts hold whole 128-row tiles per head.
 struct Workspace {
   float* dvec;
   float* lse2;
@@ -166,9 +181,9 @@ struct FwdPlan {
 // it does not split: causal, fp32, or no partial last wave worth splitting).
 size_t fwd_workspace_bytes(const Shape& s, int causal, fa_dtype dtype, FwdPlan* plan) {
   if (s.empty() || causal || dtype != FA_DTYPE_BF16) return 0;
-  const int units = fa::fwd_units((int)s.B, (int)s.H, (int)s.N);
+  const int units = fa::fwd_units((int)s.B, (int)s.H, (int)s.Nq);
   int n_full, splits;
-  fa::fwd_split_plan(units, sm_count_current_device(), (int)(s.n_pad() / 128), &n_full, &splits);
+  fa::fwd_split_plan(units, sm_count_current_device(), (int)(s.nk_pad() / 128), &n_full, &splits);
   if (splits <= 1 || n_full >= units) return 0;
   const size_t rows = (size_t)(units - n_full) * (size_t)splits * 256;
   const size_t opart = pad256(rows * (size_t)s.d * 4);
@@ -177,6 +192,163 @@ size_t fwd_workspace_bytes(const Shape& s, int causal, fa_dtype dtype, FwdPlan* 
 }
 
 constexpr float kLog2e = 1.4426950408889634074f;
+
+size_t elem_bytes(fa_dtype dtype) { return dtype == FA_DTYPE_BF16 ? 2 : 4; }
+
+// ------------------------------------------------------------------ implementations (Nq queries, Nk keys)
+
+fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                   int d, float scale, int causal, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                   fa_stream_t stream) {
+  Shape s;
+  fa_status st = check_shape(B, H, Nq, Nk, d, dtype, causal, &s);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (s.empty()) return FA_OK;
+  if ((st = check_ptrs({q, k, v, o, lse}, dtype)) != FA_OK) return st;
+  if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_WORKSPACE;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  unsigned int* fault = fault_word_for_current_device();
+  if (!fault) return FA_ERR_CUDA;
+  if (dtype == FA_DTYPE_FP32)
+    return from_cuda(fa::launch_fwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                        static_cast<const float*>(v), static_cast<float*>(o), lse, (int)s.heads(), Nq,
+                                        Nk, d, scale, causal, cs));
+  fa::FwdArgs a;
+  const long long heads = s.heads();
+  const bool rv = s.rows_view();
+  if (!encode_bf16_heads(&a.tm_q, q, heads, Nq, d, 128, rv) || !encode_bf16_heads(&a.tm_k, k, heads, Nk, d, 128, rv) ||
+      !encode_bf16_heads(&a.tm_v, v, heads, Nk, d, 128, rv))
+    return FA_ERR_CUDA;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.d = d;
+  a.scale_log2 = scale * kLog2e;
+  a.causal = causal;
+  a.fault = fault;
+  // Load balancing needs the workspace; without one (NULL) every unit runs whole.
+  FwdPlan plan;
+  const size_t need = fwd_workspace_bytes(s, causal, dtype, &plan);
+  a.n_full = fa::fwd_units(B, H, Nq);
+  a.splits = 1;
+  a.opart = nullptr;
+  a.lpart = nullptr;
+  if (need > 0 && workspace != nullptr) {
+    if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+    a.n_full = plan.n_full;
+    a.splits = plan.splits;
+    a.opart = static_cast<float*>(workspace);
+    a.lpart = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.opart_bytes);
+  }
+  return from_cuda(fa::launch_fwd_bf16(a, cs));
+}
+
+fa_status prep_impl(const void* o, const void* dO, const float* lse, int B, int H, int Nq, int Nk, int d,
+                    fa_dtype dtype, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  Shape s;
+  fa_status st = check_shape(B, H, Nq, Nk, d, dtype, 0, &s);
+  if (st != FA_OK) return st;
+  if (s.empty()) return FA_OK;
+  if ((st = check_ptrs({o, dO, lse}, dtype)) != FA_OK) return st;
+  Workspace w;
+  if ((st = carve_workspace(s, dtype, workspace, workspace_bytes, &w)) != FA_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == FA_DTYPE_FP32)
+    return from_cuda(fa::launch_bwd_prep_f32(static_cast<const float*>(o), static_cast<const float*>(dO), lse, w.dvec,
+                                             w.lse2, s.rows(), d, cs));
+  return from_cuda(fa::launch_bwd_prep_bf16(static_cast<const __nv_bfloat16*>(o),
+                                            static_cast<const __nv_bfloat16*>(dO), lse, w.dvec, w.lse2, w.dqacc,
+                                            s.heads(), Nq, (int)s.nq_pad(), d, cs));
+}
+
+fa_status tiles_impl(const void* q, const void* k, const void* v, const void* dO, void* dq, void* dk, void* dv, int B,
+                     int H, int Nq, int Nk, int d, float scale, int causal, fa_dtype dtype, void* workspace,
+                     size_t workspace_bytes, fa_stream_t stream) {
+  Shape s;
+  fa_status st = check_shape(B, H, Nq, Nk, d, dtype, causal, &s);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (s.empty()) return FA_OK;
+  if ((st = check_ptrs({q, k, v, dO, dk, dv}, dtype)) != FA_OK) return st;
+  if (dtype == FA_DTYPE_FP32 && (st = check_ptrs({dq}, dtype)) != FA_OK) return st;
+  Workspace w;
+  if ((st = carve_workspace(s, dtype, workspace, workspace_bytes, &w)) != FA_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == FA_DTYPE_FP32)
+    return from_cuda(fa::launch_bwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                        static_cast<const float*>(v), static_cast<const float*>(dO), w.lse2, w.dvec,
+                                        static_cast<float*>(dq), static_cast<float*>(dk), static_cast<float*>(dv),
+                                        (int)s.heads(), Nq, Nk, d, scale, causal, cs));
+  unsigned int* fault = fault_word_for_current_device();
+  if (!fault) return FA_ERR_CUDA;
+  fa::BwdArgs a;
+  const int bm = fa::bwd_bf16_block_m(d);
+  const long long heads = s.heads();
+  const bool rv = s.rows_view();
+  if (!encode_bf16_heads(&a.tm_q, q, heads, Nq, d, bm, rv) || !encode_bf16_heads(&a.tm_k, k, heads, Nk, d, 128, rv) ||
+      !encode_bf16_heads(&a.tm_v, v, heads, Nk, d, 128, rv) || !encode_bf16_heads(&a.tm_do, dO, heads, Nq, d, bm, rv))
+    return FA_ERR_CUDA;
+  a.lse2 = w.lse2;
+  a.dvec = w.dvec;
+  a.dqacc = w.dqacc;
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.B = B;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.d = d;
+  a.scale_log2 = scale * kLog2e;
+  a.scale = scale;
+  a.causal = causal;
+  a.fault = fault;
+  return from_cuda(fa::launch_bwd_bf16(a, cs));
+}
+
+fa_status finish_impl(void* dq, int B, int H, int Nq, int Nk, int d, float scale, fa_dtype dtype, void* workspace,
+                      size_t workspace_bytes, fa_stream_t stream) {
+  Shape s;
+  fa_status st = check_shape(B, H, Nq, Nk, d, dtype, 0, &s);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (s.empty() || dtype == FA_DTYPE_FP32) return FA_OK;
+  if ((st = check_ptrs({dq}, dtype)) != FA_OK) return st;
+  Workspace w;
+  if ((st = carve_workspace(s, dtype, workspace, workspace_bytes, &w)) != FA_OK) return st;
+  return from_cuda(fa::launch_dq_finish_bf16(w.dqacc, static_cast<__nv_bfloat16*>(dq), s.heads(), Nq,
+                                             (int)s.nq_pad(), d, scale, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                   void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                   fa_dtype dtype, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  Shape s;
+  fa_status st = check_shape(B, H, Nq, Nk, d, dtype, causal, &s);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (s.no_heads() || (Nq == 0 && Nk == 0)) return FA_OK;
+  if (Nq == 0) {
+    // No query sees the keys: their gradients are zero.
+    if ((st = check_ptrs({dk, dv}, dtype)) != FA_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const size_t bytes = (size_t)s.k_elems() * elem_bytes(dtype);
+    if (cudaMemsetAsync(dk, 0, bytes, cs) != cudaSuccess || cudaMemsetAsync(dv, 0, bytes, cs) != cudaSuccess)
+      return FA_ERR_CUDA;
+    return FA_OK;
+  }
+  if ((st = check_ptrs({q, k, v, o, dO, lse, dq, dk, dv}, dtype)) != FA_OK) return st;
+  Workspace w;
+  if ((st = carve_workspace(s, dtype, workspace, workspace_bytes, &w)) != FA_OK) return st;
+  if ((st = prep_impl(o, dO, lse, B, H, Nq, Nk, d, dtype, workspace, workspace_bytes, stream)) != FA_OK) return st;
+  if ((st = tiles_impl(q, k, v, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, dtype, workspace, workspace_bytes,
+                       stream)) != FA_OK)
+    return st;
+  return finish_impl(dq, B, H, Nq, Nk, d, scale, dtype, workspace, workspace_bytes, stream);
+}
 
 }  // namespace
 
@@ -195,161 +367,101 @@ const char* fa_status_string(fa_status s) {
   return "unknown fa_status";
 }
 
-int fa_version(void) { return 100; }
+int fa_version(void) { return 110; }
+
+size_t fa_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int causal, fa_dtype dtype) {
+  Shape s;
+  if (check_shape(B, H, Nq, Nk, d, dtype, causal, &s) != FA_OK) return 0;
+  return fwd_workspace_bytes(s, causal, dtype, nullptr);
+}
 
 size_t fa_fwd_workspace_size(int B, int H, int N, int d, int causal, fa_dtype dtype) {
-  Shape s;
-  if (check_shape(B, H, N, d, dtype, &s) != FA_OK || (causal != 0 && causal != 1)) return 0;
-  return fwd_workspace_bytes(s, causal, dtype, nullptr);
+  return fa_fwd_kv_workspace_size(B, H, N, N, d, causal, dtype);
+}
+
+fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                    int d, float scale, int causal, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                    fa_stream_t stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                  float scale, int causal, fa_dtype dtype, void* workspace, size_t workspace_bytes,
                  fa_stream_t stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, N, d, scale, causal, dtype, workspace, workspace_bytes, stream);
+}
+
+size_t fa_bwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, fa_dtype dtype) {
   Shape s;
-  fa_status st = check_shape(B, H, N, d, dtype, &s);
-  if (st != FA_OK) return st;
-  if ((st = check_scale(scale)) != FA_OK) return st;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (s.empty()) return FA_OK;
-  if ((st = check_ptrs({q, k, v, o, lse}, dtype)) != FA_OK) return st;
-  if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_WORKSPACE;
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  unsigned int* fault = fault_word_for_current_device();
-  if (!fault) return FA_ERR_CUDA;
-  if (dtype == FA_DTYPE_FP32)
-    return from_cuda(fa::launch_fwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
-                                        static_cast<const float*>(v), static_cast<float*>(o), lse, (int)(s.B * s.H),
-                                        N, d, scale, causal, cs));
-  fa::FwdArgs a;
-  const long long heads = s.B * s.H;
-  if (!encode_bf16_heads(&a.tm_q, q, heads, N, d, 128) || !encode_bf16_heads(&a.tm_k, k, heads, N, d, 128) ||
-      !encode_bf16_heads(&a.tm_v, v, heads, N, d, 128))
-    return FA_ERR_CUDA;
-  a.o = static_cast<__nv_bfloat16*>(o);
-  a.lse = lse;
-  a.B = B;
-  a.H = H;
-  a.N = N;
-  a.d = d;
-  a.scale_log2 = scale * kLog2e;
-  a.causal = causal;
-  a.fault = fault;
-  // Load balancing needs the workspace; without one (NULL) every unit runs whole.
-  FwdPlan plan;
-  const size_t need = fwd_workspace_bytes(s, causal, dtype, &plan);
-  a.n_full = fa::fwd_units(B, H, N);
-  a.splits = 1;
-  a.opart = nullptr;
-  a.lpart = nullptr;
-  if (need > 0 && workspace != nullptr) {
-    if (workspace_bytes < need) return FA_ERR_WORKSPACE;
-    a.n_full = plan.n_full;
-    a.splits = plan.splits;
-    a.opart = static_cast<float*>(workspace);
-    a.lpart = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.opart_bytes);
-  }
-  return from_cuda(fa::launch_fwd_bf16(a, cs));
+  if (check_shape(B, H, Nq, Nk, d, dtype, 0, &s) != FA_OK) return 0;
+  return workspace_bytes_for(s, dtype);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d, fa_dtype dtype) {
-  Shape s;
-  if (check_shape(B, H, N, d, dtype, &s) != FA_OK) return 0;
-  return workspace_bytes_for(s, dtype);
+  return fa_bwd_kv_workspace_size(B, H, N, N, d, dtype);
 }
 
 fa_status fa_bwd_prep(const void* o, const void* dO, const float* lse, int B, int H, int N, int d, fa_dtype dtype,
                       void* workspace, size_t workspace_bytes, fa_stream_t stream) {
-  Shape s;
-  fa_status st = check_shape(B, H, N, d, dtype, &s);
-  if (st != FA_OK) return st;
-  if (s.empty()) return FA_OK;
-  if ((st = check_ptrs({o, dO, lse}, dtype)) != FA_OK) return st;
-  Workspace w;
-  if ((st = carve_workspace(s, dtype, workspace, workspace_bytes, &w)) != FA_OK) return st;
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (dtype == FA_DTYPE_FP32)
-    return from_cuda(fa::launch_bwd_prep_f32(static_cast<const float*>(o), static_cast<const float*>(dO), lse, w.dvec,
-                                             w.lse2, s.rows(), d, cs));
-  return from_cuda(fa::launch_bwd_prep_bf16(static_cast<const __nv_bfloat16*>(o),
-                                            static_cast<const __nv_bfloat16*>(dO), lse, w.dvec, w.lse2, w.dqacc,
-                                            s.B * s.H, N, (int)s.n_pad(), d, cs));
+  return prep_impl(o, dO, lse, B, H, N, N, d, dtype, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_bwd_tiles(const void* q, const void* k, const void* v, const void* dO, void* dq, void* dk, void* dv,
                        int B, int H, int N, int d, float scale, int causal, fa_dtype dtype, void* workspace,
                        size_t workspace_bytes, fa_stream_t stream) {
-  Shape s;
-  fa_status st = check_shape(B, H, N, d, dtype, &s);
-  if (st != FA_OK) return st;
-  if ((st = check_scale(scale)) != FA_OK) return st;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (s.empty()) return FA_OK;
-  if ((st = check_ptrs({q, k, v, dO, dk, dv}, dtype)) != FA_OK) return st;
-  if (dtype == FA_DTYPE_FP32 && (st = check_ptrs({dq}, dtype)) != FA_OK) return st;
-  Workspace w;
-  if ((st = carve_workspace(s, dtype, workspace, workspace_bytes, &w)) != FA_OK) return st;
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (dtype == FA_DTYPE_FP32)
-    return from_cuda(fa::launch_bwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
-                                        static_cast<const float*>(v), static_cast<const float*>(dO), w.lse2, w.dvec,
-                                        static_cast<float*>(dq), static_cast<float*>(dk), static_cast<float*>(dv),
-                                        (int)(s.B * s.H), N, d, scale, causal, cs));
-  unsigned int* fault = fault_word_for_current_device();
-  if (!fault) return FA_ERR_CUDA;
-  fa::BwdArgs a;
-  const int bm = fa::bwd_bf16_block_m(d);
-  const long long heads = s.B * s.H;
-  if (!encode_bf16_heads(&a.tm_q, q, heads, N, d, bm) || !encode_bf16_heads(&a.tm_k, k, heads, N, d, 128) ||
-      !encode_bf16_heads(&a.tm_v, v, heads, N, d, 128) || !encode_bf16_heads(&a.tm_do, dO, heads, N, d, bm))
-    return FA_ERR_CUDA;
-  a.lse2 = w.lse2;
-  a.dvec = w.dvec;
-  a.dqacc = w.dqacc;
-  a.dk = static_cast<__nv_bfloat16*>(dk);
-  a.dv = static_cast<__nv_bfloat16*>(dv);
-  a.B = B;
-  a.H = H;
-  a.N = N;
-  a.d = d;
-  a.scale_log2 = scale * kLog2e;
-  a.scale = scale;
-  a.causal = causal;
-  a.fault = fault;
-  return from_cuda(fa::launch_bwd_bf16(a, cs));
+  return tiles_impl(q, k, v, dO, dq, dk, dv, B, H, N, N, d, scale, causal, dtype, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_bwd_dq_finish(void* dq, int B, int H, int N, int d, float scale, fa_dtype dtype, void* workspace,
                            size_t workspace_bytes, fa_stream_t stream) {
-  Shape s;
-  fa_status st = check_shape(B, H, N, d, dtype, &s);
-  if (st != FA_OK) return st;
-  if ((st = check_scale(scale)) != FA_OK) return st;
-  if (s.empty() || dtype == FA_DTYPE_FP32) return FA_OK;
-  if ((st = check_ptrs({dq}, dtype)) != FA_OK) return st;
-  Workspace w;
-  if ((st = carve_workspace(s, dtype, workspace, workspace_bytes, &w)) != FA_OK) return st;
-  return from_cuda(fa::launch_dq_finish_bf16(w.dqacc, static_cast<__nv_bfloat16*>(dq), s.B * s.H, N,
-                                             (int)s.n_pad(), d, scale, reinterpret_cast<cudaStream_t>(stream)));
+  return finish_impl(dq, B, H, N, N, d, scale, dtype, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                  void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, fa_dtype dtype,
                  void* workspace, size_t workspace_bytes, fa_stream_t stream) {
-  Shape s;
-  fa_status st = check_shape(B, H, N, d, dtype, &s);
-  if (st != FA_OK) return st;
-  if ((st = check_scale(scale)) != FA_OK) return st;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (s.empty()) return FA_OK;
-  if ((st = check_ptrs({q, k, v, o, dO, lse, dq, dk, dv}, dtype)) != FA_OK) return st;
-  Workspace w;
-  if ((st = carve_workspace(s, dtype, workspace, workspace_bytes, &w)) != FA_OK) return st;
-  if ((st = fa_bwd_prep(o, dO, lse, B, H, N, d, dtype, workspace, workspace_bytes, stream)) != FA_OK) return st;
-  if ((st = fa_bwd_tiles(q, k, v, dO, dq, dk, dv, B, H, N, d, scale, causal, dtype, workspace, workspace_bytes,
-                         stream)) != FA_OK)
-    return st;
-  return fa_bwd_dq_finish(dq, B, H, N, d, scale, dtype, workspace, workspace_bytes, stream);
+  return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, N, d, scale, causal, dtype, workspace, workspace_bytes,
+                  stream);
+}
+
+fa_status fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                    void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                    fa_dtype dtype, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, dtype, workspace, workspace_bytes,
+                  stream);
+}
+
+static_assert(FA_MERGE_MAX_PARTS == fa::kMaxMergeParts, "merge part limit differs between fa.h and the kernel");
+
+fa_status fa_merge(const void* const* o_parts, const float* const* lse_parts, int n_parts, void* o, float* lse,
+                   int B, int H, int N, int d, fa_dtype dtype, fa_stream_t stream) {
+  if (B < 0 || H < 0 || N < 0 || d <= 0) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP32) return FA_ERR_INVALID_ARG;
+  if (n_parts < 1 || n_parts > FA_MERGE_MAX_PARTS) return FA_ERR_INVALID_ARG;
+  if (d > 256) return FA_ERR_UNSUPPORTED;
+  const long long rows = (long long)B * H * N;
+  if (rows == 0) return FA_OK;
+  if (rows * d > (1ll << 40) || (rows + 7) / 8 >= (1ll << 31)) return FA_ERR_UNSUPPORTED;
+  if (o_parts == nullptr || lse_parts == nullptr) return FA_ERR_INVALID_ARG;
+  fa_status st;
+  if ((st = check_ptrs({o, lse}, dtype)) != FA_OK) return st;
+  fa::MergeArgs a;
+  for (int i = 0; i < n_parts; ++i) {
+    if ((st = check_ptrs({o_parts[i], lse_parts[i]}, dtype)) != FA_OK) return st;
+    a.o_parts[i] = o_parts[i];
+    a.lse_parts[i] = lse_parts[i];
+  }
+  for (int i = n_parts; i < fa::kMaxMergeParts; ++i) {
+    a.o_parts[i] = nullptr;
+    a.lse_parts[i] = nullptr;
+  }
+  a.n_parts = n_parts;
+  a.o = o;
+  a.lse = lse;
+  a.rows = rows;
+  a.d = d;
+  a.bf16 = dtype == FA_DTYPE_BF16 ? 1 : 0;
+  return from_cuda(fa::launch_merge(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 fa_status fa_sync_status(fa_stream_t stream) {

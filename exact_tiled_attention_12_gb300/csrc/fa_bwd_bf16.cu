@@ -124,9 +124,10 @@ __device__ __forceinline__ bool pair_sync_and(int id, bool ok) {
   return r != 0;
 }
 
-// RAGGED (N not a multiple of 128): 3-D per-head tensor maps whose rows past
-// N read as zero, masking of the keys past N and row-predicated dK/dV
-// stores.  Otherwise 2-D maps over the [B·H·N, d] row view and none of that.
+// RAGGED (Nq or Nk not a multiple of 128): 3-D per-head tensor maps whose
+// rows past the end read as zero, masking of the keys past Nk and
+// row-predicated dK/dV stores.  Otherwise 2-D maps over the row views and
+// none of that.
 template <int D, bool CAUSAL, bool RAGGED>
 // 10 warps: at most 3 per SM sub-partition, so up to 168 registers a thread.
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_constant__ BwdArgs a) {
@@ -148,25 +149,27 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int N = a.N;
+  const int Nq = a.Nq, Nk = a.Nk;
+  const int off = Nk - Nq;                   // causal: query i sees keys j ≤ i + off
   // Non-causal: head-major grid (K/V tile fastest), so a wave touches few
   // heads' Q, dO and dQ accumulator and they stay in L2.  Causal: batch·head
   // fastest, so the heaviest tiles (small jt) of every head go first.
   const int jt = CAUSAL ? (int)blockIdx.y : (int)blockIdx.x;
   const int bh = CAUSAL ? (int)blockIdx.x : (int)blockIdx.y;
   const int kv0 = jt * kBN;
-  const int row0 = bh * N;                   // first row of this head in O, dK, dV
-  const int n_tiles = RAGGED ? (N + kBM - 1) / kBM : N / kBM;   // tiles per head; the last may be ragged
+  const int n_tiles = RAGGED ? (Nq + kBM - 1) / kBM : Nq / kBM;   // query tiles per head; the last may be ragged
   // First row of this head in the workspace (whole tiles per head; the
   // workspace has fewer than 2^31 rows).
-  const int wrow0 = RAGGED ? bh * n_tiles * kBM : row0;
-  const int i0 = CAUSAL ? jt : 0;            // first query tile with a visible query (kBM == kBN)
-  // Loads rows [pos, pos + 128) of this head.
-  auto load_rows = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar_addr, int x, int pos) {
+  const int wrow0 = RAGGED ? bh * n_tiles * kBM : bh * Nq;
+  // First query tile with a query that sees a key of this tile: query tile i
+  // reaches keys up to 128i + 127 + off, so i ≥ ⌊(kv0 − off) / 128⌋ (kBM == kBN).
+  const int i0 = CAUSAL ? (kv0 > off ? (kv0 - off) / kBM : 0) : 0;
+  // Loads rows [pos, pos + 128) of this head from a map over heads of `nrows` rows.
+  auto load_rows = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar_addr, int x, int pos, int nrows) {
     if constexpr (RAGGED)
       tma_load_3d(dst, map, bar_addr, x, pos, bh);
     else
-      tma_load_2d(dst, map, bar_addr, x, row0 + pos);
+      tma_load_2d(dst, map, bar_addr, x, bh * nrows + pos);
   };
   const int n = n_tiles - i0;                // query tiles visited
 
@@ -201,13 +204,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
     const int h = warp >> 2;                       // query columns [64h, 64h + 64)
     const int r = g * 32 + lane;                   // key row within the tile = TMEM lane
     const int kv = kv0 + r;
-    // A key past N (last tile of a ragged head) reads as a zero row, so its
+    // A key past Nk (last tile of a ragged head) reads as a zero row, so its
     // score is 0 and 2^(−LSE·log2 e) could overflow; its Pᵀ and dSᵀ are
     // masked to 0 so that dQ never sees it.  Causal tiles mask it already
-    // (it lies above the diagonal of every real query).  Queries past N need
+    // (it lies beyond every real query's last key).  Queries past Nq need
     // nothing: their −LSE is −∞ and their dO row is zero.
-    const bool dead_key = RAGGED && kv >= N;
-    [[maybe_unused]] const bool ragged_cta = RAGGED && !CAUSAL && kv0 + kBN > N;   // uniform over the CTA
+    const bool dead_key = RAGGED && kv >= Nk;
+    [[maybe_unused]] const bool ragged_cta = RAGGED && !CAUSAL && kv0 + kBN > Nk;   // uniform over the CTA
     [[maybe_unused]] const int dead_lim = dead_key ? (1 << 30) : -(1 << 30);        // masks all columns or none
     const uint32_t lane_off = (uint32_t)(g * 32) << 16;
     const float sl2 = a.scale_log2;
@@ -224,7 +227,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       // one packed FMA (the exponent) and one packed add/multiply (dS).
       const uint64_t* nlse = reinterpret_cast<const uint64_t*>(sgen + C::kLSE + st * kBM * 4);
       const uint64_t* ndv = reinterpret_cast<const uint64_t*>(sgen + C::kDV + st * kBM * 4);
-      const bool masked = CAUSAL && i == 0;        // the diagonal tile (q0 == kv0)
+      // Key kv0 + r is visible to query q0 + c iff r − c ≤ delta; the tile
+      // masks something iff its largest key passes its first query's limit
+      // (square problems: only the diagonal tile, delta = 0).
+      const int delta = q0 + off - kv0;
+      const bool masked = CAUSAL && delta < kBN - 1;
       const uint64_t sl2x2 = f2_pack(sl2, sl2);
       uint64_t p[32];                              // P for query columns 64h + 2e, 2e + 1
       if (ok) {
@@ -235,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
           uint32_t s[32];
           tmem_ld_x32(tmem + lane_off + C::kColS + (uint32_t)c0, s);
           if (masked)
-            p_chunk<true, kPolyEvery>(s, sl2x2, nlse + (c0 >> 1), r - c0, p + ch * 16);
+            p_chunk<true, kPolyEvery>(s, sl2x2, nlse + (c0 >> 1), r - c0 - delta, p + ch * 16);
           else if (ragged_cta)
             p_chunk<true, 0>(s, sl2x2, nlse + (c0 >> 1), dead_lim, p + ch * 16);
           else
@@ -325,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       tc_fence_after();
       const uint32_t col = h == 0 ? C::kColDV : C::kColDK;
       const float mul = h == 0 ? 1.0f : a.scale;
-      __nv_bfloat16* dst = (h == 0 ? a.dv : a.dk) + ((size_t)row0 + (size_t)kv) * D;
+      __nv_bfloat16* dst = (h == 0 ? a.dv : a.dk) + ((size_t)bh * (size_t)Nk + (size_t)kv) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t v[32];
@@ -349,8 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       prefetch_tmap(&a.tm_do);
       mbar_arrive_expect_tx(bar(kKVFull), 2u * C::kTile);
       for (int bx = 0; bx < D / 64; ++bx) {
-        load_rows(sbase + C::kK + bx * kBox, &a.tm_k, bar(kKVFull), 64 * bx, kv0);
-        load_rows(sbase + C::kV + bx * kBox, &a.tm_v, bar(kKVFull), 64 * bx, kv0);
+        load_rows(sbase + C::kK + bx * kBox, &a.tm_k, bar(kKVFull), 64 * bx, kv0, Nk);
+        load_rows(sbase + C::kV + bx * kBox, &a.tm_v, bar(kKVFull), 64 * bx, kv0, Nk);
       }
       int issued[2] = {0, 0};
       for (int i = 0; i < n; ++i) {
@@ -359,8 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         const int q0 = (i0 + i) * kBM;
         mbar_arrive_expect_tx(bar(kQFull + s), 2u * C::kTile + 2u * kBM * 4);
         for (int bx = 0; bx < D / 64; ++bx) {
-          load_rows(sbase + C::kQ + s * C::kTile + bx * kBox, &a.tm_q, bar(kQFull + s), 64 * bx, q0);
-          load_rows(sbase + C::kDO + s * C::kTile + bx * kBox, &a.tm_do, bar(kQFull + s), 64 * bx, q0);
+          load_rows(sbase + C::kQ + s * C::kTile + bx * kBox, &a.tm_q, bar(kQFull + s), 64 * bx, q0, Nq);
+          load_rows(sbase + C::kDO + s * C::kTile + bx * kBox, &a.tm_do, bar(kQFull + s), 64 * bx, q0, Nq);
         }
         bulk_load(sbase + C::kLSE + s * kBM * 4, a.lse2 + wrow0 + q0, kBM * 4, bar(kQFull + s));
         bulk_load(sbase + C::kDV + s * kBM * 4, a.dvec + wrow0 + q0, kBM * 4, bar(kQFull + s));
@@ -466,7 +473,7 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t s) {
   const size_t smem = BwdCfg<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const unsigned tiles = (unsigned)((a.N + kBN - 1) / kBN), heads = (unsigned)(a.B * a.H);
+  const unsigned tiles = (unsigned)((a.Nk + kBN - 1) / kBN), heads = (unsigned)(a.B * a.H);
   const dim3 grid = CAUSAL ? dim3(heads, tiles) : dim3(tiles, heads);
   kern<<<grid, kThreads, smem, s>>>(a);
   return cudaGetLastError();
@@ -477,12 +484,12 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t s) {
 // Grid (n_pad·D/8 / 256, heads): one group of D/8 threads per workspace row
 // (n_pad rows per head, a multiple of 128, so every thread has a row); each
 // thread reads 8 bf16 of O and of dO (16 bytes each), so a warp covers 32·8
-// contiguous elements.  Rows past N in a head are padding: D = 0, −LSE = −∞.
+// contiguous elements.  Rows past Nq in a head are padding: D = 0, −LSE = −∞.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                        const __nv_bfloat16* __restrict__ dO,
                                                        const float* __restrict__ lse, float* __restrict__ dvec,
-                                                       float* __restrict__ lse2, float* __restrict__ dqacc, int N,
+                                                       float* __restrict__ lse2, float* __restrict__ dqacc, int Nq,
                                                        int n_pad) {
   constexpr int G = D / 8;   // threads per row
   const int tid = (int)(blockIdx.x * blockDim.x + threadIdx.x);
@@ -490,8 +497,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   const int part = tid % G;
   const long long head = blockIdx.y;
   const long long row = head * n_pad + pos;   // workspace row
-  const long long src = head * N + pos;       // row of O, dO and LSE
-  const bool live = pos < N;
+  const long long src = head * Nq + pos;       // row of O, dO and LSE
+  const bool live = pos < Nq;
   float acc = 0.f;
   {
     float4* z = reinterpret_cast<float4*>(dqacc + row * D + part * 8);
@@ -520,19 +527,19 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   }
 }
 
-// Grid (⌈N·D/8 / 256⌉, heads): one thread per 8 consecutive dQ elements of a
-// row below N; the accumulator has n_pad rows per head, dQ has N.
+// Grid (⌈Nq·D/8 / 256⌉, heads): one thread per 8 consecutive dQ elements of a
+// row below Nq; the accumulator has n_pad rows per head, dQ has Nq.
 template <int D>
 __global__ void __launch_bounds__(256) dq_finish_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
-                                                        int N, int n_pad, float scale) {
+                                                        int Nq, int n_pad, float scale) {
   constexpr int G = D / 8;
   const int tid = (int)(blockIdx.x * blockDim.x + threadIdx.x);
   const int pos = tid / G;
-  if (pos >= N) return;
+  if (pos >= Nq) return;
   const int part = tid % G;
   const long long head = blockIdx.y;
   const long long arow = head * n_pad + pos;
-  const long long i = (head * N + pos) * G + part;   // 16-byte chunk of dQ
+  const long long i = (head * Nq + pos) * G + part;   // 16-byte chunk of dQ
   const float4* a = reinterpret_cast<const float4*>(acc + arow * D + part * 8);
   const float4 a0 = a[0];
   const float4 a1 = a[1];
@@ -551,7 +558,7 @@ int bwd_bf16_block_m(int) { return kBM; }
 size_t bwd_bf16_smem_bytes(int d) { return d == 64 ? BwdCfg<64>::kBytes : BwdCfg<128>::kBytes; }
 
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t s) {
-  const bool ragged = a.N % kBN != 0;
+  const bool ragged = a.Nq % kBM != 0 || a.Nk % kBN != 0;
   if (a.d == 128) {
     if (ragged) return a.causal ? launch_impl<128, true, true>(a, s) : launch_impl<128, false, true>(a, s);
     return a.causal ? launch_impl<128, true, false>(a, s) : launch_impl<128, false, false>(a, s);
@@ -564,27 +571,27 @@ cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_bwd_prep_bf16(const __nv_bfloat16* o, const __nv_bfloat16* dO, const float* lse, float* dvec,
-                                 float* lse2, float* dqacc, long long heads, int N, int n_pad, int d,
+                                 float* lse2, float* dqacc, long long heads, int Nq, int n_pad, int d,
                                  cudaStream_t s) {
   if (heads <= 0 || heads > 65535 || n_pad % 128 != 0) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)((long long)n_pad * (d / 8) / 256), (unsigned)heads);
   if (d == 128)
-    bwd_prep_kernel<128><<<grid, 256, 0, s>>>(o, dO, lse, dvec, lse2, dqacc, N, n_pad);
+    bwd_prep_kernel<128><<<grid, 256, 0, s>>>(o, dO, lse, dvec, lse2, dqacc, Nq, n_pad);
   else if (d == 64)
-    bwd_prep_kernel<64><<<grid, 256, 0, s>>>(o, dO, lse, dvec, lse2, dqacc, N, n_pad);
+    bwd_prep_kernel<64><<<grid, 256, 0, s>>>(o, dO, lse, dvec, lse2, dqacc, Nq, n_pad);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
-cudaError_t launch_dq_finish_bf16(const float* dqacc, __nv_bfloat16* dq, long long heads, int N, int n_pad, int d,
+cudaError_t launch_dq_finish_bf16(const float* dqacc, __nv_bfloat16* dq, long long heads, int Nq, int n_pad, int d,
                                   float scale, cudaStream_t s) {
   if (heads <= 0 || heads > 65535) return cudaErrorInvalidValue;
-  const dim3 grid((unsigned)(((long long)N * (d / 8) + 255) / 256), (unsigned)heads);
+  const dim3 grid((unsigned)(((long long)Nq * (d / 8) + 255) / 256), (unsigned)heads);
   if (d == 128)
-    dq_finish_kernel<128><<<grid, 256, 0, s>>>(dqacc, dq, N, n_pad, scale);
+    dq_finish_kernel<128><<<grid, 256, 0, s>>>(dqacc, dq, Nq, n_pad, scale);
   else if (d == 64)
-    dq_finish_kernel<64><<<grid, 256, 0, s>>>(dqacc, dq, N, n_pad, scale);
+    dq_finish_kernel<64><<<grid, 256, 0, s>>>(dqacc, dq, Nq, n_pad, scale);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

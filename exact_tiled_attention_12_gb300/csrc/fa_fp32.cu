@@ -4,8 +4,9 @@
 // tensor-core path ("Flash Attention" tutorial, 2.Online Softmax §4.2, with
 // blocks of 32 keys), computed with fp32 FMAs so that results agree with an
 // exact evaluation to ~1e-6.  No tensor cores: bf16 products cannot reach
-// that accuracy.  Any N ≥ 1 and 1 ≤ d ≤ 128; causal masking as in the bf16
-// path (key j visible to query i iff j ≤ i).
+// that accuracy.  Nq queries over Nk keys (any sizes ≥ 1), 1 ≤ d ≤ 128;
+// causal masking as in the bf16 path (key j visible to query i iff
+// j ≤ i + Nk − Nq, the queries being the last Nq positions).
 //
 // Each warp owns one output row (a query row in the forward and in the dQ
 // pass, a key row in the dK/dV pass); lane j scores key/query j of the
@@ -42,12 +43,12 @@ __device__ __forceinline__ void stage_rows(float* dst, const float* src, int r0,
   }
 }
 
-// Forward.  grid = (ceil(N / 8), B·H); one warp per query row.
+// Forward.  grid = (ceil(Nq / 8), B·H); one warp per query row.
 __global__ void __launch_bounds__(32 * kRowsPerBlock) fwd_f32_kernel(const float* __restrict__ q,
                                                                      const float* __restrict__ k,
                                                                      const float* __restrict__ v, float* __restrict__ o,
-                                                                     float* __restrict__ lse, int N, int d, float scale,
-                                                                     int causal) {
+                                                                     float* __restrict__ lse, int Nq, int Nk, int d,
+                                                                     float scale, int causal) {
   extern __shared__ float sm[];
   const int ld = d + 1;
   float* sK = sm;
@@ -56,23 +57,24 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) fwd_f32_kernel(const float
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t head = blockIdx.y;
   const int i = blockIdx.x * kRowsPerBlock + warp;
-  const bool live = i < N;
-  const float* qh = q + head * (size_t)N * d;
-  const float* kh = k + head * (size_t)N * d;
-  const float* vh = v + head * (size_t)N * d;
+  const bool live = i < Nq;
+  const int off = Nk - Nq;                         // causal: query i sees keys ≤ i + off
+  const float* qh = q + head * (size_t)Nq * d;
+  const float* kh = k + head * (size_t)Nk * d;
+  const float* vh = v + head * (size_t)Nk * d;
   for (int c = lane; c < d; c += 32) sQ[warp * d + c] = live ? qh[(size_t)i * d + c] : 0.f;
-  const int last_row = min(N - 1, (int)blockIdx.x * kRowsPerBlock + kRowsPerBlock - 1);
-  const int key_end = causal ? last_row + 1 : N;   // keys any row of this block can see
+  const int last_row = min(Nq - 1, (int)blockIdx.x * kRowsPerBlock + kRowsPerBlock - 1);
+  const int key_end = causal ? last_row + off + 1 : Nk;   // keys any row of this block can see
   float m = -INFINITY, ell = 0.f;
   float acc[kMaxD / 32] = {0.f, 0.f, 0.f, 0.f};
   for (int j0 = 0; j0 < key_end; j0 += kTile) {
     __syncthreads();
-    stage_rows(sK, kh, j0, N, d);
-    stage_rows(sV, vh, j0, N, d);
+    stage_rows(sK, kh, j0, Nk, d);
+    stage_rows(sV, vh, j0, Nk, d);
     __syncthreads();
     if (!live) continue;
     const int j = j0 + lane;
-    const bool vis = j < N && (!causal || j <= i);
+    const bool vis = j < Nk && (!causal || j <= i + off);
     float s = -INFINITY;
     if (vis) {
       float dot = 0.f;
@@ -102,9 +104,9 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) fwd_f32_kernel(const float
 #pragma unroll
     for (int u = 0; u < kMaxD / 32; ++u) {
       const int c = lane + 32 * u;
-      if (c < d) o[(head * N + i) * (size_t)d + c] = acc[u] * inv;
+      if (c < d) o[(head * Nq + i) * (size_t)d + c] = acc[u] * inv;
     }
-    if (lane == 0) lse[head * N + i] = m + logf(ell);
+    if (lane == 0) lse[head * Nq + i] = m + logf(ell);
   }
 }
 
@@ -128,7 +130,7 @@ __global__ void __launch_bounds__(256) prep_f32_kernel(const float* __restrict__
 __global__ void __launch_bounds__(32 * kRowsPerBlock) dq_f32_kernel(
     const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
     const float* __restrict__ dO, const float* __restrict__ lse, const float* __restrict__ dvec,
-    float* __restrict__ dq, int N, int d, float scale, int causal) {
+    float* __restrict__ dq, int Nq, int Nk, int d, float scale, int causal) {
   extern __shared__ float sm[];
   const int ld = d + 1;
   float* sK = sm;
@@ -138,25 +140,27 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) dq_f32_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t head = blockIdx.y;
   const int i = blockIdx.x * kRowsPerBlock + warp;
-  const bool live = i < N;
-  const size_t base = head * (size_t)N * d;
+  const bool live = i < Nq;
+  const int off = Nk - Nq;
+  const size_t qbase = head * (size_t)Nq * d;
+  const size_t kbase = head * (size_t)Nk * d;
   for (int c = lane; c < d; c += 32) {
-    sQ[warp * d + c] = live ? q[base + (size_t)i * d + c] : 0.f;
-    sG[warp * d + c] = live ? dO[base + (size_t)i * d + c] : 0.f;
+    sQ[warp * d + c] = live ? q[qbase + (size_t)i * d + c] : 0.f;
+    sG[warp * d + c] = live ? dO[qbase + (size_t)i * d + c] : 0.f;
   }
-  const float Li = live ? lse[head * N + i] : 0.f;
-  const float Di = live ? dvec[head * N + i] : 0.f;
-  const int last_row = min(N - 1, (int)blockIdx.x * kRowsPerBlock + kRowsPerBlock - 1);
-  const int key_end = causal ? last_row + 1 : N;
+  const float Li = live ? lse[head * Nq + i] : 0.f;
+  const float Di = live ? dvec[head * Nq + i] : 0.f;
+  const int last_row = min(Nq - 1, (int)blockIdx.x * kRowsPerBlock + kRowsPerBlock - 1);
+  const int key_end = causal ? last_row + off + 1 : Nk;
   float acc[kMaxD / 32] = {0.f, 0.f, 0.f, 0.f};
   for (int j0 = 0; j0 < key_end; j0 += kTile) {
     __syncthreads();
-    stage_rows(sK, k + base, j0, N, d);
-    stage_rows(sV, v + base, j0, N, d);
+    stage_rows(sK, k + kbase, j0, Nk, d);
+    stage_rows(sV, v + kbase, j0, Nk, d);
     __syncthreads();
     if (!live) continue;
     const int j = j0 + lane;
-    const bool vis = j < N && (!causal || j <= i);
+    const bool vis = j < Nk && (!causal || j <= i + off);
     float ds = 0.f;
     if (vis) {
       float s = 0.f, dp = 0.f;
@@ -180,7 +184,7 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) dq_f32_kernel(
 #pragma unroll
     for (int u = 0; u < kMaxD / 32; ++u) {
       const int c = lane + 32 * u;
-      if (c < d) dq[base + (size_t)i * d + c] = acc[u] * scale;
+      if (c < d) dq[qbase + (size_t)i * d + c] = acc[u] * scale;
     }
   }
 }
@@ -189,7 +193,7 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) dq_f32_kernel(
 __global__ void __launch_bounds__(32 * kRowsPerBlock) dkv_f32_kernel(
     const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
     const float* __restrict__ dO, const float* __restrict__ lse, const float* __restrict__ dvec,
-    float* __restrict__ dk, float* __restrict__ dv, int N, int d, float scale, int causal) {
+    float* __restrict__ dk, float* __restrict__ dv, int Nq, int Nk, int d, float scale, int causal) {
   extern __shared__ float sm[];
   const int ld = d + 1;
   float* sQ = sm;
@@ -201,30 +205,32 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) dkv_f32_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t head = blockIdx.y;
   const int j = blockIdx.x * kRowsPerBlock + warp;
-  const bool live = j < N;
-  const size_t base = head * (size_t)N * d;
+  const bool live = j < Nk;
+  const int off = Nk - Nq;
+  const size_t qbase = head * (size_t)Nq * d;
+  const size_t kbase = head * (size_t)Nk * d;
   for (int c = lane; c < d; c += 32) {
-    sK[warp * d + c] = live ? k[base + (size_t)j * d + c] : 0.f;
-    sV[warp * d + c] = live ? v[base + (size_t)j * d + c] : 0.f;
+    sK[warp * d + c] = live ? k[kbase + (size_t)j * d + c] : 0.f;
+    sV[warp * d + c] = live ? v[kbase + (size_t)j * d + c] : 0.f;
   }
-  // Under the causal mask only queries i ≥ j see key j.
-  const int first_row = blockIdx.x * kRowsPerBlock;
-  const int q_begin = causal ? (first_row / kTile) * kTile : 0;
+  // Under the causal mask only queries i ≥ j − off see key j.
+  const int first_key = blockIdx.x * kRowsPerBlock;
+  const int q_begin = causal ? (max(first_key - off, 0) / kTile) * kTile : 0;
   float acc_v[kMaxD / 32] = {0.f, 0.f, 0.f, 0.f};
   float acc_k[kMaxD / 32] = {0.f, 0.f, 0.f, 0.f};
-  for (int i0 = q_begin; i0 < N; i0 += kTile) {
+  for (int i0 = q_begin; i0 < Nq; i0 += kTile) {
     __syncthreads();
-    stage_rows(sQ, q + base, i0, N, d);
-    stage_rows(sG, dO + base, i0, N, d);
+    stage_rows(sQ, q + qbase, i0, Nq, d);
+    stage_rows(sG, dO + qbase, i0, Nq, d);
     if (threadIdx.x < kTile) {
       const int ii = i0 + threadIdx.x;
-      sL[threadIdx.x] = ii < N ? lse[head * N + ii] : 0.f;
-      sD[threadIdx.x] = ii < N ? dvec[head * N + ii] : 0.f;
+      sL[threadIdx.x] = ii < Nq ? lse[head * Nq + ii] : 0.f;
+      sD[threadIdx.x] = ii < Nq ? dvec[head * Nq + ii] : 0.f;
     }
     __syncthreads();
     if (!live) continue;
     const int i = i0 + lane;
-    const bool vis = i < N && (!causal || j <= i);
+    const bool vis = i < Nq && (!causal || j <= i + off);
     float p = 0.f, ds = 0.f;
     if (vis) {
       float s = 0.f, dp = 0.f;
@@ -253,8 +259,8 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) dkv_f32_kernel(
     for (int u = 0; u < kMaxD / 32; ++u) {
       const int c = lane + 32 * u;
       if (c < d) {
-        dv[base + (size_t)j * d + c] = acc_v[u];
-        dk[base + (size_t)j * d + c] = acc_k[u] * scale;
+        dv[kbase + (size_t)j * d + c] = acc_v[u];
+        dk[kbase + (size_t)j * d + c] = acc_k[u] * scale;
       }
     }
   }
@@ -262,11 +268,11 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) dkv_f32_kernel(
 
 }  // namespace
 
-cudaError_t launch_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int BH, int N, int d,
-                           float scale, int causal, cudaStream_t s) {
+cudaError_t launch_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int BH, int Nq,
+                           int Nk, int d, float scale, int causal, cudaStream_t s) {
   const size_t smem = (size_t)(2 * kTile * (d + 1) + kRowsPerBlock * d) * sizeof(float);
-  dim3 grid((unsigned)((N + kRowsPerBlock - 1) / kRowsPerBlock), (unsigned)BH);
-  fwd_f32_kernel<<<grid, 32 * kRowsPerBlock, smem, s>>>(q, k, v, o, lse, N, d, scale, causal);
+  dim3 grid((unsigned)((Nq + kRowsPerBlock - 1) / kRowsPerBlock), (unsigned)BH);
+  fwd_f32_kernel<<<grid, 32 * kRowsPerBlock, smem, s>>>(q, k, v, o, lse, Nq, Nk, d, scale, causal);
   return cudaGetLastError();
 }
 
@@ -278,15 +284,17 @@ cudaError_t launch_bwd_prep_f32(const float* o, const float* dO, const float* ls
 }
 
 cudaError_t launch_bwd_f32(const float* q, const float* k, const float* v, const float* dO, const float* lse,
-                           const float* dvec, float* dq, float* dk, float* dv, int BH, int N, int d, float scale,
-                           int causal, cudaStream_t s) {
-  dim3 grid((unsigned)((N + kRowsPerBlock - 1) / kRowsPerBlock), (unsigned)BH);
+                           const float* dvec, float* dq, float* dk, float* dv, int BH, int Nq, int Nk, int d,
+                           float scale, int causal, cudaStream_t s) {
+  const dim3 grid_q((unsigned)((Nq + kRowsPerBlock - 1) / kRowsPerBlock), (unsigned)BH);
   const size_t smem_q = (size_t)(2 * kTile * (d + 1) + 2 * kRowsPerBlock * d) * sizeof(float);
-  dq_f32_kernel<<<grid, 32 * kRowsPerBlock, smem_q, s>>>(q, k, v, dO, lse, dvec, dq, N, d, scale, causal);
+  dq_f32_kernel<<<grid_q, 32 * kRowsPerBlock, smem_q, s>>>(q, k, v, dO, lse, dvec, dq, Nq, Nk, d, scale, causal);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  const dim3 grid_k((unsigned)((Nk + kRowsPerBlock - 1) / kRowsPerBlock), (unsigned)BH);
   const size_t smem_kv = (size_t)(2 * kTile * (d + 1) + 2 * kRowsPerBlock * d + 2 * kTile) * sizeof(float);
-  dkv_f32_kernel<<<grid, 32 * kRowsPerBlock, smem_kv, s>>>(q, k, v, dO, lse, dvec, dk, dv, N, d, scale, causal);
+  dkv_f32_kernel<<<grid_k, 32 * kRowsPerBlock, smem_kv, s>>>(q, k, v, dO, lse, dvec, dk, dv, Nq, Nk, d, scale,
+                                                              causal);
   return cudaGetLastError();
 }
 

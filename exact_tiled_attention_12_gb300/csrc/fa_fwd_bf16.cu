@@ -107,9 +107,10 @@ __device__ __forceinline__ float exp_tile_to_p(const uint32_t (&s)[128], float s
   return (la + lb) + (lc + ld);
 }
 
-// RAGGED (N not a multiple of 128): 3-D per-head tensor maps whose rows past
-// N read as zero, masking of the missing keys and row-predicated stores.
-// Otherwise 2-D maps over the [B·H·N, d] row view and none of that code.
+// RAGGED (Nq or Nk not a multiple of 128): 3-D per-head tensor maps whose
+// rows past the end read as zero, masking of the missing keys and
+// row-predicated stores.  Otherwise 2-D maps over the row views and none of
+// that code.
 template <int D, bool CAUSAL, bool RAGGED>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_constant__ FwdArgs a) {
   using L = FwdLayout<D>;
@@ -130,15 +131,16 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int N = a.N;
-  const int pairs = (N + 2 * kBM - 1) / (2 * kBM);       // two-tile units per head
+  const int Nq = a.Nq, Nk = a.Nk;
+  const int off = Nk - Nq;                               // causal: query i sees keys j ≤ i + off
+  const int pairs = (Nq + 2 * kBM - 1) / (2 * kBM);      // two-tile units per head
   // Work of this CTA (1-D grid).  Causal: batch·head fastest with the
   // heaviest pairs first across the whole grid (longest tiles scheduled
   // first).  Non-causal: head-major (pair fastest), so a wave touches few
   // heads' K/V and they stay in L2; the last `tail` units are split into
   // `splits` CTAs over equal K/V sub-ranges, each writing a partial result
   // (normalised O and LSE of its keys) that fwd_combine merges.
-  const int n_kv_all = (N + kBN - 1) / kBN;
+  const int n_kv_all = (Nk + kBN - 1) / kBN;
   int bh, pair, kv_begin = 0, n_kv = n_kv_all, part_slot = -1;
   const int idx = (int)blockIdx.x;
   if (CAUSAL) {
@@ -157,26 +159,32 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
     n_kv = (part + 1) * n_kv / a.splits - kv_begin;
   }
   const int q0 = pair * 2 * kBM;
-  const int row0 = bh * N;                                 // first row of this head in the [B·H·N, d] view
-  // Keys of the head's last K/V tile that exist (128 unless N is ragged).
-  // Non-causal rows must not see the zero-filled keys past N; causal rows
-  // never do, since those keys lie above the diagonal of every real query.
-  const int kv_tail = N - (n_kv_all - 1) * kBN;
+  const int row0 = bh * Nq;                                // first row of this head in the [B·H·Nq, d] view
+  // Keys of the head's last K/V tile that exist (128 unless Nk is ragged).
+  // Non-causal rows must not see the zero-filled keys past Nk; causal rows
+  // never do, since those keys lie beyond every real query's last key.
+  const int kv_tail = Nk - (n_kv_all - 1) * kBN;
   const bool ragged_last = RAGGED && !CAUSAL && kv_tail < kBN && kv_begin + n_kv == n_kv_all;
-  // Loads rows [pos, pos + 128) of this head.
-  auto load_rows = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar_addr, int x, int pos) {
+  // Loads rows [pos, pos + 128) of this head from a map over heads of `n` rows.
+  auto load_rows = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar_addr, int x, int pos, int n) {
     if constexpr (RAGGED)
       tma_load_3d(dst, map, bar_addr, x, pos, bh);
     else
-      tma_load_2d(dst, map, bar_addr, x, row0 + pos);
+      tma_load_2d(dst, map, bar_addr, x, bh * n + pos);
   };
 
-  // Number of K/V tiles each query tile visits (0 if the tile is past N).
-  int n_t[2];
+  // Number of K/V tiles each query tile visits (0 if the tile is past Nq),
+  // and under the causal mask the first tile that masks some of its scores:
+  // tile j holds keys 128j + c, visible to row qt + r iff
+  // c ≤ r + (qt + off − 128j); the last row that exists sees up to
+  // min(qt + 127, Nq − 1) + off ≤ Nk − 1.
+  int n_t[2], first_masked[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int qt = q0 + t * kBM;
-    n_t[t] = qt >= N ? 0 : (CAUSAL ? qt / kBN + 1 : n_kv);
+    const int last_key = (qt + kBM - 1 < Nq ? qt + kBM - 1 : Nq - 1) + off;
+    n_t[t] = qt >= Nq ? 0 : (CAUSAL ? last_key / kBN + 1 : n_kv);
+    first_masked[t] = (qt + off + 1) / kBN;
   }
   const int J = n_t[0] > n_t[1] ? n_t[0] : n_t[1];
 
@@ -212,6 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
     const int r = (warp & 3) * 32 + lane;                // row within the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int nt = n_t[t];
+    const int fm = first_masked[t];
+    const int qt = q0 + t * kBM;
     const float sl2 = a.scale_log2;
     float m_ref = -INFINITY;   // reference max of the row, base-2 scaled units
     float ell = 0.f;
@@ -223,11 +233,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
       tc_fence_after();
       uint32_t s[128];
       tmem_ld_x128(tmem + lane_off + s_col(t), s);
-      if (CAUSAL && j == nt - 1) {
-        // Diagonal tile: key j·128 + c is visible to query j·128 + r iff c ≤ r.
+      if (CAUSAL && j >= fm) {
+        // A tile crossing the diagonal: key 128j + c is visible to query
+        // qt + r iff c ≤ r + qt + off − 128j (c ≤ r for square problems).
+        const int lim = r + qt + off - j * kBN;
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          if (c > r) s[c] = f2u(-INFINITY);
+          if (c > lim) s[c] = f2u(-INFINITY);
       }
       if (ragged_last && j == nt - 1) {
 #pragma unroll
@@ -265,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
       // Masked tiles take every exponential on MUFU, so masked scores give
       // exactly 0.
       const uint32_t p_addr = tmem + lane_off + s_col(t);
-      if ((CAUSAL || ragged_last) && j == nt - 1)
+      if ((CAUSAL && j >= fm) || (ragged_last && j == nt - 1))
         ell += exp_tile_to_p<0>(s, sl2, m_ref, p_addr);
       else
         ell += exp_tile_to_p<kPolyEvery>(s, sl2, m_ref, p_addr);
@@ -284,8 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
         const float lse = (m_ref + log2f(ell)) * 0.69314718055994530942f;
         if (part_slot < 0) {
           // tcgen05.ld is warp-collective: every lane loads, and only rows
-          // below N (the last tile of a ragged head) are stored.
-          const bool live = !RAGGED || q < N;
+          // below Nq (the last tile of a ragged head) are stored.
+          const bool live = !RAGGED || q < Nq;
           __nv_bfloat16* orow = a.o + ((size_t)row0 + (size_t)q) * D;
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
@@ -333,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
         for (int t = 0; t < 2; ++t)
           if (n_t[t] > 0)
             for (int b = 0; b < D / 64; ++b)
-              load_rows(sbase + L::kQ + t * L::kTile + b * kBoxBytes, &a.tm_q, bar(kQFull), 64 * b, q0 + t * kBM);
+              load_rows(sbase + L::kQ + t * L::kTile + b * kBoxBytes, &a.tm_q, bar(kQFull), 64 * b, q0 + t * kBM, Nq);
       }
       for (int j = 0; j < J; ++j) {
         const int s = j & 1;
@@ -341,13 +353,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
         mbar_arrive_expect_tx(bar(kKFull + s), tile);
         for (int b = 0; b < D / 64; ++b)
           load_rows(sbase + L::kK + s * L::kTile + b * kBoxBytes, &a.tm_k, bar(kKFull + s), 64 * b,
-                    (kv_begin + j) * kBN);
+                    (kv_begin + j) * kBN, Nk);
         ++issued_k[s];
         if (j >= 2 && !mbar_wait(bar(kVEmpty + s), (uint32_t)(((j >> 1) - 1) & 1), wc, site(4))) break;
         mbar_arrive_expect_tx(bar(kVFull + s), tile);
         for (int b = 0; b < D / 64; ++b)
           load_rows(sbase + L::kV + s * L::kTile + b * kBoxBytes, &a.tm_v, bar(kVFull + s), 64 * b,
-                    (kv_begin + j) * kBN);
+                    (kv_begin + j) * kBN, Nk);
         ++issued_v[s];
       }
       // Never leave the CTA with copies in flight: wait for the last load of
@@ -434,7 +446,7 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t s) {
   const size_t smem = FwdLayout<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const long long units = (long long)fwd_units(a.B, a.H, a.N);
+  const long long units = (long long)fwd_units(a.B, a.H, a.Nq);
   const long long ctas = CAUSAL ? units : a.n_full + (units - a.n_full) * a.splits;
   kern<<<(unsigned)ctas, kThreads, smem, s>>>(a);
   e = cudaGetLastError();
@@ -449,18 +461,18 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t s) {
 template <int D>
 __global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restrict__ opart,
                                                           const float* __restrict__ lpart, __nv_bfloat16* __restrict__ o,
-                                                          float* __restrict__ lse, int N, int n_full, int splits,
+                                                          float* __restrict__ lse, int Nq, int n_full, int splits,
                                                           int tail) {
   constexpr int V = D / 32;   // floats per lane
   const int row = (int)(blockIdx.x * 8 + (threadIdx.x >> 5));
   const int lane = threadIdx.x & 31;
   if (row >= tail * 2 * kBM) return;
   const int u = row / (2 * kBM), rr = row % (2 * kBM);
-  const int pairs = (N + 2 * kBM - 1) / (2 * kBM);
+  const int pairs = (Nq + 2 * kBM - 1) / (2 * kBM);
   const int unit = n_full + u;
   const int q = (unit % pairs) * 2 * kBM + rr;
-  if (q >= N) return;
-  const size_t orow = (size_t)(unit / pairs) * N + (size_t)q;
+  if (q >= Nq) return;
+  const size_t orow = (size_t)(unit / pairs) * Nq + (size_t)q;
   float mx = -INFINITY;
   for (int k = 0; k < splits; ++k) mx = fmaxf(mx, lpart[(size_t)(u * splits + k) * 2 * kBM + rr]);
   float sum = 0.f;
@@ -485,14 +497,14 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restric
 template <int D>
 cudaError_t launch_combine(const FwdArgs& a, int tail, cudaStream_t s) {
   const int rows = tail * 2 * kBM;
-  fwd_combine_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a.opart, a.lpart, a.o, a.lse, a.N, a.n_full,
+  fwd_combine_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a.opart, a.lpart, a.o, a.lse, a.Nq, a.n_full,
                                                                    a.splits, tail);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int fwd_units(int B, int H, int N) { return B * H * ((N + 2 * kBM - 1) / (2 * kBM)); }
+int fwd_units(int B, int H, int Nq) { return B * H * ((Nq + 2 * kBM - 1) / (2 * kBM)); }
 
 void fwd_split_plan(int units, int num_sms, int n_kv, int* n_full, int* splits) {
   *n_full = units;
@@ -516,7 +528,7 @@ size_t fwd_bf16_smem_bytes(int d) {
 }
 
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s) {
-  const bool ragged = a.N % kBN != 0;
+  const bool ragged = a.Nq % kBM != 0 || a.Nk % kBN != 0;
   if (a.d == 128) {
     if (ragged) return a.causal ? launch_impl<128, true, true>(a, s) : launch_impl<128, false, true>(a, s);
     return a.causal ? launch_impl<128, true, false>(a, s) : launch_impl<128, false, false>(a, s);

@@ -12,14 +12,18 @@ namespace fa {
 
 // ---------------------------------------------------------------- bf16 tensor-core path
 
+// Q, O, dO, dQ are [B·H, Nq, d]; K, V, dK, dV are [B·H, Nk, d]; LSE [B·H, Nq].
+// Under the causal mask query i sees keys j ≤ i + Nk − Nq (Nq ≤ Nk).
+//
 // Forward: tensor maps over Q, K, V with boxes of 64 columns (128 bytes) ×
-// 128 rows and 128-byte swizzle: 2-D over the [B·H·N, d] row view when N is a
-// multiple of 128, else 3-D over [B·H, N, d] with rows past N read as zero.
+// 128 rows and 128-byte swizzle: 2-D over the [B·H·Nq, d] / [B·H·Nk, d] row
+// views when Nq and Nk are multiples of 128, else 3-D over [B·H, N, d] with
+// rows past N read as zero.
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v;
   __nv_bfloat16* o;
   float* lse;
-  int B, H, N, d;
+  int B, H, Nq, Nk, d;
   float scale_log2;       // scale · log2(e): scores are handled in base 2
   int causal;
   unsigned int* fault;
@@ -32,15 +36,15 @@ struct FwdArgs {
   float* lpart;
 };
 // Two-tile (256-query) work units of the forward.
-int fwd_units(int B, int H, int N);
+int fwd_units(int B, int H, int Nq);
 // Split plan for `units` equal units of `n_kv` K/V tiles on `num_sms` SMs: the
 // units of the last, partial wave are split when that fills the GPU better.
 void fwd_split_plan(int units, int num_sms, int n_kv, int* n_full, int* splits);
 size_t fwd_bf16_smem_bytes(int d);
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s);
 
-// Backward tiled loop.  Tensor maps as in the forward (3-D, 128-row boxes).
-// The workspace arrays hold n_pad = 128·⌈N/128⌉ rows per head.
+// Backward tiled loop.  Tensor maps as in the forward (128-row boxes).
+// The workspace arrays hold n_pad = 128·⌈Nq/128⌉ rows per head.
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
   const float* lse2;      // workspace: −LSE · log2(e), [B·H·n_pad]
@@ -48,7 +52,7 @@ struct BwdArgs {
   float* dqacc;           // workspace: fp32 dQ accumulator, [B·H·n_pad, d]
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  int B, H, N, d;
+  int B, H, Nq, Nk, d;
   float scale_log2;
   float scale;
   int causal;
@@ -58,24 +62,43 @@ int bwd_bf16_block_m(int d);
 size_t bwd_bf16_smem_bytes(int d);
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t s);
 
-// Backward pre-pass: −D = −rowsum(dO ⊙ O) and −LSE·log2(e) per row, dQ
-// accumulator zeroed.  The workspace arrays hold n_pad ≥ N rows per head
+// Backward pre-pass: −D = −rowsum(dO ⊙ O) and −LSE·log2(e) per query row, dQ
+// accumulator zeroed.  The workspace arrays hold n_pad ≥ Nq rows per head
 // (whole 128-row tiles); padding rows get −LSE = −∞ (so P = 0) and D = 0.
 cudaError_t launch_bwd_prep_bf16(const __nv_bfloat16* o, const __nv_bfloat16* dO, const float* lse,
-                                 float* dvec, float* lse2, float* dqacc, long long heads, int N, int n_pad, int d,
+                                 float* dvec, float* lse2, float* dqacc, long long heads, int Nq, int n_pad, int d,
                                  cudaStream_t s);
-// dQ = scale · accumulator (n_pad rows per head), rounded to bf16 [heads, N, d].
-cudaError_t launch_dq_finish_bf16(const float* dqacc, __nv_bfloat16* dq, long long heads, int N, int n_pad, int d,
+// dQ = scale · accumulator (n_pad rows per head), rounded to bf16 [heads, Nq, d].
+cudaError_t launch_dq_finish_bf16(const float* dqacc, __nv_bfloat16* dq, long long heads, int Nq, int n_pad, int d,
                                   float scale, cudaStream_t s);
+
+// ---------------------------------------------------------------- merge of partial results
+
+// O = Σ_k e^{LSE_k − LSE} O_k, LSE = ln Σ_k e^{LSE_k} over n_parts partial
+// results of the same rows ([rows, d] in the dtype, LSE fp32 [rows]).  Rows
+// every part missed (LSE_k = −∞) get O = 0, LSE = −∞.  `o` / `lse` may be one
+// of the parts (each row is read completely before it is written).
+constexpr int kMaxMergeParts = 16;
+struct MergeArgs {
+  const void* o_parts[kMaxMergeParts];
+  const float* lse_parts[kMaxMergeParts];
+  int n_parts;
+  void* o;
+  float* lse;
+  long long rows;
+  int d;
+  int bf16;   // 1: O in bf16, 0: fp32
+};
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
 
 // ---------------------------------------------------------------- fp32 SIMT path
 
-cudaError_t launch_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int BH, int N,
-                           int d, float scale, int causal, cudaStream_t s);
+cudaError_t launch_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int BH, int Nq,
+                           int Nk, int d, float scale, int causal, cudaStream_t s);
 cudaError_t launch_bwd_prep_f32(const float* o, const float* dO, const float* lse, float* dvec, float* lse_copy,
                                 long long rows, int d, cudaStream_t s);
 cudaError_t launch_bwd_f32(const float* q, const float* k, const float* v, const float* dO, const float* lse,
-                           const float* dvec, float* dq, float* dk, float* dv, int BH, int N, int d, float scale,
-                           int causal, cudaStream_t s);
+                           const float* dvec, float* dq, float* dk, float* dv, int BH, int Nq, int Nk, int d,
+                           float scale, int causal, cudaStream_t s);
 
 }  // namespace fa

@@ -99,6 +99,30 @@ def make_inputs(B, H, N, d, dtype="bf16", dist="normal", seed=BASE_SEED, device=
     return tuple(out)
 
 
+def make_inputs_kv(B, H, Nq, Nk, d, dtype="bf16", dist="normal", seed=BASE_SEED, device="cpu"):
+    """Draw q [B, H, Nq, d], k and v [B, H, Nk, d], do [B, H, Nq, d] (in that
+    order, same distributions and rounding as ``make_inputs``)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    qs, ks = (B, H, Nq, d), (B, H, Nk, d)
+    if dist == "normal":
+        q = torch.randn(qs, generator=g, dtype=torch.float32)
+        k = torch.randn(ks, generator=g, dtype=torch.float32)
+        v = torch.randn(ks, generator=g, dtype=torch.float32)
+    elif dist == "stress":
+        q = torch.randn(qs, generator=g, dtype=torch.float32) * 8.0
+        k = torch.randn(ks, generator=g, dtype=torch.float32) * 8.0
+        v = torch.rand(ks, generator=g, dtype=torch.float32) * 2.0 - 1.0
+    else:
+        raise ValueError(f"unknown distribution {dist!r}")
+    do = torch.randn(qs, generator=g, dtype=torch.float32)
+    td = torch_dtype(dtype)
+    out = [t.to(td).contiguous() for t in (q, k, v, do)]
+    if device != "cpu":
+        out = [t.to(device) for t in out]
+    return tuple(out)
+
+
 def make_workload_inputs(w: Workload, device="cpu", heads=None):
     """Inputs of a named workload; ``heads`` optionally overrides H (same seed)."""
     return make_inputs(w.B, w.H if heads is None else heads, w.N, w.d, w.dtype, w.dist, w.seed, device)

@@ -29,7 +29,12 @@
  *               FA_DTYPE_FP32: every tensor is float32 and computed with
  *               fp32 arithmetic (no tensor cores); any N ≥ 1, 1 ≤ d ≤ 128.
  *   causal      0: every key visible.  1: key j visible to query i iff j ≤ i
- *               (square, top-left aligned; no row is ever empty).
+ *               (square, top-left aligned; no row is ever empty).  The _kv
+ *               entry points take Nq queries over Nk keys; there the queries
+ *               are the last Nq positions of the sequence ("Flash Attention"
+ *               tutorial, 2.Online Softmax §七 item 3: later tokens extend a
+ *               cached prefix), so query i sees keys j ≤ i + Nk − Nq, which
+ *               needs Nq ≤ Nk (FA_ERR_UNSUPPORTED otherwise).
  *   scale       finite and > 0; callers usually pass 1/sqrt(d).
  *   Empty       B, H or N equal to 0 is a valid empty problem: FA_OK, nothing
  *               launched, pointers may be NULL.
@@ -75,7 +80,7 @@ typedef enum { FA_DTYPE_BF16 = 0, FA_DTYPE_FP32 = 1 } fa_dtype;
 /* Human-readable name of a status code (static string, never NULL). */
 const char* fa_status_string(fa_status s);
 
-/* Library ABI version (major*100 + minor). */
+/* Library ABI version (major*100 + minor): 110 adds the _kv entry points and fa_merge. */
 int fa_version(void);
 
 /*
@@ -105,6 +110,21 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  fa_stream_t stream);
 
 /*
+ * Nq queries over Nk keys: Q and O are [B,H,Nq,d], K and V [B,H,Nk,d], LSE
+ * [B,H,Nq].  Otherwise as fa_fwd_workspace_size / fa_fwd (which are these with
+ * Nq = Nk = N).  Nq = 0 is an empty problem; Nk = 0 with Nq > 0 (queries with
+ * no key) is FA_ERR_INVALID_ARG.  With causal = 1 the queries are the last Nq
+ * positions (see "causal" above): e.g. a decode step is Nq = 1 over the Nk
+ * cached keys plus itself, and prefix caching runs the new tokens' queries
+ * over all keys.
+ */
+size_t fa_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int causal, fa_dtype dtype);
+fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                    fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                    fa_stream_t stream);
+
+/*
  * Bytes of device workspace fa_bwd needs for this problem (0 for an empty
  * one).  BF16: D and the base-2 LSE (4·B·H·Np bytes each) plus a float32 dQ
  * accumulator (4·B·H·Np·d bytes), Np = 128·⌈N/128⌉ (whole tiles per head),
@@ -130,6 +150,44 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
                  int B, int H, int N, int d, float scale, int causal,
                  fa_dtype dtype, void* workspace, size_t workspace_bytes,
                  fa_stream_t stream);
+
+/*
+ * Backward for Nq queries over Nk keys (layouts as fa_fwd_kv; dq like q, dk
+ * and dv like k).  The workspace depends on Nq only (the same formula as
+ * fa_bwd_workspace_size with N = Nq).  Nq = 0 with Nk > 0 writes dk = dv = 0.
+ */
+size_t fa_bwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, fa_dtype dtype);
+fa_status fa_bwd_kv(const void* q, const void* k, const void* v, const void* o,
+                    const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                    int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                    fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                    fa_stream_t stream);
+
+/* Most partial results one fa_merge call takes. */
+#define FA_MERGE_MAX_PARTS 16
+
+/*
+ * Merge of partial results of the same queries over disjoint key sets
+ * ("Flash Attention" tutorial, 2.Online Softmax §3.1/§4.1, the two-block
+ * merge, in log-sum-exp form; §七 lists its uses: ring attention, streaming
+ * inference / prefix caching).  For every row:
+ *   LSE = ln Σ_k e^{LSE_k},   O = Σ_k e^{LSE_k − LSE} · O_k.
+ * A part whose LSE_k is −∞ saw no key of that row and contributes nothing;
+ * a row no part saw gets O = 0 and LSE = −∞.
+ *   o_parts, lse_parts  HOST arrays of n_parts DEVICE pointers: part k's O
+ *                       [B,H,N,d] in `dtype` and LSE [B,H,N] float32 (as
+ *                       fa_fwd / fa_fwd_kv write them).  1 ≤ n_parts ≤
+ *                       FA_MERGE_MAX_PARTS; the host arrays are read before
+ *                       the call returns.
+ *   o, lse              outputs, same layouts; may be the same buffers as
+ *                       one of the parts (each row is read before it is
+ *                       written), so a running state can be extended in place.
+ *   d                   1 ≤ d ≤ 256 for either dtype.
+ * Errors as the other entry points (null or misaligned pointers, sizes).
+ */
+fa_status fa_merge(const void* const* o_parts, const float* const* lse_parts, int n_parts,
+                   void* o, float* lse, int B, int H, int N, int d, fa_dtype dtype,
+                   fa_stream_t stream);
 
 /*
  * The three stages of fa_bwd, exposed so each can be timed on its own.  They

@@ -29,7 +29,8 @@ def _declared():
 
 def test_header_declares_the_expected_entry_points():
     assert _declared() >= {"fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_status_string", "fa_version",
-                           "fa_bwd_prep", "fa_bwd_tiles", "fa_bwd_dq_finish", "fa_sync_status"}
+                           "fa_bwd_prep", "fa_bwd_tiles", "fa_bwd_dq_finish", "fa_sync_status", "fa_fwd_kv",
+                           "fa_fwd_kv_workspace_size", "fa_bwd_kv", "fa_bwd_kv_workspace_size", "fa_merge"}
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -44,7 +45,7 @@ def test_status_strings(L):
     for code in range(7):
         s = L.fa_status_string(code).decode()
         assert s.startswith("FA_")
-    assert L.fa_version() == 100
+    assert L.fa_version() == 110
 
 
 def test_workspace_size(L):
@@ -94,3 +95,45 @@ def test_backward_argument_checks(L):
     assert L.fa_bwd_tiles(*([FAKE] * 7), 1, 1, 128, 64, 0.125, 0, 0, None, 0, None) == 4
     assert L.fa_bwd_dq_finish(FAKE, 1, 1, 100, 64, 0.125, 0, None, 0, None) == 4
     assert L.fa_bwd_dq_finish(FAKE, 1, 1, 100, 96, 0.125, 0, None, 0, None) == 2
+
+
+def _fwd_kv(L, Nq=128, Nk=256, causal=0, B=1, d=64, dtype=0):
+    return L.fa_fwd_kv(FAKE, FAKE, FAKE, FAKE, FAKE, B, 1, Nq, Nk, d, 0.1, causal, dtype, ctypes.c_void_p(0x10010), 1,
+                       None)
+
+
+def test_kv_argument_checks(L):
+    # shapes pass (a misaligned workspace is then the first error), so 4 means "accepted"
+    assert _fwd_kv(L, 128, 256) == 4 and _fwd_kv(L, 1, 8192, causal=1) == 4 and _fwd_kv(L, 300, 77) == 4
+    assert _fwd_kv(L, 256, 128, causal=1) == 2          # causal with more queries than keys
+    assert _fwd_kv(L, 5, 0) == 1                        # queries with no key
+    assert _fwd_kv(L, 0, 64) == 0 and _fwd_kv(L, 0, 0) == 0 and _fwd_kv(L, 5, 3, B=0) == 0
+    # workspace of the backward depends on Nq only
+    assert L.fa_bwd_kv_workspace_size(2, 1, 200, 4096, 64, 0) == L.fa_bwd_workspace_size(2, 1, 200, 64, 0)
+    assert L.fa_bwd_kv_workspace_size(2, 1, 300, 100, 64, 0) > 0
+    assert L.fa_bwd_kv_workspace_size(2, 1, 5, 0, 64, 0) == 0
+    args = [FAKE] * 9 + [1, 1, 64, 128, 64, 0.125, 1, 0]
+    assert L.fa_bwd_kv(*args, None, 0, None) == 4
+    bad = [FAKE] * 9 + [1, 1, 128, 64, 64, 0.125, 1, 0]
+    assert L.fa_bwd_kv(*bad, None, 0, None) == 2
+    # Nq = 0: dk and dv are zero-filled, so they must be valid pointers
+    none = [FAKE] * 7 + [ctypes.c_void_p(0), FAKE] + [1, 1, 0, 128, 64, 0.125, 0, 0]
+    assert L.fa_bwd_kv(*none, None, 0, None) == 1
+
+
+def test_merge_argument_checks(L):
+    arr = (ctypes.c_void_p * 17)(*([0x10000] * 17))
+    ok_parts = ctypes.cast(arr, ctypes.c_void_p)
+
+    def merge(n=2, o=FAKE, B=1, N=4, d=64, dtype=0, parts=ok_parts, lparts=ok_parts):
+        return L.fa_merge(parts, lparts, n, o, FAKE, B, 1, N, d, dtype, None)
+
+    assert merge(n=0) == 1 and merge(n=17) == 1
+    assert merge(d=300) == 2 and merge(d=0) == 1
+    assert merge(parts=ctypes.c_void_p(0)) == 1
+    assert merge(o=ODD) == 3
+    odd = (ctypes.c_void_p * 2)(0x10000, 0x10008)
+    assert merge(parts=ctypes.cast(odd, ctypes.c_void_p)) == 3
+    assert merge(N=0) == 0 and merge(B=0) == 0
+    null = (ctypes.c_void_p * 2)(0x10000, 0)
+    assert merge(lparts=ctypes.cast(null, ctypes.c_void_p)) == 1

@@ -34,6 +34,6 @@ class _Attention(torch.autograd.Function):
 
 def attention(q, k, v, scale=None, causal=False):
     """softmax(scale · Q Kᵀ) V, differentiable: q [B, H, Nq, d], k and v
-    [B, H, Nk, d] CUDA tensors (bf16 or fp32).  Under ``causal`` the queries
+    [B, H, Nk, d] CUDA tensors (bf16, fp16 or fp32).  Under ``causal`` the queries
     are the last Nq positions (query i sees keys j <= i + Nk - Nq)."""
     return _Attention.apply(q, k, v, scale, causal)

@@ -18,6 +18,8 @@ _LIB = None
 
 FA_DTYPE_BF16 = 0
 FA_DTYPE_FP32 = 1
+FA_DTYPE_FP16 = 2
+_CODES = {torch.bfloat16: FA_DTYPE_BF16, torch.float32: FA_DTYPE_FP32, torch.float16: FA_DTYPE_FP16}
 _STATUS = {
     0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_MISALIGNED",
     4: "FA_ERR_WORKSPACE", 5: "FA_ERR_CUDA", 6: "FA_ERR_TIMEOUT",
@@ -87,11 +89,7 @@ def _check(fn: str, code: int) -> None:
 
 
 def _dtype_code(t: torch.Tensor) -> int:
-    if t.dtype == torch.bfloat16:
-        return FA_DTYPE_BF16
-    if t.dtype == torch.float32:
-        return FA_DTYPE_FP32
-    raise TypeError(f"unsupported dtype {t.dtype}; use torch.bfloat16 or torch.float32")
+    return _code(t.dtype)
 
 
 def _ptr(t):
@@ -126,7 +124,9 @@ def _check_tensors(qside, kside):
 
 
 def _code(dtype) -> int:
-    return FA_DTYPE_BF16 if dtype == torch.bfloat16 else FA_DTYPE_FP32
+    if dtype not in _CODES:
+        raise TypeError(f"unsupported dtype {dtype}; use torch.bfloat16, torch.float16 or torch.float32")
+    return _CODES[dtype]
 
 
 def fwd_workspace_size(B, H, N, d, causal=False, dtype=torch.bfloat16, Nk=None) -> int:

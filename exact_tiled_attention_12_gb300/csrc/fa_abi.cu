@@ -46,27 +46,31 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return f;
 }
 
-// Tensor map over a [B·H, N, d] bf16 tensor with boxes of 64 columns (128
+// Tensor map over a [B·H, N, d] bf16 (or fp16) tensor with boxes of 64 columns (128
 // bytes) × box_rows rows and 128-byte swizzle.  rows_view (every sequence
 // length of the call a multiple of 128): a 2-D map over the [B·H·N, d] row
 // view (a tile never straddles two heads).  Otherwise a 3-D map whose rows
 // past N read as zero, so the last tile of a head never picks up the next
 // head's rows.  The kernels take the matching copy form from the same test.
 bool encode_bf16_heads(CUtensorMap* m, const void* base, long long heads, long long N, int d, int box_rows,
-                       bool rows_view) {
+                       bool rows_view, bool f16) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)(rows_view ? heads * N : N), (cuuint64_t)heads};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * (cuuint64_t)d * 2};
   cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rows_view ? 2 : 3, const_cast<void*>(base), dims, strides,
+  CUresult r = enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rows_view ? 2 : 3, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
 inline size_t pad256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool valid_dtype(fa_dtype t) { return t == FA_DTYPE_BF16 || t == FA_DTYPE_FP32 || t == FA_DTYPE_FP16; }
+// The 16-bit dtypes run on the tensor cores; float32 runs the SIMT kernels.
+bool is16(fa_dtype t) { return t == FA_DTYPE_BF16 || t == FA_DTYPE_FP16; }
 
 // ------------------------------------------------------------------ validation
 
@@ -88,7 +92,7 @@ struct Shape {
 
 fa_status check_shape(int B, int H, int Nq, int Nk, int d, fa_dtype dtype, int causal, Shape* out) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0) return FA_ERR_INVALID_ARG;
-  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP32) return FA_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   Shape s{B, H, Nq, Nk, d};
   if (s.q_elems() > (1ll << 40) || s.k_elems() > (1ll << 40)) return FA_ERR_UNSUPPORTED;
@@ -101,7 +105,7 @@ fa_status check_shape(int B, int H, int Nq, int Nk, int d, fa_dtype dtype, int c
   // than keys would leave rows with no visible key.
   if (causal && Nq > Nk) return FA_ERR_UNSUPPORTED;
   if (s.heads() > 65535) return FA_ERR_UNSUPPORTED;
-  if (dtype == FA_DTYPE_BF16) {
+  if (is16(dtype)) {
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     if (s.rows_pad() >= (1ll << 31) || s.heads() * s.nk_pad() >= (1ll << 31) || s.nk_pad() / 128 > 65535)
       return FA_ERR_UNSUPPORTED;
@@ -122,7 +126,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 fa_status check_ptrs(std::initializer_list<const void*> ptrs, fa_dtype dtype) {
   for (const void* p : ptrs)
     if (p == nullptr) return FA_ERR_INVALID_ARG;
-  if (dtype == FA_DTYPE_BF16)
+  if (is16(dtype))
     for (const void* p : ptrs)
       if (!aligned16(p)) return FA_ERR_MISALIGNED;
   for (const void* p : ptrs)
@@ -180,7 +184,7 @@ struct FwdPlan {
 // Workspace the forward's load balancing needs on the current device (0 when
 // it does not split: causal, fp32, or no partial last wave worth splitting).
 size_t fwd_workspace_bytes(const Shape& s, int causal, fa_dtype dtype, FwdPlan* plan) {
-  if (s.empty() || causal || dtype != FA_DTYPE_BF16) return 0;
+  if (s.empty() || causal || !is16(dtype)) return 0;
   const int units = fa::fwd_units((int)s.B, (int)s.H, (int)s.Nq);
   int n_full, splits;
   fa::fwd_split_plan(units, sm_count_current_device(), (int)(s.nk_pad() / 128), &n_full, &splits);
@@ -193,7 +197,7 @@ size_t fwd_workspace_bytes(const Shape& s, int causal, fa_dtype dtype, FwdPlan* 
 
 constexpr float kLog2e = 1.4426950408889634074f;
 
-size_t elem_bytes(fa_dtype dtype) { return dtype == FA_DTYPE_BF16 ? 2 : 4; }
+size_t elem_bytes(fa_dtype dtype) { return is16(dtype) ? 2 : 4; }
 
 // ------------------------------------------------------------------ implementations (Nq queries, Nk keys)
 
@@ -217,10 +221,13 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
   fa::FwdArgs a;
   const long long heads = s.heads();
   const bool rv = s.rows_view();
-  if (!encode_bf16_heads(&a.tm_q, q, heads, Nq, d, 128, rv) || !encode_bf16_heads(&a.tm_k, k, heads, Nk, d, 128, rv) ||
-      !encode_bf16_heads(&a.tm_v, v, heads, Nk, d, 128, rv))
+  const bool f16 = dtype == FA_DTYPE_FP16;
+  if (!encode_bf16_heads(&a.tm_q, q, heads, Nq, d, 128, rv, f16) ||
+      !encode_bf16_heads(&a.tm_k, k, heads, Nk, d, 128, rv, f16) ||
+      !encode_bf16_heads(&a.tm_v, v, heads, Nk, d, 128, rv, f16))
     return FA_ERR_CUDA;
-  a.o = static_cast<__nv_bfloat16*>(o);
+  a.o = o;
+  a.f16 = f16 ? 1 : 0;
   a.lse = lse;
   a.B = B;
   a.H = H;
@@ -260,9 +267,8 @@ fa_status prep_impl(const void* o, const void* dO, const float* lse, int B, int 
   if (dtype == FA_DTYPE_FP32)
     return from_cuda(fa::launch_bwd_prep_f32(static_cast<const float*>(o), static_cast<const float*>(dO), lse, w.dvec,
                                              w.lse2, s.rows(), d, cs));
-  return from_cuda(fa::launch_bwd_prep_bf16(static_cast<const __nv_bfloat16*>(o),
-                                            static_cast<const __nv_bfloat16*>(dO), lse, w.dvec, w.lse2, w.dqacc,
-                                            s.heads(), Nq, (int)s.nq_pad(), d, cs));
+  return from_cuda(fa::launch_bwd_prep_bf16(o, dO, lse, w.dvec, w.lse2, w.dqacc, s.heads(), Nq, (int)s.nq_pad(), d,
+                                            dtype == FA_DTYPE_FP16 ? 1 : 0, cs));
 }
 
 fa_status tiles_impl(const void* q, const void* k, const void* v, const void* dO, void* dq, void* dk, void* dv, int B,
@@ -289,14 +295,18 @@ fa_status tiles_impl(const void* q, const void* k, const void* v, const void* dO
   const int bm = fa::bwd_bf16_block_m(d);
   const long long heads = s.heads();
   const bool rv = s.rows_view();
-  if (!encode_bf16_heads(&a.tm_q, q, heads, Nq, d, bm, rv) || !encode_bf16_heads(&a.tm_k, k, heads, Nk, d, 128, rv) ||
-      !encode_bf16_heads(&a.tm_v, v, heads, Nk, d, 128, rv) || !encode_bf16_heads(&a.tm_do, dO, heads, Nq, d, bm, rv))
+  const bool f16 = dtype == FA_DTYPE_FP16;
+  if (!encode_bf16_heads(&a.tm_q, q, heads, Nq, d, bm, rv, f16) ||
+      !encode_bf16_heads(&a.tm_k, k, heads, Nk, d, 128, rv, f16) ||
+      !encode_bf16_heads(&a.tm_v, v, heads, Nk, d, 128, rv, f16) ||
+      !encode_bf16_heads(&a.tm_do, dO, heads, Nq, d, bm, rv, f16))
     return FA_ERR_CUDA;
+  a.f16 = f16 ? 1 : 0;
   a.lse2 = w.lse2;
   a.dvec = w.dvec;
   a.dqacc = w.dqacc;
-  a.dk = static_cast<__nv_bfloat16*>(dk);
-  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.dk = dk;
+  a.dv = dv;
   a.B = B;
   a.H = H;
   a.Nq = Nq;
@@ -319,8 +329,8 @@ fa_status finish_impl(void* dq, int B, int H, int Nq, int Nk, int d, float scale
   if ((st = check_ptrs({dq}, dtype)) != FA_OK) return st;
   Workspace w;
   if ((st = carve_workspace(s, dtype, workspace, workspace_bytes, &w)) != FA_OK) return st;
-  return from_cuda(fa::launch_dq_finish_bf16(w.dqacc, static_cast<__nv_bfloat16*>(dq), s.heads(), Nq,
-                                             (int)s.nq_pad(), d, scale, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(fa::launch_dq_finish_bf16(w.dqacc, dq, s.heads(), Nq, (int)s.nq_pad(), d, scale,
+                                             dtype == FA_DTYPE_FP16 ? 1 : 0, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
@@ -436,7 +446,7 @@ static_assert(FA_MERGE_MAX_PARTS == fa::kMaxMergeParts, "merge part limit differ
 fa_status fa_merge(const void* const* o_parts, const float* const* lse_parts, int n_parts, void* o, float* lse,
                    int B, int H, int N, int d, fa_dtype dtype, fa_stream_t stream) {
   if (B < 0 || H < 0 || N < 0 || d <= 0) return FA_ERR_INVALID_ARG;
-  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP32) return FA_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return FA_ERR_INVALID_ARG;
   if (n_parts < 1 || n_parts > FA_MERGE_MAX_PARTS) return FA_ERR_INVALID_ARG;
   if (d > 256) return FA_ERR_UNSUPPORTED;
   const long long rows = (long long)B * H * N;
@@ -460,7 +470,7 @@ fa_status fa_merge(const void* const* o_parts, const float* const* lse_parts, in
   a.lse = lse;
   a.rows = rows;
   a.d = d;
-  a.bf16 = dtype == FA_DTYPE_BF16 ? 1 : 0;
+  a.elem = dtype == FA_DTYPE_BF16 ? 1 : dtype == FA_DTYPE_FP16 ? 2 : 0;
   return from_cuda(fa::launch_merge(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

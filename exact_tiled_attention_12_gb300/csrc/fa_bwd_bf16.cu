@@ -128,7 +128,8 @@ __device__ __forceinline__ bool pair_sync_and(int id, bool ok) {
 // rows past the end read as zero, masking of the keys past Nk and
 // row-predicated dK/dV stores.  Otherwise 2-D maps over the row views and
 // none of that.
-template <int D, bool CAUSAL, bool RAGGED>
+// F16: fp16 inputs and outputs (else bf16); Pᵀ and dSᵀ are rounded to the same type.
+template <int D, bool CAUSAL, bool RAGGED, bool F16>
 // 10 warps: at most 3 per SM sub-partition, so up to 168 registers a thread.
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_constant__ BwdArgs a) {
   using C = BwdCfg<D>;
@@ -260,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         for (int e = 0; e < 16; ++e) {
           float a0, a1;
           f2_unpack(p[half * 16 + e], a0, a1);
-          pk[e] = pack_bf16x2(a0, a1);
+          pk[e] = pack2<F16>(a0, a1);
         }
         tmem_st_x16(tmem + lane_off + C::kColS + (uint32_t)(h * 32 + 16 * half), pk);
       }
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
           const uint64_t ds = f2_mul(p[ch * 16 + e], f2_add(f2_pack(u2f(dp[2 * e]), u2f(dp[2 * e + 1])), ndv[(c0 >> 1) + e]));
           float d0, d1;
           f2_unpack(ds, d0, d1);
-          dk[e] = pack_bf16x2(d0, d1);
+          dk[e] = pack2<F16>(d0, d1);
         }
         // 32 query columns = four 16-byte chunks of this key row, in box h
         // (queries 64h..64h+63), placed with the 128-byte swizzle.
@@ -332,14 +333,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       tc_fence_after();
       const uint32_t col = h == 0 ? C::kColDV : C::kColDK;
       const float mul = h == 0 ? 1.0f : a.scale;
-      __nv_bfloat16* dst = (h == 0 ? a.dv : a.dk) + ((size_t)bh * (size_t)Nk + (size_t)kv) * D;
+      uint16_t* dst = static_cast<uint16_t*>(h == 0 ? a.dv : a.dk) + ((size_t)bh * (size_t)Nk + (size_t)kv) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t v[32];
         tmem_ld_x32(tmem + lane_off + col + 32 * cc, v);   // warp-collective: every lane loads
         uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(v[2 * e]) * mul, u2f(v[2 * e + 1]) * mul);
+        for (int e = 0; e < 16; ++e) pk[e] = pack2<F16>(u2f(v[2 * e]) * mul, u2f(v[2 * e + 1]) * mul);
         if (!dead_key) {
 #pragma unroll
           for (int u = 0; u < 4; ++u)
@@ -380,10 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
   } else {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, kBM, false, false);  // Sᵀ = K Qᵀ, dPᵀ = V dOᵀ
-      constexpr uint32_t kIdKV = idesc_bf16(128, D, false, true);    // dV += Pᵀ dO, dK += dSᵀ Q
+      constexpr uint32_t kIdS = idesc_f16kind(128, kBM, false, false, F16);  // Sᵀ = K Qᵀ, dPᵀ = V dOᵀ
+      constexpr uint32_t kIdKV = idesc_f16kind(128, D, false, true, F16);    // dV += Pᵀ dO, dK += dSᵀ Q
       // d = 128: dQᵀ = Kᵀ dSᵀ (M = head dims, N = 128 queries); d = 64: dQ = dS K (M = queries, N = 64)
-      constexpr uint32_t kIdQ = D == 128 ? idesc_bf16(128, kBM, true, true) : idesc_bf16(128, D, true, true);
+      constexpr uint32_t kIdQ =
+          D == 128 ? idesc_f16kind(128, kBM, true, true, F16) : idesc_f16kind(128, D, true, true, F16);
       auto issue_sd = [&](int i, uint32_t col, uint32_t a_tile) {    // Sᵀ (A = K) or dPᵀ (A = V)
         const int st = i & 1;
         const uint32_t b_tile = (a_tile == sbase + C::kK ? sbase + C::kQ : sbase + C::kDO) + st * C::kTile;
@@ -467,9 +469,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
   }
 }
 
-template <int D, bool CAUSAL, bool RAGGED>
+template <int D, bool CAUSAL, bool RAGGED, bool F16>
 cudaError_t launch_impl(const BwdArgs& a, cudaStream_t s) {
-  auto kern = fa_bwd_bf16_kernel<D, CAUSAL, RAGGED>;
+  auto kern = fa_bwd_bf16_kernel<D, CAUSAL, RAGGED, F16>;
   const size_t smem = BwdCfg<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -483,11 +485,12 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t s) {
 
 // Grid (n_pad·D/8 / 256, heads): one group of D/8 threads per workspace row
 // (n_pad rows per head, a multiple of 128, so every thread has a row); each
-// thread reads 8 bf16 of O and of dO (16 bytes each), so a warp covers 32·8
-// contiguous elements.  Rows past Nq in a head are padding: D = 0, −LSE = −∞.
-template <int D>
-__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
-                                                       const __nv_bfloat16* __restrict__ dO,
+// thread reads 8 16-bit elements of O and of dO (16 bytes each), so a warp
+// covers 32·8 contiguous elements.  Rows past Nq in a head are padding: D = 0,
+// −LSE = −∞.
+template <int D, bool F16>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restrict__ o,
+                                                       const uint16_t* __restrict__ dO,
                                                        const float* __restrict__ lse, float* __restrict__ dvec,
                                                        float* __restrict__ lse2, float* __restrict__ dqacc, int Nq,
                                                        int n_pad) {
@@ -508,12 +511,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   if (live) {
     const uint4 ov = *reinterpret_cast<const uint4*>(o + src * D + part * 8);
     const uint4 gv = *reinterpret_cast<const uint4*>(dO + src * D + part * 8);
-    const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(&ov);
-    const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(&gv);
+    const uint32_t op[4] = {ov.x, ov.y, ov.z, ov.w};
+    const uint32_t gp[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float2 a2 = __bfloat1622float2(op[i]);
-      const float2 b2 = __bfloat1622float2(gp[i]);
+      const float2 a2 = unpack2<F16>(op[i]);
+      const float2 b2 = unpack2<F16>(gp[i]);
       acc = fmaf(a2.x, b2.x, acc);
       acc = fmaf(a2.y, b2.y, acc);
     }
@@ -529,8 +532,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
 
 // Grid (⌈Nq·D/8 / 256⌉, heads): one thread per 8 consecutive dQ elements of a
 // row below Nq; the accumulator has n_pad rows per head, dQ has Nq.
-template <int D>
-__global__ void __launch_bounds__(256) dq_finish_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
+template <int D, bool F16>
+__global__ void __launch_bounds__(256) dq_finish_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq,
                                                         int Nq, int n_pad, float scale) {
   constexpr int G = D / 8;
   const int tid = (int)(blockIdx.x * blockDim.x + threadIdx.x);
@@ -544,10 +547,10 @@ __global__ void __launch_bounds__(256) dq_finish_kernel(const float* __restrict_
   const float4 a0 = a[0];
   const float4 a1 = a[1];
   uint4 out;
-  out.x = pack_bf16x2(a0.x * scale, a0.y * scale);
-  out.y = pack_bf16x2(a0.z * scale, a0.w * scale);
-  out.z = pack_bf16x2(a1.x * scale, a1.y * scale);
-  out.w = pack_bf16x2(a1.z * scale, a1.w * scale);
+  out.x = pack2<F16>(a0.x * scale, a0.y * scale);
+  out.y = pack2<F16>(a0.z * scale, a0.w * scale);
+  out.z = pack2<F16>(a1.x * scale, a1.y * scale);
+  out.w = pack2<F16>(a1.z * scale, a1.w * scale);
   reinterpret_cast<uint4*>(dq)[i] = out;
 }
 
@@ -557,41 +560,61 @@ int bwd_bf16_block_m(int) { return kBM; }
 
 size_t bwd_bf16_smem_bytes(int d) { return d == 64 ? BwdCfg<64>::kBytes : BwdCfg<128>::kBytes; }
 
-cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t s) {
-  const bool ragged = a.Nq % kBM != 0 || a.Nk % kBN != 0;
+template <bool F16>
+static cudaError_t dispatch_bwd(const BwdArgs& a, bool ragged, cudaStream_t s) {
   if (a.d == 128) {
-    if (ragged) return a.causal ? launch_impl<128, true, true>(a, s) : launch_impl<128, false, true>(a, s);
-    return a.causal ? launch_impl<128, true, false>(a, s) : launch_impl<128, false, false>(a, s);
+    if (ragged) return a.causal ? launch_impl<128, true, true, F16>(a, s) : launch_impl<128, false, true, F16>(a, s);
+    return a.causal ? launch_impl<128, true, false, F16>(a, s) : launch_impl<128, false, false, F16>(a, s);
   }
   if (a.d == 64) {
-    if (ragged) return a.causal ? launch_impl<64, true, true>(a, s) : launch_impl<64, false, true>(a, s);
-    return a.causal ? launch_impl<64, true, false>(a, s) : launch_impl<64, false, false>(a, s);
+    if (ragged) return a.causal ? launch_impl<64, true, true, F16>(a, s) : launch_impl<64, false, true, F16>(a, s);
+    return a.causal ? launch_impl<64, true, false, F16>(a, s) : launch_impl<64, false, false, F16>(a, s);
   }
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_bwd_prep_bf16(const __nv_bfloat16* o, const __nv_bfloat16* dO, const float* lse, float* dvec,
-                                 float* lse2, float* dqacc, long long heads, int Nq, int n_pad, int d,
-                                 cudaStream_t s) {
+cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t s) {
+  const bool ragged = a.Nq % kBM != 0 || a.Nk % kBN != 0;
+  return a.f16 ? dispatch_bwd<true>(a, ragged, s) : dispatch_bwd<false>(a, ragged, s);
+}
+
+template <int D, bool F16>
+static void launch_prep(dim3 grid, const void* o, const void* dO, const float* lse, float* dvec, float* lse2,
+                        float* dqacc, int Nq, int n_pad, cudaStream_t s) {
+  bwd_prep_kernel<D, F16><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dO), lse,
+                                               dvec, lse2, dqacc, Nq, n_pad);
+}
+
+cudaError_t launch_bwd_prep_bf16(const void* o, const void* dO, const float* lse, float* dvec, float* lse2,
+                                 float* dqacc, long long heads, int Nq, int n_pad, int d, int f16, cudaStream_t s) {
   if (heads <= 0 || heads > 65535 || n_pad % 128 != 0) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)((long long)n_pad * (d / 8) / 256), (unsigned)heads);
   if (d == 128)
-    bwd_prep_kernel<128><<<grid, 256, 0, s>>>(o, dO, lse, dvec, lse2, dqacc, Nq, n_pad);
+    f16 ? launch_prep<128, true>(grid, o, dO, lse, dvec, lse2, dqacc, Nq, n_pad, s)
+        : launch_prep<128, false>(grid, o, dO, lse, dvec, lse2, dqacc, Nq, n_pad, s);
   else if (d == 64)
-    bwd_prep_kernel<64><<<grid, 256, 0, s>>>(o, dO, lse, dvec, lse2, dqacc, Nq, n_pad);
+    f16 ? launch_prep<64, true>(grid, o, dO, lse, dvec, lse2, dqacc, Nq, n_pad, s)
+        : launch_prep<64, false>(grid, o, dO, lse, dvec, lse2, dqacc, Nq, n_pad, s);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
-cudaError_t launch_dq_finish_bf16(const float* dqacc, __nv_bfloat16* dq, long long heads, int Nq, int n_pad, int d,
-                                  float scale, cudaStream_t s) {
+template <int D, bool F16>
+static void launch_finish(dim3 grid, const float* dqacc, void* dq, int Nq, int n_pad, float scale, cudaStream_t s) {
+  dq_finish_kernel<D, F16><<<grid, 256, 0, s>>>(dqacc, static_cast<uint16_t*>(dq), Nq, n_pad, scale);
+}
+
+cudaError_t launch_dq_finish_bf16(const float* dqacc, void* dq, long long heads, int Nq, int n_pad, int d, float scale,
+                                  int f16, cudaStream_t s) {
   if (heads <= 0 || heads > 65535) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)(((long long)Nq * (d / 8) + 255) / 256), (unsigned)heads);
   if (d == 128)
-    dq_finish_kernel<128><<<grid, 256, 0, s>>>(dqacc, dq, Nq, n_pad, scale);
+    f16 ? launch_finish<128, true>(grid, dqacc, dq, Nq, n_pad, scale, s)
+        : launch_finish<128, false>(grid, dqacc, dq, Nq, n_pad, scale, s);
   else if (d == 64)
-    dq_finish_kernel<64><<<grid, 256, 0, s>>>(dqacc, dq, Nq, n_pad, scale);
+    f16 ? launch_finish<64, true>(grid, dqacc, dq, Nq, n_pad, scale, s)
+        : launch_finish<64, false>(grid, dqacc, dq, Nq, n_pad, scale, s);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

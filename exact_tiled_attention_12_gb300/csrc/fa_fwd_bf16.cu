@@ -74,7 +74,7 @@ __device__ __forceinline__ uint32_t site(int s) { return 0x0100u | (uint32_t)s; 
 // The scale-and-subtract and the sum run as packed f32x2 operations; with
 // POLY_EVERY > 0, one pair of exponentials in POLY_EVERY runs on the FMA pipe
 // (exp2_fma_x2), the others on MUFU.
-template <int POLY_EVERY>
+template <int POLY_EVERY, bool F16>
 __device__ __forceinline__ float exp_tile_to_p(const uint32_t (&s)[128], float sl2, float m_ref, uint32_t p_addr) {
   const uint64_t sl2x2 = f2_pack(sl2, sl2);
   const uint64_t negx2 = f2_pack(-m_ref, -m_ref);
@@ -97,7 +97,7 @@ __device__ __forceinline__ float exp_tile_to_p(const uint32_t (&s)[128], float s
         lsum1 = f2_add(lsum1, f2_pack(e0, e1));
       else
         lsum0 = f2_add(lsum0, f2_pack(e0, e1));
-      p[i] = pack_bf16x2(e0, e1);
+      p[i] = pack2<F16>(e0, e1);
     }
     tmem_st_x16(p_addr + 16 * cc, p);
   }
@@ -111,7 +111,8 @@ __device__ __forceinline__ float exp_tile_to_p(const uint32_t (&s)[128], float s
 // rows past the end read as zero, masking of the missing keys and
 // row-predicated stores.  Otherwise 2-D maps over the row views and none of
 // that code.
-template <int D, bool CAUSAL, bool RAGGED>
+// F16: fp16 inputs and outputs (else bf16); P is rounded to the same type.
+template <int D, bool CAUSAL, bool RAGGED, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_constant__ FwdArgs a) {
   using L = FwdLayout<D>;
   // Dynamic shared memory starts on a 1024-byte boundary (no static shared
@@ -278,9 +279,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
       // exactly 0.
       const uint32_t p_addr = tmem + lane_off + s_col(t);
       if ((CAUSAL && j >= fm) || (ragged_last && j == nt - 1))
-        ell += exp_tile_to_p<0>(s, sl2, m_ref, p_addr);
+        ell += exp_tile_to_p<0, F16>(s, sl2, m_ref, p_addr);
       else
-        ell += exp_tile_to_p<kPolyEvery>(s, sl2, m_ref, p_addr);
+        ell += exp_tile_to_p<kPolyEvery, F16>(s, sl2, m_ref, p_addr);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kPFull + t));
@@ -298,14 +299,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
           // tcgen05.ld is warp-collective: every lane loads, and only rows
           // below Nq (the last tile of a ragged head) are stored.
           const bool live = !RAGGED || q < Nq;
-          __nv_bfloat16* orow = a.o + ((size_t)row0 + (size_t)q) * D;
+          uint16_t* orow = static_cast<uint16_t*>(a.o) + ((size_t)row0 + (size_t)q) * D;
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t o[32];
             tmem_ld_x32(tmem + lane_off + o_col(t) + 32 * cc, o);
             uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
+            for (int i = 0; i < 16; ++i) pk[i] = pack2<F16>(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
             if (live) {
 #pragma unroll
               for (int v4 = 0; v4 < 4; ++v4)
@@ -373,8 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
   } else {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, kBN, false, false);   // S = Q Kᵀ, both K-major
-      constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);      // O += P V, V is MN-major
+      constexpr uint32_t kIdS = idesc_f16kind(128, kBN, false, false, F16);   // S = Q Kᵀ, both K-major
+      constexpr uint32_t kIdO = idesc_f16kind(128, D, false, true, F16);      // O += P V, V is MN-major
       bool ok = J == 0 || mbar_wait(bar(kQFull), 0, wc, site(6));
       int k_ready = -1;
       auto issue_s = [&](int t, int j) -> bool {
@@ -437,12 +438,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
   }
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_combine(const FwdArgs& a, int tail, cudaStream_t s);
 
-template <int D, bool CAUSAL, bool RAGGED>
+template <int D, bool CAUSAL, bool RAGGED, bool F16>
 cudaError_t launch_impl(const FwdArgs& a, cudaStream_t s) {
-  auto kern = fa_fwd_bf16_kernel<D, CAUSAL, RAGGED>;
+  auto kern = fa_fwd_bf16_kernel<D, CAUSAL, RAGGED, F16>;
   const size_t smem = FwdLayout<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -451,16 +452,16 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t s) {
   kern<<<(unsigned)ctas, kThreads, smem, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess || CAUSAL || a.splits <= 1 || a.n_full >= units) return e;
-  return launch_combine<D>(a, (int)(units - a.n_full), s);
+  return launch_combine<D, F16>(a, (int)(units - a.n_full), s);
 }
 
 // Merge of the split partials, "Flash Attention" tutorial, 2.Online Softmax
 // §3.1/§4.1 and §七 (the merge is log-sum-exp): for one query row with
 // partials (O_k, L_k) over disjoint key ranges, L = ln Σ_k e^{L_k} and
 // O = Σ_k e^{L_k − L} O_k.  One warp per row; lanes over the head dims.
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restrict__ opart,
-                                                          const float* __restrict__ lpart, __nv_bfloat16* __restrict__ o,
+                                                          const float* __restrict__ lpart, uint16_t* __restrict__ o,
                                                           float* __restrict__ lse, int Nq, int n_full, int splits,
                                                           int tail) {
   constexpr int V = D / 32;   // floats per lane
@@ -488,16 +489,17 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restric
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[v] = fmaf(w, src[v], acc[v]);
   }
-  __nv_bfloat16* dst = o + orow * D + lane * V;
+  uint16_t* dst = o + orow * D + lane * V;
 #pragma unroll
-  for (int v = 0; v < V; v += 2) reinterpret_cast<uint32_t*>(dst)[v / 2] = pack_bf16x2(acc[v], acc[v + 1]);
+  for (int v = 0; v < V; v += 2) reinterpret_cast<uint32_t*>(dst)[v / 2] = pack2<F16>(acc[v], acc[v + 1]);
   if (lane == 0) lse[orow] = total;
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_combine(const FwdArgs& a, int tail, cudaStream_t s) {
   const int rows = tail * 2 * kBM;
-  fwd_combine_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a.opart, a.lpart, a.o, a.lse, a.Nq, a.n_full,
+  fwd_combine_kernel<D, F16><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a.opart, a.lpart,
+                                                                        static_cast<uint16_t*>(a.o), a.lse, a.Nq, a.n_full,
                                                                    a.splits, tail);
   return cudaGetLastError();
 }
@@ -527,17 +529,23 @@ size_t fwd_bf16_smem_bytes(int d) {
   return d == 64 ? FwdLayout<64>::kBytes : FwdLayout<128>::kBytes;
 }
 
-cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s) {
-  const bool ragged = a.Nq % kBM != 0 || a.Nk % kBN != 0;
+template <bool F16>
+static cudaError_t dispatch_fwd(const FwdArgs& a, bool ragged, cudaStream_t s) {
   if (a.d == 128) {
-    if (ragged) return a.causal ? launch_impl<128, true, true>(a, s) : launch_impl<128, false, true>(a, s);
-    return a.causal ? launch_impl<128, true, false>(a, s) : launch_impl<128, false, false>(a, s);
+    if (ragged) return a.causal ? launch_impl<128, true, true, F16>(a, s) : launch_impl<128, false, true, F16>(a, s);
+    return a.causal ? launch_impl<128, true, false, F16>(a, s) : launch_impl<128, false, false, F16>(a, s);
   }
   if (a.d == 64) {
-    if (ragged) return a.causal ? launch_impl<64, true, true>(a, s) : launch_impl<64, false, true>(a, s);
-    return a.causal ? launch_impl<64, true, false>(a, s) : launch_impl<64, false, false>(a, s);
+    if (ragged) return a.causal ? launch_impl<64, true, true, F16>(a, s) : launch_impl<64, false, true, F16>(a, s);
+    return a.causal ? launch_impl<64, true, false, F16>(a, s) : launch_impl<64, false, false, F16>(a, s);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s) {
+  const bool ragged = a.Nq % kBM != 0 || a.Nk % kBN != 0;
+  if (a.f16) return dispatch_fwd<true>(a, ragged, s);
+  return dispatch_fwd<false>(a, ragged, s);
 }
 
 }  // namespace fa

@@ -19,11 +19,13 @@ namespace fa {
 // 128 rows and 128-byte swizzle: 2-D over the [B·H·Nq, d] / [B·H·Nk, d] row
 // views when Nq and Nk are multiples of 128, else 3-D over [B·H, N, d] with
 // rows past N read as zero.
+// Element type of the 16-bit tensors: bf16, or fp16 when f16 = 1.
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v;
-  __nv_bfloat16* o;
+  void* o;                // [B·H, Nq, d] in the 16-bit type
   float* lse;
   int B, H, Nq, Nk, d;
+  int f16;
   float scale_log2;       // scale · log2(e): scores are handled in base 2
   int causal;
   unsigned int* fault;
@@ -50,9 +52,10 @@ struct BwdArgs {
   const float* lse2;      // workspace: −LSE · log2(e), [B·H·n_pad]
   const float* dvec;      // workspace: −D = −rowsum(dO ⊙ O), [B·H·n_pad]
   float* dqacc;           // workspace: fp32 dQ accumulator, [B·H·n_pad, d]
-  __nv_bfloat16* dk;
-  __nv_bfloat16* dv;
+  void* dk;               // [B·H, Nk, d] in the 16-bit type
+  void* dv;
   int B, H, Nq, Nk, d;
+  int f16;
   float scale_log2;
   float scale;
   int causal;
@@ -65,12 +68,11 @@ cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t s);
 // Backward pre-pass: −D = −rowsum(dO ⊙ O) and −LSE·log2(e) per query row, dQ
 // accumulator zeroed.  The workspace arrays hold n_pad ≥ Nq rows per head
 // (whole 128-row tiles); padding rows get −LSE = −∞ (so P = 0) and D = 0.
-cudaError_t launch_bwd_prep_bf16(const __nv_bfloat16* o, const __nv_bfloat16* dO, const float* lse,
-                                 float* dvec, float* lse2, float* dqacc, long long heads, int Nq, int n_pad, int d,
-                                 cudaStream_t s);
-// dQ = scale · accumulator (n_pad rows per head), rounded to bf16 [heads, Nq, d].
-cudaError_t launch_dq_finish_bf16(const float* dqacc, __nv_bfloat16* dq, long long heads, int Nq, int n_pad, int d,
-                                  float scale, cudaStream_t s);
+cudaError_t launch_bwd_prep_bf16(const void* o, const void* dO, const float* lse, float* dvec, float* lse2,
+                                 float* dqacc, long long heads, int Nq, int n_pad, int d, int f16, cudaStream_t s);
+// dQ = scale · accumulator (n_pad rows per head), rounded to the 16-bit type [heads, Nq, d].
+cudaError_t launch_dq_finish_bf16(const float* dqacc, void* dq, long long heads, int Nq, int n_pad, int d, float scale,
+                                  int f16, cudaStream_t s);
 
 // ---------------------------------------------------------------- merge of partial results
 
@@ -87,7 +89,7 @@ struct MergeArgs {
   float* lse;
   long long rows;
   int d;
-  int bf16;   // 1: O in bf16, 0: fp32
+  int elem;   // O element type: 0 fp32, 1 bf16, 2 fp16
 };
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
 

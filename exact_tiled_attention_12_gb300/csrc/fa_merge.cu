@@ -13,6 +13,8 @@
 // One warp per row: lane k < n_parts holds part k's weight, and the lanes
 // stride over the d columns (coalesced).  HBM-bound: it reads n_parts rows of
 // O and LSE and writes one.
+#include <cuda_fp16.h>
+
 #include "fa_kernels.h"
 
 namespace fa {
@@ -20,23 +22,28 @@ namespace {
 
 constexpr unsigned kFullMask = 0xffffffffu;
 
-template <bool BF16>
+// ELEM: 0 fp32, 1 bf16, 2 fp16.
+template <int ELEM>
 __device__ __forceinline__ float load_o(const void* p, long long i) {
-  if constexpr (BF16)
+  if constexpr (ELEM == 1)
     return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+  else if constexpr (ELEM == 2)
+    return __half2float(static_cast<const __half*>(p)[i]);
   else
     return static_cast<const float*>(p)[i];
 }
 
-template <bool BF16>
+template <int ELEM>
 __device__ __forceinline__ void store_o(void* p, long long i, float x) {
-  if constexpr (BF16)
+  if constexpr (ELEM == 1)
     static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(x);
+  else if constexpr (ELEM == 2)
+    static_cast<__half*>(p)[i] = __float2half_rn(x);
   else
     static_cast<float*>(p)[i] = x;
 }
 
-template <bool BF16>
+template <int ELEM>
 __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ MergeArgs a) {
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -48,7 +55,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
   const long long base = row * (long long)a.d;
   __syncwarp();   // every lane has read its LSE part before anything is written
   if (m == -INFINITY) {   // warp-uniform after the reduction
-    for (int c = lane; c < a.d; c += 32) store_o<BF16>(a.o, base + c, 0.f);
+    for (int c = lane; c < a.d; c += 32) store_o<ELEM>(a.o, base + c, 0.f);
     if (lane == 0) a.lse[row] = -INFINITY;
     return;
   }
@@ -64,9 +71,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
     float acc = 0.f;
     for (int k = 0; k < a.n_parts; ++k) {
       const float wk = __shfl_sync(kFullMask, w, k);
-      if (wk != 0.f && c < a.d) acc = fmaf(wk, load_o<BF16>(a.o_parts[k], base + c), acc);
+      if (wk != 0.f && c < a.d) acc = fmaf(wk, load_o<ELEM>(a.o_parts[k], base + c), acc);
     }
-    if (c < a.d) store_o<BF16>(a.o, base + c, acc);
+    if (c < a.d) store_o<ELEM>(a.o, base + c, acc);
   }
   if (lane == 0) a.lse[row] = m + logf(sum);
 }
@@ -76,10 +83,12 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s) {
   if (a.rows <= 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((a.rows + 7) / 8);
-  if (a.bf16)
-    merge_kernel<true><<<blocks, 256, 0, s>>>(a);
+  if (a.elem == 1)
+    merge_kernel<1><<<blocks, 256, 0, s>>>(a);
+  else if (a.elem == 2)
+    merge_kernel<2><<<blocks, 256, 0, s>>>(a);
   else
-    merge_kernel<false><<<blocks, 256, 0, s>>>(a);
+    merge_kernel<0><<<blocks, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

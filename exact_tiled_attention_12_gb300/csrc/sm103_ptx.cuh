@@ -11,6 +11,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -216,12 +217,16 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
-// Bits: [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B format,
-// 15 A major (1 = MN), 16 B major, [17,23) N>>3, [24,29) M>>4.
+// Instruction descriptor for kind::f16 with 16-bit A/B (both bf16, or both
+// f16: one MMA never mixes them) and fp32 accumulation.
+// Bits: [4,6) D format (1 = f32), [7,10) A format (0 = f16, 1 = bf16),
+// [10,13) B format, 15 A major (1 = MN), 16 B major, [17,23) N>>3, [24,29) M>>4.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, bool a_mn_major, bool b_mn_major, bool f16) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+  return idesc_f16kind(M, N, a_mn_major, b_mn_major, false);
 }
 
 // ------------------------------------------------------------------ arithmetic
@@ -237,6 +242,33 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+// Same for f16x2 (round-to-nearest-even; values past ±65504 become ±inf).
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// The 16-bit element type of the tensor-core path: F16 = fp16, else bf16.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (F16)
+    return pack_f16x2(lo, hi);
+  else
+    return pack_bf16x2(lo, hi);
+}
+// Unpacks a pair of 16-bit elements (low half first) to floats.
+template <bool F16>
+__device__ __forceinline__ float2 unpack2(uint32_t u) {
+  if constexpr (F16) {
+    __half2 h;
+    memcpy(&h, &u, 4);
+    return __half22float2(h);
+  } else {
+    __nv_bfloat162 h;
+    memcpy(&h, &u, 4);
+    return __bfloat1622float2(h);
+  }
 }
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }

@@ -6,7 +6,7 @@ from it without sharing any of the method.
 
 Recipe: a CPU ``torch.Generator`` seeded with ``seed`` draws Q, K, V, dO in
 that order as float32, then each is rounded to the working dtype (bf16 with
-round-to-nearest-even, or kept fp32).  Both sides read the same rounded bits;
+round-to-nearest-even, fp16 likewise, or kept fp32).  Both sides read the same rounded bits;
 bf16 -> fp64 is exact, so the oracle sees exactly what the kernels see.
 
 Distributions:
@@ -73,7 +73,7 @@ WORKLOADS = {
 
 
 def torch_dtype(name: str) -> torch.dtype:
-    return {"bf16": torch.bfloat16, "fp32": torch.float32}[name]
+    return {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[name]
 
 
 def make_inputs(B, H, N, d, dtype="bf16", dist="normal", seed=BASE_SEED, device="cpu"):

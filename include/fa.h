@@ -26,6 +26,8 @@
  *               any N ≥ 1 (tiles of 128 rows; a ragged last tile reads zero
  *               rows past N and masks those keys), base pointers 16-byte
  *               aligned.
+ *               FA_DTYPE_FP16: the same with IEEE half precision (P and dS
+ *               rounded to fp16; outputs that pass ±65504 become ±inf).
  *               FA_DTYPE_FP32: every tensor is float32 and computed with
  *               fp32 arithmetic (no tensor cores); any N ≥ 1, 1 ≤ d ≤ 128.
  *   causal      0: every key visible.  1: key j visible to query i iff j ≤ i
@@ -69,18 +71,19 @@ typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad scale/causal/dtype */
   FA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (bf16 d∉{64,128}, fp32 d>128, sizes past the grid limits) */
-  FA_ERR_MISALIGNED = 3,   /* bf16 base pointer not 16-byte aligned */
+  FA_ERR_MISALIGNED = 3,   /* bf16/fp16 base pointer not 16-byte aligned */
   FA_ERR_WORKSPACE = 4,    /* workspace NULL, misaligned (256 B) or too small */
   FA_ERR_CUDA = 5,         /* a CUDA runtime/driver call or launch failed */
   FA_ERR_TIMEOUT = 6       /* a kernel abandoned a pipeline wait (see fa_sync_status) */
 } fa_status;
 
-typedef enum { FA_DTYPE_BF16 = 0, FA_DTYPE_FP32 = 1 } fa_dtype;
+typedef enum { FA_DTYPE_BF16 = 0, FA_DTYPE_FP32 = 1, FA_DTYPE_FP16 = 2 } fa_dtype;
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* fa_status_string(fa_status s);
 
-/* Library ABI version (major*100 + minor): 110 adds the _kv entry points and fa_merge. */
+/* Library ABI version (major*100 + minor): 110 adds the _kv entry points,
+ * fa_merge and FA_DTYPE_FP16. */
 int fa_version(void);
 
 /*

@@ -74,7 +74,8 @@ def _fwd(L, ptr=FAKE, B=1, H=1, N=128, d=128, scale=0.1, causal=0, dtype=0, ws=N
     (dict(d=96), 2), (dict(d=256, dtype=1), 2), (dict(B=300, H=300), 2), (dict(N=65535 * 128 + 1), 2),
     (dict(ptr=ODD), 3),
     (dict(ws=ctypes.c_void_p(0x10010)), 4),
-    (dict(N=0), 0), (dict(B=0, ptr=ctypes.c_void_p(0)), 0),
+    (dict(N=0), 0), (dict(B=0, ptr=ctypes.c_void_p(0)), 0), (dict(dtype=2, ws=ctypes.c_void_p(0x10010)), 4),
+    (dict(dtype=2, ptr=ODD), 3), (dict(dtype=2, d=96), 2), (dict(dtype=3), 1),
     (dict(N=200, ws=ctypes.c_void_p(0x10010)), 4),   # ragged N passes the shape check
 ])
 def test_forward_argument_checks(L, kwargs, code):

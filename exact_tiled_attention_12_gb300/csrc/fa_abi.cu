@@ -183,7 +183,12 @@ struct FwdPlan {
 
 // Workspace the forward's load balancing needs on the current device (0 when
 // it does not split: causal, fp32, or no partial last wave worth splitting).
+// One query (a decoding step) sees every key under the causal mask, so it
+// runs as the unmasked problem, which may split its keys over several CTAs.
+int forward_causal(int causal, const Shape& s) { return causal && s.Nq > 1 ? 1 : 0; }
+
 size_t fwd_workspace_bytes(const Shape& s, int causal, fa_dtype dtype, FwdPlan* plan) {
+  causal = forward_causal(causal, s);
   if (s.empty() || causal || !is16(dtype)) return 0;
   const int units = fa::fwd_units((int)s.B, (int)s.H, (int)s.Nq);
   int n_full, splits;
@@ -209,6 +214,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
   if (st != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (s.empty()) return FA_OK;
+  causal = forward_causal(causal, s);
   if ((st = check_ptrs({q, k, v, o, lse}, dtype)) != FA_OK) return st;
   if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_WORKSPACE;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);

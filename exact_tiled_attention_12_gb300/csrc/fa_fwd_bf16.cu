@@ -515,7 +515,11 @@ void fwd_split_plan(int units, int num_sms, int n_kv, int* n_full, int* splits) 
   const int tail = units % num_sms;
   if (tail == 0) return;
   int s = num_sms / tail;         // CTAs per tail unit that still fit in one wave
-  if (s > 4) s = 4;
+  // Up to 4 parts for the last wave of a multi-wave grid; when every unit
+  // fits in one partial wave (few heads, long K/V: decoding), up to 16, so
+  // that the K/V reads spread over more SMs.
+  const int cap = units < num_sms ? 16 : 4;
+  if (s > cap) s = cap;
   // Each part must keep at least 8 K/V tiles: shorter parts cost more in
   // per-CTA start-up, fp32 partial writes and the merge than they save
   // (measured on GB300 with 8 tiles per unit split in two).

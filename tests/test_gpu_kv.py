@@ -50,6 +50,7 @@ KV_SHAPES = [
     (1, 1, 77, 589, 64),     # offset 512 with a 77-row query tile
     (1, 2, 1, 4096, 128),    # one query over 4096 keys (a decode step)
     (2, 2, 130, 430, 128),   # offset 300, two query tiles, the second with 2 rows
+    (1, 2, 1, 32768, 128),   # one query over 32768 keys: the keys split over 16 CTAs
 ]
 
 

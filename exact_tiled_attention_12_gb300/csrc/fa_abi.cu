@@ -106,7 +106,7 @@ fa_status check_shape(int B, int H, int Nq, int Nk, int d, fa_dtype dtype, int c
   if (causal && Nq > Nk) return FA_ERR_UNSUPPORTED;
   if (s.heads() > 65535) return FA_ERR_UNSUPPORTED;
   if (is16(dtype)) {
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
     if (s.rows_pad() >= (1ll << 31) || s.heads() * s.nk_pad() >= (1ll << 31) || s.nk_pad() / 128 > 65535)
       return FA_ERR_UNSUPPORTED;
   } else {

@@ -129,9 +129,15 @@ __device__ __forceinline__ bool pair_sync_and(int id, bool ok) {
 // row-predicated dK/dV stores.  Otherwise 2-D maps over the row views and
 // none of that.
 // F16: fp16 inputs and outputs (else bf16); Pᵀ and dSᵀ are rounded to the same type.
-template <int D, bool CAUSAL, bool RAGGED, bool F16>
+// DR: the head dimension (64, 96 or 128).  Tiles are laid out D = 64 or 128
+// columns wide; with DR = 96 the tensor maps read columns 96..127 as zeros,
+// the products run over the 96 real columns (6 K-steps for Sᵀ and dPᵀ,
+// N = 96 for dV and dK; dQᵀ keeps M = 128 with zero rows past 96) and only
+// 96 columns are reduced or stored.
+template <int DR, bool CAUSAL, bool RAGGED, bool F16>
 // 10 warps: at most 3 per SM sub-partition, so up to 168 registers a thread.
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_constant__ BwdArgs a) {
+  constexpr int D = DR <= 64 ? 64 : 128;
   using C = BwdCfg<D>;
   // Dynamic shared memory starts on a 1024-byte boundary (no static shared
   // memory is declared); 128-byte swizzled tiles need that alignment.
@@ -305,13 +311,19 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       if constexpr (D == 128) {
         // dQᵀ: lane = head dim, columns = queries [64h, 64h + 64); a warp's
         // reduction covers 32 consecutive floats of one accumulator row.
-        uint32_t v[64];
-        tmem_ld_x64(tmem + lane_off + C::kColDP + (uint32_t)(64 * h), v);
-        tc_fence_before();
-        mbar_arrive(bar(kDqDrained));
-        float* base = a.dqacc + ((size_t)wrow0 + (size_t)q0 + (size_t)(64 * h)) * D + (size_t)r;
+        // Warps whose head dims are all past DR only release the columns.
+        if (g * 32 < DR) {
+          uint32_t v[64];
+          tmem_ld_x64(tmem + lane_off + C::kColDP + (uint32_t)(64 * h), v);
+          tc_fence_before();
+          mbar_arrive(bar(kDqDrained));
+          float* base = a.dqacc + ((size_t)wrow0 + (size_t)q0 + (size_t)(64 * h)) * DR + (size_t)r;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) red_add_f32(base + (size_t)c * D, u2f(v[c]));
+          for (int c = 0; c < 64; ++c) red_add_f32(base + (size_t)c * DR, u2f(v[c]));
+        } else {
+          tc_fence_before();
+          mbar_arrive(bar(kDqDrained));
+        }
       } else {
         // dQ: lane = query row, columns = head dims [32h, 32h + 32); 16-byte
         // vector reductions along the row.
@@ -333,9 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       tc_fence_after();
       const uint32_t col = h == 0 ? C::kColDV : C::kColDK;
       const float mul = h == 0 ? 1.0f : a.scale;
-      uint16_t* dst = static_cast<uint16_t*>(h == 0 ? a.dv : a.dk) + ((size_t)bh * (size_t)Nk + (size_t)kv) * D;
+      uint16_t* dst = static_cast<uint16_t*>(h == 0 ? a.dv : a.dk) + ((size_t)bh * (size_t)Nk + (size_t)kv) * DR;
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < DR / 32; ++cc) {
         uint32_t v[32];
         tmem_ld_x32(tmem + lane_off + col + 32 * cc, v);   // warp-collective: every lane loads
         uint32_t pk[16];
@@ -382,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16kind(128, kBM, false, false, F16);  // Sᵀ = K Qᵀ, dPᵀ = V dOᵀ
-      constexpr uint32_t kIdKV = idesc_f16kind(128, D, false, true, F16);    // dV += Pᵀ dO, dK += dSᵀ Q
+      constexpr uint32_t kIdKV = idesc_f16kind(128, DR, false, true, F16);   // dV += Pᵀ dO, dK += dSᵀ Q
       // d = 128: dQᵀ = Kᵀ dSᵀ (M = head dims, N = 128 queries); d = 64: dQ = dS K (M = queries, N = 64)
       constexpr uint32_t kIdQ =
           D == 128 ? idesc_f16kind(128, kBM, true, true, F16) : idesc_f16kind(128, D, true, true, F16);
@@ -390,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         const int st = i & 1;
         const uint32_t b_tile = (a_tile == sbase + C::kK ? sbase + C::kQ : sbase + C::kDO) + st * C::kTile;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
+        for (int ks = 0; ks < DR / 16; ++ks) {
           const uint32_t off = (uint32_t)((ks >> 2) * kBox + (ks & 3) * 32);
           mma_ss(tmem + col, sdesc_sw128(a_tile + off, 16, 1024), sdesc_sw128(b_tile + off, 16, 1024), kIdS,
                  ks > 0 ? 1u : 0u);
@@ -469,10 +481,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
   }
 }
 
-template <int D, bool CAUSAL, bool RAGGED, bool F16>
+template <int DR, bool CAUSAL, bool RAGGED, bool F16>
 cudaError_t launch_impl(const BwdArgs& a, cudaStream_t s) {
-  auto kern = fa_bwd_bf16_kernel<D, CAUSAL, RAGGED, F16>;
-  const size_t smem = BwdCfg<D>::kBytes;
+  auto kern = fa_bwd_bf16_kernel<DR, CAUSAL, RAGGED, F16>;
+  const size_t smem = BwdCfg<(DR <= 64 ? 64 : 128)>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const unsigned tiles = (unsigned)((a.Nk + kBN - 1) / kBN), heads = (unsigned)(a.B * a.H);
@@ -488,29 +500,32 @@ cudaError_t launch_impl(const BwdArgs& a, cudaStream_t s) {
 // thread reads 8 16-bit elements of O and of dO (16 bytes each), so a warp
 // covers 32·8 contiguous elements.  Rows past Nq in a head are padding: D = 0,
 // −LSE = −∞.
-template <int D, bool F16>
+// DR = 96: groups of 16 threads (a power of two, for the shuffle sum) of
+// which the last 4 hold no columns.
+template <int DR, bool F16>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restrict__ o,
                                                        const uint16_t* __restrict__ dO,
                                                        const float* __restrict__ lse, float* __restrict__ dvec,
                                                        float* __restrict__ lse2, float* __restrict__ dqacc, int Nq,
                                                        int n_pad) {
-  constexpr int G = D / 8;   // threads per row
+  constexpr int G = DR == 96 ? 16 : DR / 8;   // threads per row
   const int tid = (int)(blockIdx.x * blockDim.x + threadIdx.x);
   const int pos = tid / G;                  // row within the head
   const int part = tid % G;
+  const bool has_cols = part * 8 < DR;
   const long long head = blockIdx.y;
   const long long row = head * n_pad + pos;   // workspace row
   const long long src = head * Nq + pos;       // row of O, dO and LSE
   const bool live = pos < Nq;
   float acc = 0.f;
-  {
-    float4* z = reinterpret_cast<float4*>(dqacc + row * D + part * 8);
+  if (has_cols) {
+    float4* z = reinterpret_cast<float4*>(dqacc + row * DR + part * 8);
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  if (live) {
-    const uint4 ov = *reinterpret_cast<const uint4*>(o + src * D + part * 8);
-    const uint4 gv = *reinterpret_cast<const uint4*>(dO + src * D + part * 8);
+  if (live && has_cols) {
+    const uint4 ov = *reinterpret_cast<const uint4*>(o + src * DR + part * 8);
+    const uint4 gv = *reinterpret_cast<const uint4*>(dO + src * DR + part * 8);
     const uint32_t op[4] = {ov.x, ov.y, ov.z, ov.w};
     const uint32_t gp[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
@@ -532,10 +547,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
 
 // Grid (⌈Nq·D/8 / 256⌉, heads): one thread per 8 consecutive dQ elements of a
 // row below Nq; the accumulator has n_pad rows per head, dQ has Nq.
-template <int D, bool F16>
+template <int DR, bool F16>
 __global__ void __launch_bounds__(256) dq_finish_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq,
                                                         int Nq, int n_pad, float scale) {
-  constexpr int G = D / 8;
+  constexpr int G = DR / 8;
   const int tid = (int)(blockIdx.x * blockDim.x + threadIdx.x);
   const int pos = tid / G;
   if (pos >= Nq) return;
@@ -543,7 +558,7 @@ __global__ void __launch_bounds__(256) dq_finish_kernel(const float* __restrict_
   const long long head = blockIdx.y;
   const long long arow = head * n_pad + pos;
   const long long i = (head * Nq + pos) * G + part;   // 16-byte chunk of dQ
-  const float4* a = reinterpret_cast<const float4*>(acc + arow * D + part * 8);
+  const float4* a = reinterpret_cast<const float4*>(acc + arow * DR + part * 8);
   const float4 a0 = a[0];
   const float4 a1 = a[1];
   uint4 out;
@@ -558,13 +573,17 @@ __global__ void __launch_bounds__(256) dq_finish_kernel(const float* __restrict_
 
 int bwd_bf16_block_m(int) { return kBM; }
 
-size_t bwd_bf16_smem_bytes(int d) { return d == 64 ? BwdCfg<64>::kBytes : BwdCfg<128>::kBytes; }
+size_t bwd_bf16_smem_bytes(int d) { return d <= 64 ? BwdCfg<64>::kBytes : BwdCfg<128>::kBytes; }
 
 template <bool F16>
 static cudaError_t dispatch_bwd(const BwdArgs& a, bool ragged, cudaStream_t s) {
   if (a.d == 128) {
     if (ragged) return a.causal ? launch_impl<128, true, true, F16>(a, s) : launch_impl<128, false, true, F16>(a, s);
     return a.causal ? launch_impl<128, true, false, F16>(a, s) : launch_impl<128, false, false, F16>(a, s);
+  }
+  if (a.d == 96) {
+    if (ragged) return a.causal ? launch_impl<96, true, true, F16>(a, s) : launch_impl<96, false, true, F16>(a, s);
+    return a.causal ? launch_impl<96, true, false, F16>(a, s) : launch_impl<96, false, false, F16>(a, s);
   }
   if (a.d == 64) {
     if (ragged) return a.causal ? launch_impl<64, true, true, F16>(a, s) : launch_impl<64, false, true, F16>(a, s);
@@ -588,10 +607,14 @@ static void launch_prep(dim3 grid, const void* o, const void* dO, const float* l
 cudaError_t launch_bwd_prep_bf16(const void* o, const void* dO, const float* lse, float* dvec, float* lse2,
                                  float* dqacc, long long heads, int Nq, int n_pad, int d, int f16, cudaStream_t s) {
   if (heads <= 0 || heads > 65535 || n_pad % 128 != 0) return cudaErrorInvalidValue;
-  const dim3 grid((unsigned)((long long)n_pad * (d / 8) / 256), (unsigned)heads);
+  const int threads_per_row = d == 96 ? 16 : d / 8;
+  const dim3 grid((unsigned)((long long)n_pad * threads_per_row / 256), (unsigned)heads);
   if (d == 128)
     f16 ? launch_prep<128, true>(grid, o, dO, lse, dvec, lse2, dqacc, Nq, n_pad, s)
         : launch_prep<128, false>(grid, o, dO, lse, dvec, lse2, dqacc, Nq, n_pad, s);
+  else if (d == 96)
+    f16 ? launch_prep<96, true>(grid, o, dO, lse, dvec, lse2, dqacc, Nq, n_pad, s)
+        : launch_prep<96, false>(grid, o, dO, lse, dvec, lse2, dqacc, Nq, n_pad, s);
   else if (d == 64)
     f16 ? launch_prep<64, true>(grid, o, dO, lse, dvec, lse2, dqacc, Nq, n_pad, s)
         : launch_prep<64, false>(grid, o, dO, lse, dvec, lse2, dqacc, Nq, n_pad, s);
@@ -612,6 +635,9 @@ cudaError_t launch_dq_finish_bf16(const float* dqacc, void* dq, long long heads,
   if (d == 128)
     f16 ? launch_finish<128, true>(grid, dqacc, dq, Nq, n_pad, scale, s)
         : launch_finish<128, false>(grid, dqacc, dq, Nq, n_pad, scale, s);
+  else if (d == 96)
+    f16 ? launch_finish<96, true>(grid, dqacc, dq, Nq, n_pad, scale, s)
+        : launch_finish<96, false>(grid, dqacc, dq, Nq, n_pad, scale, s);
   else if (d == 64)
     f16 ? launch_finish<64, true>(grid, dqacc, dq, Nq, n_pad, scale, s)
         : launch_finish<64, false>(grid, dqacc, dq, Nq, n_pad, scale, s);

@@ -112,8 +112,13 @@ __device__ __forceinline__ float exp_tile_to_p(const uint32_t (&s)[128], float s
 // row-predicated stores.  Otherwise 2-D maps over the row views and none of
 // that code.
 // F16: fp16 inputs and outputs (else bf16); P is rounded to the same type.
-template <int D, bool CAUSAL, bool RAGGED, bool F16>
+// DR: the head dimension (64, 96 or 128).  Tiles are laid out D = 64 or 128
+// columns wide; with DR = 96 the tensor maps read columns 96..127 as zeros,
+// the products run over the 96 real columns only (6 K-steps of 16 for S, an
+// N = 96 product for O) and 96 columns are stored.
+template <int DR, bool CAUSAL, bool RAGGED, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_constant__ FwdArgs a) {
+  constexpr int D = DR <= 64 ? 64 : 128;
   using L = FwdLayout<D>;
   // Dynamic shared memory starts on a 1024-byte boundary (no static shared
   // memory is declared); 128-byte swizzled tiles need that alignment.
@@ -265,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
         // whose commit we just waited on) and the next product into O_t waits
         // for P_full, so this row of O_t is ours to rescale.
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < DR / 32; ++cc) {
           uint32_t o[32];
           tmem_ld_x32(tmem + lane_off + o_col(t) + 32 * cc, o);
 #pragma unroll
@@ -299,9 +304,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
           // tcgen05.ld is warp-collective: every lane loads, and only rows
           // below Nq (the last tile of a ragged head) are stored.
           const bool live = !RAGGED || q < Nq;
-          uint16_t* orow = static_cast<uint16_t*>(a.o) + ((size_t)row0 + (size_t)q) * D;
+          uint16_t* orow = static_cast<uint16_t*>(a.o) + ((size_t)row0 + (size_t)q) * DR;
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
+          for (int cc = 0; cc < DR / 32; ++cc) {
             uint32_t o[32];
             tmem_ld_x32(tmem + lane_off + o_col(t) + 32 * cc, o);
             uint32_t pk[16];
@@ -317,9 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
         } else {
           // Partial over this CTA's keys: normalised O and LSE in fp32.
           const size_t prow = (size_t)part_slot * (2 * kBM) + (size_t)(t * kBM + r);
-          float* orow = a.opart + prow * D;
+          float* orow = a.opart + prow * DR;
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
+          for (int cc = 0; cc < DR / 32; ++cc) {
             uint32_t o[32];
             tmem_ld_x32(tmem + lane_off + o_col(t) + 32 * cc, o);
 #pragma unroll
@@ -375,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16kind(128, kBN, false, false, F16);   // S = Q Kᵀ, both K-major
-      constexpr uint32_t kIdO = idesc_f16kind(128, D, false, true, F16);      // O += P V, V is MN-major
+      constexpr uint32_t kIdO = idesc_f16kind(128, DR, false, true, F16);     // O += P V, V is MN-major
       bool ok = J == 0 || mbar_wait(bar(kQFull), 0, wc, site(6));
       int k_ready = -1;
       auto issue_s = [&](int t, int j) -> bool {
@@ -387,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
         const uint32_t qa = sbase + L::kQ + t * L::kTile;
         const uint32_t kb = sbase + L::kK + (j & 1) * L::kTile;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
+        for (int ks = 0; ks < DR / 16; ++ks) {
           const uint32_t off = (uint32_t)((ks >> 2) * kBoxBytes + (ks & 3) * 32);
           mma_ss(tmem + s_col(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdS,
                  ks > 0 ? 1u : 0u);
@@ -438,13 +443,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
   }
 }
 
-template <int D, bool F16>
+template <int DR, bool F16>
 cudaError_t launch_combine(const FwdArgs& a, int tail, cudaStream_t s);
 
-template <int D, bool CAUSAL, bool RAGGED, bool F16>
+template <int DR, bool CAUSAL, bool RAGGED, bool F16>
 cudaError_t launch_impl(const FwdArgs& a, cudaStream_t s) {
-  auto kern = fa_fwd_bf16_kernel<D, CAUSAL, RAGGED, F16>;
-  const size_t smem = FwdLayout<D>::kBytes;
+  auto kern = fa_fwd_bf16_kernel<DR, CAUSAL, RAGGED, F16>;
+  const size_t smem = FwdLayout<(DR <= 64 ? 64 : 128)>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long long units = (long long)fwd_units(a.B, a.H, a.Nq);
@@ -452,19 +457,19 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t s) {
   kern<<<(unsigned)ctas, kThreads, smem, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess || CAUSAL || a.splits <= 1 || a.n_full >= units) return e;
-  return launch_combine<D, F16>(a, (int)(units - a.n_full), s);
+  return launch_combine<DR, F16>(a, (int)(units - a.n_full), s);
 }
 
 // Merge of the split partials, "Flash Attention" tutorial, 2.Online Softmax
 // §3.1/§4.1 and §七 (the merge is log-sum-exp): for one query row with
 // partials (O_k, L_k) over disjoint key ranges, L = ln Σ_k e^{L_k} and
 // O = Σ_k e^{L_k − L} O_k.  One warp per row; lanes over the head dims.
-template <int D, bool F16>
+template <int DR, bool F16>
 __global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restrict__ opart,
                                                           const float* __restrict__ lpart, uint16_t* __restrict__ o,
                                                           float* __restrict__ lse, int Nq, int n_full, int splits,
                                                           int tail) {
-  constexpr int V = D / 32;   // floats per lane
+  constexpr int V = DR / 32;   // consecutive head dims per lane
   const int row = (int)(blockIdx.x * 8 + (threadIdx.x >> 5));
   const int lane = threadIdx.x & 31;
   if (row >= tail * 2 * kBM) return;
@@ -485,20 +490,25 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restric
   for (int k = 0; k < splits; ++k) {
     const size_t pr = (size_t)(u * splits + k) * 2 * kBM + rr;
     const float w = expf(lpart[pr] - total);
-    const float* src = opart + pr * D + lane * V;
+    const float* src = opart + pr * DR + lane * V;
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[v] = fmaf(w, src[v], acc[v]);
   }
-  uint16_t* dst = o + orow * D + lane * V;
+  uint16_t* dst = o + orow * DR + lane * V;
+  if constexpr (V % 2 == 0) {
 #pragma unroll
-  for (int v = 0; v < V; v += 2) reinterpret_cast<uint32_t*>(dst)[v / 2] = pack2<F16>(acc[v], acc[v + 1]);
+    for (int v = 0; v < V; v += 2) reinterpret_cast<uint32_t*>(dst)[v / 2] = pack2<F16>(acc[v], acc[v + 1]);
+  } else {   // an odd count per lane (DR = 96): 16-bit stores
+#pragma unroll
+    for (int v = 0; v < V; ++v) dst[v] = (uint16_t)(pack2<F16>(acc[v], 0.f) & 0xFFFFu);
+  }
   if (lane == 0) lse[orow] = total;
 }
 
-template <int D, bool F16>
+template <int DR, bool F16>
 cudaError_t launch_combine(const FwdArgs& a, int tail, cudaStream_t s) {
   const int rows = tail * 2 * kBM;
-  fwd_combine_kernel<D, F16><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a.opart, a.lpart,
+  fwd_combine_kernel<DR, F16><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a.opart, a.lpart,
                                                                         static_cast<uint16_t*>(a.o), a.lse, a.Nq, a.n_full,
                                                                    a.splits, tail);
   return cudaGetLastError();
@@ -530,7 +540,7 @@ void fwd_split_plan(int units, int num_sms, int n_kv, int* n_full, int* splits) 
 }
 
 size_t fwd_bf16_smem_bytes(int d) {
-  return d == 64 ? FwdLayout<64>::kBytes : FwdLayout<128>::kBytes;
+  return d <= 64 ? FwdLayout<64>::kBytes : FwdLayout<128>::kBytes;
 }
 
 template <bool F16>
@@ -538,6 +548,10 @@ static cudaError_t dispatch_fwd(const FwdArgs& a, bool ragged, cudaStream_t s) {
   if (a.d == 128) {
     if (ragged) return a.causal ? launch_impl<128, true, true, F16>(a, s) : launch_impl<128, false, true, F16>(a, s);
     return a.causal ? launch_impl<128, true, false, F16>(a, s) : launch_impl<128, false, false, F16>(a, s);
+  }
+  if (a.d == 96) {
+    if (ragged) return a.causal ? launch_impl<96, true, true, F16>(a, s) : launch_impl<96, false, true, F16>(a, s);
+    return a.causal ? launch_impl<96, true, false, F16>(a, s) : launch_impl<96, false, false, F16>(a, s);
   }
   if (a.d == 64) {
     if (ragged) return a.causal ? launch_impl<64, true, true, F16>(a, s) : launch_impl<64, false, true, F16>(a, s);

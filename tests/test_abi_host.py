@@ -71,11 +71,11 @@ def _fwd(L, ptr=FAKE, B=1, H=1, N=128, d=128, scale=0.1, causal=0, dtype=0, ws=N
     (dict(B=-1), 1), (dict(N=-5), 1), (dict(d=0), 1), (dict(scale=0.0), 1), (dict(scale=-1.0), 1),
     (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1), (dict(causal=2), 1), (dict(dtype=7), 1),
     (dict(ptr=ctypes.c_void_p(0)), 1),
-    (dict(d=96), 2), (dict(d=256, dtype=1), 2), (dict(B=300, H=300), 2), (dict(N=65535 * 128 + 1), 2),
+    (dict(d=80), 2), (dict(d=256, dtype=1), 2), (dict(d=96, ws=ctypes.c_void_p(0x10010)), 4), (dict(B=300, H=300), 2), (dict(N=65535 * 128 + 1), 2),
     (dict(ptr=ODD), 3),
     (dict(ws=ctypes.c_void_p(0x10010)), 4),
     (dict(N=0), 0), (dict(B=0, ptr=ctypes.c_void_p(0)), 0), (dict(dtype=2, ws=ctypes.c_void_p(0x10010)), 4),
-    (dict(dtype=2, ptr=ODD), 3), (dict(dtype=2, d=96), 2), (dict(dtype=3), 1),
+    (dict(dtype=2, ptr=ODD), 3), (dict(dtype=2, d=80), 2), (dict(dtype=3), 1),
     (dict(N=200, ws=ctypes.c_void_p(0x10010)), 4),   # ragged N passes the shape check
 ])
 def test_forward_argument_checks(L, kwargs, code):
@@ -95,7 +95,7 @@ def test_backward_argument_checks(L):
     assert L.fa_bwd_prep(FAKE, FAKE, FAKE, 1, 1, 128, 64, 0, None, 0, None) == 4
     assert L.fa_bwd_tiles(*([FAKE] * 7), 1, 1, 128, 64, 0.125, 0, 0, None, 0, None) == 4
     assert L.fa_bwd_dq_finish(FAKE, 1, 1, 100, 64, 0.125, 0, None, 0, None) == 4
-    assert L.fa_bwd_dq_finish(FAKE, 1, 1, 100, 96, 0.125, 0, None, 0, None) == 2
+    assert L.fa_bwd_dq_finish(FAKE, 1, 1, 100, 80, 0.125, 0, None, 0, None) == 2
 
 
 def _fwd_kv(L, Nq=128, Nk=256, causal=0, B=1, d=64, dtype=0):

@@ -217,3 +217,14 @@ def test_autograd_with_fewer_queries_than_keys():
     gpu = {"O": to64(o.detach()[0]), "LSE": ref["LSE"], "dQ": to64(q.grad[0]), "dK": to64(k.grad[0]),
            "dV": to64(v.grad[0])}
     compare(gpu, ref, "bf16")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_d96_kv_and_split(dtype, causal):
+    """d = 96 with Nq != Nk, ragged lengths, and a shape whose forward splits."""
+    for B, H, Nq, Nk in ((1, 2, 200, 460), (1, 1, 2048, 2048)):
+        q, k, v, do = make_inputs_kv(B, H, Nq, Nk, 96, dtype, "normal", 400 + Nq, device="cuda")
+        gpu = _run(q, k, v, do, causal)
+        ref = run_oracle_heads(q, k, v, do, causal, 96 ** -0.5, _heads(B, H))
+        compare({key: val.reshape((-1,) + val.shape[2:]) for key, val in gpu.items()}, ref, dtype)

@@ -72,6 +72,8 @@ BF16_SHAPES = [
     (1, 1, 1, 128),     # a single row
     (1, 1, 127, 64),
     (2, 2, 1000, 128),  # ragged with several K/V stages
+    (1, 2, 256, 96),    # d = 96: tiles padded to 128 columns
+    (2, 1, 333, 96),
 ]
 
 
@@ -206,7 +208,7 @@ def test_empty_problems(dtype):
 def test_unsupported_shapes_raise():
     import exact_tiled_attention_12_gb300 as fa
 
-    for shape in [(1, 1, 256, 96), (1, 1, 200, 32)]:
+    for shape in [(1, 1, 256, 80), (1, 1, 200, 32)]:
         q, k, v, _ = make_inputs(*shape, "bf16", "normal", 1, device="cuda")
         with pytest.raises(fa.FaError) as e:
             fa.fwd(q, k, v)

@@ -22,7 +22,7 @@
  *               visible keys.  All pointers are DEVICE pointers.
  *   dtype       FA_DTYPE_BF16: every [B,H,N,d] tensor is bfloat16; arithmetic
  *               is fp32 accumulation on the tensor cores, P and dS are rounded
- *               to bf16 before their products.  Supported: d ∈ {64, 128},
+ *               to bf16 before their products.  Supported: d ∈ {64, 96, 128},
  *               any N ≥ 1 (tiles of 128 rows; a ragged last tile reads zero
  *               rows past N and masks those keys), base pointers 16-byte
  *               aligned.
@@ -70,7 +70,7 @@ typedef struct CUstream_st* fa_stream_t;
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad scale/causal/dtype */
-  FA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (bf16 d∉{64,128}, fp32 d>128, sizes past the grid limits) */
+  FA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (bf16/fp16 d∉{64,96,128}, fp32 d>128, sizes past the grid limits) */
   FA_ERR_MISALIGNED = 3,   /* bf16/fp16 base pointer not 16-byte aligned */
   FA_ERR_WORKSPACE = 4,    /* workspace NULL, misaligned (256 B) or too small */
   FA_ERR_CUDA = 5,         /* a CUDA runtime/driver call or launch failed */

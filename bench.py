@@ -228,6 +228,11 @@ def run_ours(args, w, rank, world):
     tiles_tflops = flops_bwd / (statistics.mean(t_tiles) * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
     peak_sus = float(peaks.get("bf16_tflops_sustained", peak))
+    # Clock-derived dense bf16 rate: SMs × 8192 FLOP per SM clock (2·4096 MACs,
+    # the nominal 2.25 PFLOP/s over SMs and boost clock) × the maximum SM clock.
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
+    peak_theory = n_sms * 8192 * sm_max * 1e6 / 1e12
 
     # End to end through the public API: pinned host inputs copied in, results
     # (O, LSE, dQ, dK, dV) copied back, every step.
@@ -275,19 +280,33 @@ def run_ours(args, w, rank, world):
                    "l2": "flushed before every timed step (256 MiB write, outside the step's events)",
                    "parallelism": f"replicas x{world}"},
         "fwd": {"tflops": round(fwd_tflops, 2), "ms": round(statistics.mean(t_fwd), 4),
-                "frac_of_peak": round(fwd_tflops / peak, 4)},
+                "ms_median": round(statistics.median(t_fwd), 4), "ms_min": round(min(t_fwd), 4),
+                "ms_max": round(max(t_fwd), 4), "frac_of_peak": round(fwd_tflops / peak, 4)},
         "bwd": {"tflops": round(bwd_tflops, 2), "ms": round(statistics.mean(t_bwd), 4),
-                "frac_of_peak": round(bwd_tflops / peak, 4)},
+                "ms_median": round(statistics.median(t_bwd), 4), "ms_min": round(min(t_bwd), 4),
+                "ms_max": round(max(t_bwd), 4), "frac_of_peak": round(bwd_tflops / peak, 4)},
         "roofline": {"bound": "tensor", "kernel": f"fa_bwd_bf16_kernel<d={d},causal={int(w.causal)}> (fa_bwd_tiles)",
                      "achieved": round(tiles_tflops, 2), "peak": peak, "peak_kind": f"{peak_kind} bf16 burst",
                      "unit": "TFLOP/s", "frac": round(tiles_tflops / peak, 4),
                      "frac_of_sustained": round(tiles_tflops / peak_sus, 4),
+                     "peak_theoretical": round(peak_theory, 1),
+                     "frac_of_theoretical": round(tiles_tflops / peak_theory, 4),
+                     "peak_theoretical_note": f"{n_sms} SMs x 8192 FLOP/clk x {sm_max:.0f} MHz (clock-derived estimate)",
                      "ms_per_launch": round(statistics.mean(t_tiles), 4),
                      "algorithmic_flops_per_launch": flops_bwd,
                      "traffic": measured_traffic("fa_bwd_bf16_kernel", d, w.causal, w.name),
                      "traffic_unit": "bytes per launch (ncu dram read + write)"},
         "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
+        "softmax": {
+            # exponentials of the forward (one per visible score) per SM clock at
+            # the sampled median SM clock: the MUFU-side rate of the softmax
+            "exp_per_clk_per_sm": (round(w.B * w.H * N * N / (2 if w.causal else 1)
+                                         / (statistics.mean(t_fwd) * 1e-3) / (clk["sm_mhz"] * 1e6) / n_sms, 2)
+                                   if clk.get("sm_mhz") else None),
+        },
+        # per step: forward (+ the split-merge kernel when the forward splits),
+        # D pre-pass, tiled backward, dQ finish
+        "gpu_launches": (3 + (2 if fws_n else 1)) * args.steps,
         "clocks": clk,
         "wall_s_timed": round(wall, 4),
     }
@@ -394,7 +413,7 @@ def run_reference(args, w, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=600)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

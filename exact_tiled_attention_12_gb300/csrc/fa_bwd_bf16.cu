@@ -27,10 +27,12 @@
 // dPᵀ/dQ [2d+128, 2d+256).  dQ reuses the dPᵀ columns once the compute warps
 // have read dPᵀ; the next dPᵀ waits until dQ has been drained.
 //
-// CTA: 10 warps.  Warps 0-7 compute Pᵀ/dSᵀ (warp w owns key rows 32(w%4)..+31
-// and query columns 64(w/4)..+63) and then drain that tile's dQ from tensor
-// memory into the fp32 accumulator; warp 8 issues TMA, warp 9 issues the MMAs and
-// owns tensor memory.  The grid is head-major (K/V tile fastest).
+// CTA: 16 warps.  Warps 0-7 compute Pᵀ/dSᵀ (warp w owns key rows 32(w%4)..+31
+// and query columns 64(w/4)..+63); warps 8-11 drain each tile's dQ from
+// tensor memory into the fp32 accumulator with global reductions, so those
+// run while the compute warps work on the next tile; warp 12 issues TMA,
+// warp 13 issues the MMAs and owns tensor memory.  The grid is head-major
+// (K/V tile fastest).
 #include "fa_kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -39,10 +41,20 @@ namespace {
 
 constexpr int kBN = 128;            // keys per CTA
 constexpr int kBM = 128;            // queries per step
-constexpr int kThreads = 320;
-constexpr int kComputeWarps = 8;
-constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kThreads = 512;       // four warpgroups
+constexpr int kComputeWarps = 8;    // warpgroups 0, 1: Pᵀ and dSᵀ
+constexpr int kRedWarp = 8;         // warpgroup 2: dQ reductions
+constexpr int kRedWarps = 4;
+constexpr int kTmaWarp = 12;        // warpgroup 3: TMA, MMA (warps 14, 15 idle)
+constexpr int kMmaWarp = 13;
+// Registers per thread of each warpgroup (setmaxnreg).  The CTA's pool is
+// fixed at launch: kThreads × (65536 / kThreads) = 65536; the four
+// warpgroups' shares must fit in it or an increase would wait forever.
+constexpr int kRegsCompute = 176;
+constexpr int kRegsRed = 80;
+constexpr int kRegsMisc = 80;
+constexpr int kEndBarrier = 15;     // named barrier of the CTA's last step (1..4: Pᵀ pair barriers)
+static_assert(128 * (2 * kRegsCompute + kRegsRed + kRegsMisc) <= 65536, "warpgroup register shares exceed the pool");
 constexpr int kBox = 16384;         // one TMA box: 128 rows × 128 bytes
 // Exponential pairs per FMA-pipe exponential (0 = all on MUFU); measured on
 // GB300 the split makes no difference here, so all stay on MUFU.
@@ -135,7 +147,6 @@ __device__ __forceinline__ bool pair_sync_and(int id, bool ok) {
 // N = 96 for dV and dK; dQᵀ keeps M = 128 with zero rows past 96) and only
 // 96 columns are reduced or stored.
 template <int DR, bool CAUSAL, bool RAGGED, bool F16>
-// 10 warps: at most 3 per SM sub-partition, so up to 168 registers a thread.
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_constant__ BwdArgs a) {
   constexpr int D = DR <= 64 ? 64 : 128;
   using C = BwdCfg<D>;
@@ -190,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
     mbar_init(bar(kDPFull), 1);
     mbar_init(bar(kPdsFull), 32 * kComputeWarps);
     mbar_init(bar(kDqFull), 1);
-    mbar_init(bar(kDqDrained), 32 * kComputeWarps);
+    mbar_init(bar(kDqDrained), 32 * kRedWarps);
     mbar_init(bar(kDKVFull), 1);
     mbar_init(bar(kMmaDone), 1);
     *abort_flag = 0;
@@ -207,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
 
   if (warp < kComputeWarps) {
     // ------------------------------------------------------------ Pᵀ, dSᵀ
+    setmaxnreg_inc<kRegsCompute>();
     const int g = warp & 3;
     const int h = warp >> 2;                       // query columns [64h, 64h + 64)
     const int r = g * 32 + lane;                   // key row within the tile = TMEM lane
@@ -227,8 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       const int st = i & 1;
       const uint32_t par = (uint32_t)(i & 1);
       const int q0 = (i0 + i) * kBM;
-      ok = mbar_wait(bar(kSFull), par, wc, site(1)) && mbar_wait(bar(kDPFull), par, wc, site(2)) &&
-           mbar_wait(bar(kQFull + st), (uint32_t)((i >> 1) & 1), wc, site(3));
+      ok = mbar_wait_inl(bar(kSFull), par, wc, site(1)) &&
+           mbar_wait_inl(bar(kQFull + st), (uint32_t)((i >> 1) & 1), wc, site(3));
       ok = __all_sync(kFull, ok);
       // The pre-pass stored −LSE·log2(e) and −D, so each pair of columns is
       // one packed FMA (the exponent) and one packed add/multiply (dS).
@@ -256,10 +268,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
             p_chunk<false, kPolyEvery>(s, sl2x2, nlse + (c0 >> 1), r - c0, p + ch * 16);
         }
       }
+      // dPᵀ is issued after the previous tile's dQ has been drained, so it
+      // lands while the exponentials above run: wait for it only now.
+      if (ok) ok = mbar_wait_inl(bar(kDPFull), par, wc, site(2));
       // Both warps of the lane quarter have read their Sᵀ columns; Pᵀ may now
       // be written over the first 64 of them.
       ok = pair_sync_and(1 + g, ok);
       if (!ok) break;
+      tc_fence_after();
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[16];
@@ -299,46 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       fence_proxy_async_smem();
       mbar_arrive(bar(kPdsFull));
       mbar_arrive(bar(kQEmpty + st));
-
-      // dQ of this tile: the MMA thread issues it first after Pᵀ/dSᵀ, and the
-      // next Sᵀ/dPᵀ arrive only after dQ, dV and dK, so these warps are free
-      // to drain it.  Each thread reads its share into registers, releases the
-      // columns, then adds into the fp32 accumulator with global reductions.
-      ok = mbar_wait(bar(kDqFull), par, wc, site(6));
-      ok = __all_sync(kFull, ok);
-      if (!ok) break;
-      tc_fence_after();
-      if constexpr (D == 128) {
-        // dQᵀ: lane = head dim, columns = queries [64h, 64h + 64); a warp's
-        // reduction covers 32 consecutive floats of one accumulator row.
-        // Warps whose head dims are all past DR only release the columns.
-        if (g * 32 < DR) {
-          uint32_t v[64];
-          tmem_ld_x64(tmem + lane_off + C::kColDP + (uint32_t)(64 * h), v);
-          tc_fence_before();
-          mbar_arrive(bar(kDqDrained));
-          float* base = a.dqacc + ((size_t)wrow0 + (size_t)q0 + (size_t)(64 * h)) * DR + (size_t)r;
-#pragma unroll
-          for (int c = 0; c < 64; ++c) red_add_f32(base + (size_t)c * DR, u2f(v[c]));
-        } else {
-          tc_fence_before();
-          mbar_arrive(bar(kDqDrained));
-        }
-      } else {
-        // dQ: lane = query row, columns = head dims [32h, 32h + 32); 16-byte
-        // vector reductions along the row.
-        uint32_t v[32];
-        tmem_ld_x32(tmem + lane_off + C::kColDP + (uint32_t)(32 * h), v);
-        tc_fence_before();
-        mbar_arrive(bar(kDqDrained));
-        float* base = a.dqacc + ((size_t)wrow0 + (size_t)q0 + (size_t)r) * D + (size_t)(32 * h);
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) red_add_v4_f32(base + c, u2f(v[c]), u2f(v[c + 1]), u2f(v[c + 2]), u2f(v[c + 3]));
-      }
     }
     // ------------------------------------------------------------ dK, dV epilogue
     if (ok) {
-      ok = mbar_wait(bar(kDKVFull), 0, wc, site(5));
+      ok = mbar_wait_inl(bar(kDKVFull), 0, wc, site(5));
       ok = __all_sync(kFull, ok);
     }
     if (ok) {
@@ -360,7 +340,64 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         }
       }
     }
-  } else if (warp == kTmaWarp) {
+    tc_fence_before();
+    named_bar_arrive(kEndBarrier, kThreads);
+  } else if (warp < kRedWarp + kRedWarps) {
+    // ------------------------------------------------------------ dQ reductions
+    // The MMA thread issues each tile's dQ first after Pᵀ/dSᵀ and the next
+    // dPᵀ only after these warps have read dQ out of its columns.  Each thread
+    // reads its lane's share into registers, releases the columns, and adds
+    // into the fp32 accumulator with global reductions while the compute
+    // warps move on to the next tile.
+    setmaxnreg_dec<kRegsRed>();
+    const int g = warp & 3;                        // TMEM lane quarter
+    const int r = g * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(g * 32) << 16;
+    for (int i = 0; i < n; ++i) {
+      const int q0 = (i0 + i) * kBM;
+      bool ok = mbar_wait_inl(bar(kDqFull), (uint32_t)(i & 1), wc, site(6));
+      ok = __all_sync(kFull, ok);
+      if (!ok) break;
+      tc_fence_after();
+      if constexpr (D == 128) {
+        // dQᵀ: lane = head dim r, columns = the tile's 128 queries, read in
+        // two halves of 64; a warp's reduction covers 32 consecutive floats of
+        // one accumulator row.  Warps whose head dims are all past DR only
+        // release the columns.
+        if (g * 32 < DR) {
+          float* base = a.dqacc + ((size_t)wrow0 + (size_t)q0) * DR + (size_t)r;
+          uint32_t v[64];
+          tmem_ld_x64(tmem + lane_off + C::kColDP, v);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) red_add_f32(base + (size_t)c * DR, u2f(v[c]));
+          tmem_ld_x64(tmem + lane_off + C::kColDP + 64u, v);
+          tc_fence_before();
+          mbar_arrive(bar(kDqDrained));
+#pragma unroll
+          for (int c = 0; c < 64; ++c) red_add_f32(base + (size_t)(64 + c) * DR, u2f(v[c]));
+        } else {
+          tc_fence_before();
+          mbar_arrive(bar(kDqDrained));
+        }
+      } else {
+        // dQ: lane = query row r, columns = the 64 head dims; 16-byte vector
+        // reductions along the row.
+        uint32_t v[64];
+        tmem_ld_x64(tmem + lane_off + C::kColDP, v);
+        tc_fence_before();
+        mbar_arrive(bar(kDqDrained));
+        float* base = a.dqacc + ((size_t)wrow0 + (size_t)q0 + (size_t)r) * D;
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) red_add_v4_f32(base + c, u2f(v[c]), u2f(v[c + 1]), u2f(v[c + 2]), u2f(v[c + 3]));
+      }
+    }
+    tc_fence_before();
+    named_bar_arrive(kEndBarrier, kThreads);
+  } else {
+  // Warpgroup 3.  setmaxnreg is .aligned: the four warps execute this one
+  // instruction before taking their separate roles.
+  setmaxnreg_dec<kRegsMisc>();
+  if (warp == kTmaWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tmap(&a.tm_q);
@@ -375,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       int issued[2] = {0, 0};
       for (int i = 0; i < n; ++i) {
         const int s = i & 1;
-        if (i >= 2 && !mbar_wait(bar(kQEmpty + s), (uint32_t)(((i >> 1) - 1) & 1), wc, site(7))) break;
+        if (i >= 2 && !mbar_wait_inl(bar(kQEmpty + s), (uint32_t)(((i >> 1) - 1) & 1), wc, site(7))) break;
         const int q0 = (i0 + i) * kBM;
         mbar_arrive_expect_tx(bar(kQFull + s), 2u * C::kTile + 2u * kBM * 4);
         for (int bx = 0; bx < D / 64; ++bx) {
@@ -386,11 +423,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         bulk_load(sbase + C::kDV + s * kBM * 4, a.dvec + wrow0 + q0, kBM * 4, bar(kQFull + s));
         ++issued[s];
       }
-      mbar_wait_drain(bar(kKVFull), 0, wc, site(8));
+      mbar_wait_drain_inl(bar(kKVFull), 0, wc, site(8));
       for (int s = 0; s < 2; ++s)
-        if (issued[s] > 0) mbar_wait_drain(bar(kQFull + s), (uint32_t)((issued[s] - 1) & 1), wc, site(8));
+        if (issued[s] > 0) mbar_wait_drain_inl(bar(kQFull + s), (uint32_t)((issued[s] - 1) & 1), wc, site(8));
     }
-  } else {
+    __syncwarp();
+    named_bar_arrive(kEndBarrier, kThreads);
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16kind(128, kBM, false, false, F16);  // Sᵀ = K Qᵀ, dPᵀ = V dOᵀ
@@ -408,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
                  ks > 0 ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(bar(kKVFull), 0, wc, site(9)) && mbar_wait(bar(kQFull), 0, wc, site(10));
+      bool ok = mbar_wait_inl(bar(kKVFull), 0, wc, site(9)) && mbar_wait_inl(bar(kQFull), 0, wc, site(10));
       if (ok && n > 0) {
         tc_fence_after();
         issue_sd(0, C::kColS, sbase + C::kK);
@@ -418,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       }
       for (int i = 0; ok && i < n; ++i) {
         const int st = i & 1;
-        if (!mbar_wait(bar(kPdsFull), (uint32_t)(i & 1), wc, site(11))) {
+        if (!mbar_wait_inl(bar(kPdsFull), (uint32_t)(i & 1), wc, site(11))) {
           ok = false;
           break;
         }
@@ -451,14 +490,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         tc_commit(bar(kQEmpty + st));
         if (i + 1 < n) {
           // Sᵀ of the next tile overwrites Pᵀ: issued after dV, which reads it.
-          if (!mbar_wait(bar(kQFull + ((i + 1) & 1)), (uint32_t)(((i + 1) >> 1) & 1), wc, site(12))) {
+          if (!mbar_wait_inl(bar(kQFull + ((i + 1) & 1)), (uint32_t)(((i + 1) >> 1) & 1), wc, site(12))) {
             ok = false;
             break;
           }
           tc_fence_after();
           issue_sd(i + 1, C::kColS, sbase + C::kK);
           tc_commit(bar(kSFull));
-          if (!mbar_wait(bar(kDqDrained), (uint32_t)(i & 1), wc, site(13))) {
+          if (!mbar_wait_inl(bar(kDqDrained), (uint32_t)(i & 1), wc, site(13))) {
             ok = false;
             break;
           }
@@ -469,16 +508,19 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       }
       if (ok) tc_commit(bar(kDKVFull));
       tc_commit(bar(kMmaDone));
-      mbar_wait_drain(bar(kMmaDone), 0, wc, site(14));
+      mbar_wait_drain_inl(bar(kMmaDone), 0, wc, site(14));
     }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == kMmaWarp) {
+    __syncwarp();
+    // Every thread of the CTA has finished with tensor memory once all have
+    // arrived here; the allocating warp then frees it.
+    named_bar_sync(kEndBarrier, kThreads);
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  } else {
+    named_bar_arrive(kEndBarrier, kThreads);   // warps 14, 15
   }
+  }
+  // No code after the roles: their register counts differ (setmaxnreg).
 }
 
 template <int DR, bool CAUSAL, bool RAGGED, bool F16>

@@ -63,6 +63,26 @@ struct WaitCtx {
   unsigned int* fault;
 };
 
+// The slow path of a bounded wait, inlined at every call: kernels whose
+// warpgroups run with different register counts (setmaxnreg) cannot call one
+// out-of-line function from all of them.  mbar_wait_slow below is the
+// out-of-line copy (smaller code) for the other kernels.
+__device__ __forceinline__ bool mbar_wait_slow_inline(uint32_t bar, uint32_t parity, WaitCtx c, uint32_t site,
+                                                      bool honour_abort) {
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (honour_abort && *c.abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *c.abort_flag = 1;
+      atomicCAS(c.fault, 0u, site);
+      return false;
+    }
+  }
+}
+
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtx c, uint32_t site,
                                             bool honour_abort) {
   const unsigned long long t0 = globaltimer_ns();
@@ -91,6 +111,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, WaitCtx
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, WaitCtx c, uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, c, site, false);
+}
+// The two waits with the slow path inlined (for setmaxnreg kernels).
+__device__ __forceinline__ bool mbar_wait_inl(uint32_t bar, uint32_t parity, WaitCtx c, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow_inline(bar, parity, c, site, true);
+}
+__device__ __forceinline__ bool mbar_wait_drain_inl(uint32_t bar, uint32_t parity, WaitCtx c, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow_inline(bar, parity, c, site, false);
 }
 
 // ------------------------------------------------------------------ TMA / bulk copies
@@ -129,8 +158,26 @@ __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Named barrier over `count` threads (a multiple of 32).
+// Per-thread register count of the executing warpgroup (all four warps must
+// execute the same instruction).  `inc` waits until the CTA's pool, fixed at
+// launch (threads × registers at launch), has the registers, so the shares of
+// all warpgroups must add up to at most that pool.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg takes a multiple of 8 in [24, 256]");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg takes a multiple of 8 in [24, 256]");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 // Named barrier that also returns the AND of every participant's `ok`, so all
 // of them take the same branch afterwards.

@@ -482,14 +482,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         for (int ks = 0; ks < kBM / 16; ++ks)
           mma_ts(tmem + C::kColDV, tmem + C::kColS + (uint32_t)(8 * ks),
                  sdesc_sw128(ob + (uint32_t)(ks * 2048), kBox, 1024), kIdKV, (i > 0 || ks > 0) ? 1u : 0u);
-        // dK += dSᵀ Q
-#pragma unroll
-        for (int ks = 0; ks < kBM / 16; ++ks)
-          mma_ss(tmem + C::kColDK, sdesc_sw128(ds + (uint32_t)((ks >> 2) * kBox + (ks & 3) * 32), 16, 1024),
-                 sdesc_sw128(qb + (uint32_t)(ks * 2048), kBox, 1024), kIdKV, (i > 0 || ks > 0) ? 1u : 0u);
-        tc_commit(bar(kQEmpty + st));
-        if (i + 1 < n) {
-          // Sᵀ of the next tile overwrites Pᵀ: issued after dV, which reads it.
+        // Sᵀ of the next tile overwrites Pᵀ: issued right after dV, which
+        // reads it (the products run in issue order), and before dK, so the
+        // compute warps can start on it sooner.
+        const bool next = i + 1 < n;
+        if (next) {
           if (!mbar_wait_inl(bar(kQFull + ((i + 1) & 1)), (uint32_t)(((i + 1) >> 1) & 1), wc, site(12))) {
             ok = false;
             break;
@@ -497,6 +494,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
           tc_fence_after();
           issue_sd(i + 1, C::kColS, sbase + C::kK);
           tc_commit(bar(kSFull));
+        }
+        // dK += dSᵀ Q
+#pragma unroll
+        for (int ks = 0; ks < kBM / 16; ++ks)
+          mma_ss(tmem + C::kColDK, sdesc_sw128(ds + (uint32_t)((ks >> 2) * kBox + (ks & 3) * 32), 16, 1024),
+                 sdesc_sw128(qb + (uint32_t)(ks * 2048), kBox, 1024), kIdKV, (i > 0 || ks > 0) ? 1u : 0u);
+        tc_commit(bar(kQEmpty + st));
+        if (next) {
           if (!mbar_wait_inl(bar(kDqDrained), (uint32_t)(i & 1), wc, site(13))) {
             ok = false;
             break;

@@ -43,6 +43,7 @@ SIGNATURES = {
     "fa_bwd_kv_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
     "fa_bwd_kv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _Z, _P]),
     "fa_merge": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "fa_selftest_wait_timeout": (_I, [_P]),
 }
 MERGE_MAX_PARTS = 16
 

@@ -480,6 +480,12 @@ fa_status fa_merge(const void* const* o_parts, const float* const* lse_parts, in
   return from_cuda(fa::launch_merge(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+fa_status fa_selftest_wait_timeout(fa_stream_t stream) {
+  unsigned int* fault = fault_word_for_current_device();
+  if (!fault) return FA_ERR_CUDA;
+  return from_cuda(fa::launch_wait_timeout_selftest(fault, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 fa_status fa_sync_status(fa_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return FA_ERR_CUDA;

@@ -93,6 +93,12 @@ struct MergeArgs {
 };
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
 
+// ---------------------------------------------------------------- self-test
+
+// One CTA whose pipeline wait can never complete: the bounded wait gives up
+// after its time limit and records a fault code in `fault` (no trap, no hang).
+cudaError_t launch_wait_timeout_selftest(unsigned int* fault, cudaStream_t s);
+
 // ---------------------------------------------------------------- fp32 SIMT path
 
 cudaError_t launch_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int BH, int Nq,

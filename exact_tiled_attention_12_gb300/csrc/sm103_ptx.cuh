@@ -18,6 +18,9 @@
 namespace fa {
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
+// Backstop that ends a wait even if the timer were not to advance: rounds of
+// 64 polls (2^28 polls: past the 2 s limit unless one poll took under ~8 ns).
+constexpr uint32_t kWaitRoundLimit = 1u << 22;
 constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -70,12 +73,12 @@ struct WaitCtx {
 __device__ __forceinline__ bool mbar_wait_slow_inline(uint32_t bar, uint32_t parity, WaitCtx c, uint32_t site,
                                                       bool honour_abort) {
   const unsigned long long t0 = globaltimer_ns();
-  for (;;) {
+  for (uint32_t rounds = 0;; ++rounds) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (honour_abort && *c.abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs || rounds >= kWaitRoundLimit) {
       *c.abort_flag = 1;
       atomicCAS(c.fault, 0u, site);
       return false;
@@ -86,12 +89,12 @@ __device__ __forceinline__ bool mbar_wait_slow_inline(uint32_t bar, uint32_t par
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtx c, uint32_t site,
                                             bool honour_abort) {
   const unsigned long long t0 = globaltimer_ns();
-  for (;;) {
+  for (uint32_t rounds = 0;; ++rounds) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (honour_abort && *c.abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs || rounds >= kWaitRoundLimit) {
       *c.abort_flag = 1;
       atomicCAS(c.fault, 0u, site);
       return false;

@@ -226,6 +226,18 @@ fa_status fa_bwd_dq_finish(void* dq, int B, int H, int N, int d, float scale,
 fa_status fa_sync_status(fa_stream_t stream);
 
 /*
+ * Self-test of the failure path (not part of the computation).  Enqueues one
+ * small kernel whose pipeline wait can never complete, so the wait gives up
+ * after its time limit (2 s), records the fault word and raises the CTA's
+ * abort flag, and the CTA's other wait gives up on seeing it; the kernel then
+ * exits normally — nothing faults, traps or hangs.  Returns FA_OK if the
+ * launch succeeded; a following fa_sync_status() returns FA_ERR_TIMEOUT (and
+ * clears the word), after which the device is fully usable.  This is the
+ * path every tensor-core kernel takes when a wait runs out.
+ */
+fa_status fa_selftest_wait_timeout(fa_stream_t stream);
+
+/*
  * Size of the scratch array compiled into libfa.so for fa_bwd_noalloc:
  * 32 MiB, held on every GPU that loads the library until the process exits.
  */

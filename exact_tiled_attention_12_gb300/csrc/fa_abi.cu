@@ -106,7 +106,7 @@ fa_status check_shape(int B, int H, int Nq, int Nk, int d, fa_dtype dtype, int c
   if (causal && Nq > Nk) return FA_ERR_UNSUPPORTED;
   if (s.heads() > 65535) return FA_ERR_UNSUPPORTED;
   if (is16(dtype)) {
-    if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 96 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
     if (s.rows_pad() >= (1ll << 31) || s.heads() * s.nk_pad() >= (1ll << 31) || s.nk_pad() / 128 > 65535)
       return FA_ERR_UNSUPPORTED;
   } else {
@@ -138,7 +138,8 @@ size_t workspace_bytes_for(const Shape& s, fa_dtype dtype) {
   if (s.empty()) return 0;
   if (dtype == FA_DTYPE_FP32) return 2 * pad256((size_t)s.rows() * 4);
   const size_t rows = (size_t)s.rows_pad();
-  return 2 * pad256(rows * 4) + pad256(rows * (size_t)s.d * 4);
+  // d = 256 writes dQ directly (no fp32 accumulator).
+  return 2 * pad256(rows * 4) + (s.d == 256 ? 0 : pad256(rows * (size_t)s.d * 4));
 }
 
 // Workspace parts: D (float32 per query row), the forward's LSE per row (base
@@ -158,7 +159,7 @@ fa_status carve_workspace(const Shape& s, fa_dtype dtype, void* ws, size_t bytes
   const size_t rows = dtype == FA_DTYPE_FP32 ? (size_t)s.rows() : (size_t)s.rows_pad();
   w->dvec = reinterpret_cast<float*>(p);
   w->lse2 = reinterpret_cast<float*>(p + pad256(rows * 4));
-  w->dqacc = dtype == FA_DTYPE_FP32 ? nullptr : reinterpret_cast<float*>(p + 2 * pad256(rows * 4));
+  w->dqacc = (dtype == FA_DTYPE_FP32 || s.d == 256) ? nullptr : reinterpret_cast<float*>(p + 2 * pad256(rows * 4));
   return FA_OK;
 }
 
@@ -190,11 +191,11 @@ int forward_causal(int causal, const Shape& s) { return causal && s.Nq > 1 ? 1 :
 size_t fwd_workspace_bytes(const Shape& s, int causal, fa_dtype dtype, FwdPlan* plan) {
   causal = forward_causal(causal, s);
   if (s.empty() || causal || !is16(dtype)) return 0;
-  const int units = fa::fwd_units((int)s.B, (int)s.H, (int)s.Nq);
+  const int units = fa::fwd_units((int)s.B, (int)s.H, (int)s.Nq, (int)s.d);
   int n_full, splits;
   fa::fwd_split_plan(units, sm_count_current_device(), (int)(s.nk_pad() / 128), &n_full, &splits);
   if (splits <= 1 || n_full >= units) return 0;
-  const size_t rows = (size_t)(units - n_full) * (size_t)splits * 256;
+  const size_t rows = (size_t)(units - n_full) * (size_t)splits * (size_t)fa::fwd_unit_rows((int)s.d);
   const size_t opart = pad256(rows * (size_t)s.d * 4);
   if (plan) *plan = FwdPlan{n_full, splits, opart};
   return opart + pad256(rows * 4);
@@ -246,7 +247,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
   // Load balancing needs the workspace; without one (NULL) every unit runs whole.
   FwdPlan plan;
   const size_t need = fwd_workspace_bytes(s, causal, dtype, &plan);
-  a.n_full = fa::fwd_units(B, H, Nq);
+  a.n_full = fa::fwd_units(B, H, Nq, d);
   a.splits = 1;
   a.opart = nullptr;
   a.lpart = nullptr;
@@ -286,7 +287,7 @@ fa_status tiles_impl(const void* q, const void* k, const void* v, const void* dO
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (s.empty()) return FA_OK;
   if ((st = check_ptrs({q, k, v, dO, dk, dv}, dtype)) != FA_OK) return st;
-  if (dtype == FA_DTYPE_FP32 && (st = check_ptrs({dq}, dtype)) != FA_OK) return st;
+  if ((dtype == FA_DTYPE_FP32 || d == 256) && (st = check_ptrs({dq}, dtype)) != FA_OK) return st;
   Workspace w;
   if ((st = carve_workspace(s, dtype, workspace, workspace_bytes, &w)) != FA_OK) return st;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
@@ -299,18 +300,20 @@ fa_status tiles_impl(const void* q, const void* k, const void* v, const void* dO
   if (!fault) return FA_ERR_CUDA;
   fa::BwdArgs a;
   const int bm = fa::bwd_bf16_block_m(d);
+  const int bn = fa::bwd_kv_box_rows(d);
   const long long heads = s.heads();
   const bool rv = s.rows_view();
   const bool f16 = dtype == FA_DTYPE_FP16;
   if (!encode_bf16_heads(&a.tm_q, q, heads, Nq, d, bm, rv, f16) ||
-      !encode_bf16_heads(&a.tm_k, k, heads, Nk, d, 128, rv, f16) ||
-      !encode_bf16_heads(&a.tm_v, v, heads, Nk, d, 128, rv, f16) ||
+      !encode_bf16_heads(&a.tm_k, k, heads, Nk, d, bn, rv, f16) ||
+      !encode_bf16_heads(&a.tm_v, v, heads, Nk, d, bn, rv, f16) ||
       !encode_bf16_heads(&a.tm_do, dO, heads, Nq, d, bm, rv, f16))
     return FA_ERR_CUDA;
   a.f16 = f16 ? 1 : 0;
   a.lse2 = w.lse2;
   a.dvec = w.dvec;
   a.dqacc = w.dqacc;
+  a.dq = d == 256 ? dq : nullptr;
   a.dk = dk;
   a.dv = dv;
   a.B = B;
@@ -331,7 +334,8 @@ fa_status finish_impl(void* dq, int B, int H, int Nq, int Nk, int d, float scale
   fa_status st = check_shape(B, H, Nq, Nk, d, dtype, 0, &s);
   if (st != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
-  if (s.empty() || dtype == FA_DTYPE_FP32) return FA_OK;
+  // fp32 and d = 256 write dQ in the tiled pass.
+  if (s.empty() || dtype == FA_DTYPE_FP32 || d == 256) return FA_OK;
   if ((st = check_ptrs({dq}, dtype)) != FA_OK) return st;
   Workspace w;
   if ((st = carve_workspace(s, dtype, workspace, workspace_bytes, &w)) != FA_OK) return st;

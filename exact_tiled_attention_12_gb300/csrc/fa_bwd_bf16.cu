@@ -565,7 +565,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
   const long long src = head * Nq + pos;       // row of O, dO and LSE
   const bool live = pos < Nq;
   float acc = 0.f;
-  if (has_cols) {
+  if (has_cols && dqacc != nullptr) {
     float4* z = reinterpret_cast<float4*>(dqacc + row * DR + part * 8);
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -620,6 +620,8 @@ __global__ void __launch_bounds__(256) dq_finish_kernel(const float* __restrict_
 
 int bwd_bf16_block_m(int) { return kBM; }
 
+int bwd_kv_box_rows(int d) { return d == 256 ? 64 : kBN; }
+
 size_t bwd_bf16_smem_bytes(int d) { return d <= 64 ? BwdCfg<64>::kBytes : BwdCfg<128>::kBytes; }
 
 template <bool F16>
@@ -640,6 +642,7 @@ static cudaError_t dispatch_bwd(const BwdArgs& a, bool ragged, cudaStream_t s) {
 }
 
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t s) {
+  if (a.d == 256) return launch_bwd_d256(a, s);
   const bool ragged = a.Nq % kBM != 0 || a.Nk % kBN != 0;
   return a.f16 ? dispatch_bwd<true>(a, ragged, s) : dispatch_bwd<false>(a, ragged, s);
 }
@@ -656,7 +659,10 @@ cudaError_t launch_bwd_prep_bf16(const void* o, const void* dO, const float* lse
   if (heads <= 0 || heads > 65535 || n_pad % 128 != 0) return cudaErrorInvalidValue;
   const int threads_per_row = d == 96 ? 16 : d / 8;
   const dim3 grid((unsigned)((long long)n_pad * threads_per_row / 256), (unsigned)heads);
-  if (d == 128)
+  if (d == 256)
+    f16 ? launch_prep<256, true>(grid, o, dO, lse, dvec, lse2, dqacc, Nq, n_pad, s)
+        : launch_prep<256, false>(grid, o, dO, lse, dvec, lse2, dqacc, Nq, n_pad, s);
+  else if (d == 128)
     f16 ? launch_prep<128, true>(grid, o, dO, lse, dvec, lse2, dqacc, Nq, n_pad, s)
         : launch_prep<128, false>(grid, o, dO, lse, dvec, lse2, dqacc, Nq, n_pad, s);
   else if (d == 96)

@@ -443,52 +443,52 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
   }
 }
 
-template <int DR, bool F16>
-cudaError_t launch_combine(const FwdArgs& a, int tail, cudaStream_t s);
-
 template <int DR, bool CAUSAL, bool RAGGED, bool F16>
 cudaError_t launch_impl(const FwdArgs& a, cudaStream_t s) {
   auto kern = fa_fwd_bf16_kernel<DR, CAUSAL, RAGGED, F16>;
   const size_t smem = FwdLayout<(DR <= 64 ? 64 : 128)>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const long long units = (long long)fwd_units(a.B, a.H, a.Nq);
+  const long long units = (long long)fwd_units(a.B, a.H, a.Nq, DR);
   const long long ctas = CAUSAL ? units : a.n_full + (units - a.n_full) * a.splits;
   kern<<<(unsigned)ctas, kThreads, smem, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess || CAUSAL || a.splits <= 1 || a.n_full >= units) return e;
-  return launch_combine<DR, F16>(a, (int)(units - a.n_full), s);
+  return launch_fwd_combine(a, (int)(units - a.n_full), 2 * kBM, s);
 }
 
 // Merge of the split partials, "Flash Attention" tutorial, 2.Online Softmax
 // §3.1/§4.1 and §七 (the merge is log-sum-exp): for one query row with
 // partials (O_k, L_k) over disjoint key ranges, L = ln Σ_k e^{L_k} and
 // O = Σ_k e^{L_k − L} O_k.  One warp per row; lanes over the head dims.
+// A work unit covers `unit_rows` query rows of one head (256 for the
+// two-tile kernel, 128 at d = 256); partial row p of unit slot u·splits + k
+// is opart row (u·splits + k)·unit_rows + p.
 template <int DR, bool F16>
 __global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restrict__ opart,
                                                           const float* __restrict__ lpart, uint16_t* __restrict__ o,
                                                           float* __restrict__ lse, int Nq, int n_full, int splits,
-                                                          int tail) {
+                                                          int tail, int unit_rows) {
   constexpr int V = DR / 32;   // consecutive head dims per lane
   const int row = (int)(blockIdx.x * 8 + (threadIdx.x >> 5));
   const int lane = threadIdx.x & 31;
-  if (row >= tail * 2 * kBM) return;
-  const int u = row / (2 * kBM), rr = row % (2 * kBM);
-  const int pairs = (Nq + 2 * kBM - 1) / (2 * kBM);
+  if (row >= tail * unit_rows) return;
+  const int u = row / unit_rows, rr = row % unit_rows;
+  const int per_head = (Nq + unit_rows - 1) / unit_rows;
   const int unit = n_full + u;
-  const int q = (unit % pairs) * 2 * kBM + rr;
+  const int q = (unit % per_head) * unit_rows + rr;
   if (q >= Nq) return;
-  const size_t orow = (size_t)(unit / pairs) * Nq + (size_t)q;
+  const size_t orow = (size_t)(unit / per_head) * Nq + (size_t)q;
   float mx = -INFINITY;
-  for (int k = 0; k < splits; ++k) mx = fmaxf(mx, lpart[(size_t)(u * splits + k) * 2 * kBM + rr]);
+  for (int k = 0; k < splits; ++k) mx = fmaxf(mx, lpart[(size_t)(u * splits + k) * unit_rows + rr]);
   float sum = 0.f;
-  for (int k = 0; k < splits; ++k) sum += expf(lpart[(size_t)(u * splits + k) * 2 * kBM + rr] - mx);
+  for (int k = 0; k < splits; ++k) sum += expf(lpart[(size_t)(u * splits + k) * unit_rows + rr] - mx);
   const float total = mx + logf(sum);
   float acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
   for (int k = 0; k < splits; ++k) {
-    const size_t pr = (size_t)(u * splits + k) * 2 * kBM + rr;
+    const size_t pr = (size_t)(u * splits + k) * unit_rows + rr;
     const float w = expf(lpart[pr] - total);
     const float* src = opart + pr * DR + lane * V;
 #pragma unroll
@@ -506,17 +506,36 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restric
 }
 
 template <int DR, bool F16>
-cudaError_t launch_combine(const FwdArgs& a, int tail, cudaStream_t s) {
-  const int rows = tail * 2 * kBM;
-  fwd_combine_kernel<DR, F16><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a.opart, a.lpart,
-                                                                        static_cast<uint16_t*>(a.o), a.lse, a.Nq, a.n_full,
-                                                                   a.splits, tail);
+cudaError_t combine_impl(const FwdArgs& a, int tail, int unit_rows, cudaStream_t s) {
+  const int rows = tail * unit_rows;
+  fwd_combine_kernel<DR, F16><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
+      a.opart, a.lpart, static_cast<uint16_t*>(a.o), a.lse, a.Nq, a.n_full, a.splits, tail, unit_rows);
   return cudaGetLastError();
+}
+
+template <bool F16>
+cudaError_t combine_dispatch(const FwdArgs& a, int tail, int unit_rows, cudaStream_t s) {
+  switch (a.d) {
+    case 64: return combine_impl<64, F16>(a, tail, unit_rows, s);
+    case 96: return combine_impl<96, F16>(a, tail, unit_rows, s);
+    case 128: return combine_impl<128, F16>(a, tail, unit_rows, s);
+    case 256: return combine_impl<256, F16>(a, tail, unit_rows, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-int fwd_units(int B, int H, int Nq) { return B * H * ((Nq + 2 * kBM - 1) / (2 * kBM)); }
+int fwd_unit_rows(int d) { return d == 256 ? kBM : 2 * kBM; }
+
+int fwd_units(int B, int H, int Nq, int d) {
+  const int rows = fwd_unit_rows(d);
+  return B * H * ((Nq + rows - 1) / rows);
+}
+
+cudaError_t launch_fwd_combine(const FwdArgs& a, int tail, int unit_rows, cudaStream_t s) {
+  return a.f16 ? combine_dispatch<true>(a, tail, unit_rows, s) : combine_dispatch<false>(a, tail, unit_rows, s);
+}
 
 void fwd_split_plan(int units, int num_sms, int n_kv, int* n_full, int* splits) {
   *n_full = units;
@@ -561,6 +580,7 @@ static cudaError_t dispatch_fwd(const FwdArgs& a, bool ragged, cudaStream_t s) {
 }
 
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s) {
+  if (a.d == 256) return launch_fwd_d256(a, s);
   const bool ragged = a.Nq % kBM != 0 || a.Nk % kBN != 0;
   if (a.f16) return dispatch_fwd<true>(a, ragged, s);
   return dispatch_fwd<false>(a, ragged, s);

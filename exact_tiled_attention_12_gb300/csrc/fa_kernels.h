@@ -29,21 +29,27 @@ struct FwdArgs {
   float scale_log2;       // scale · log2(e): scores are handled in base 2
   int causal;
   unsigned int* fault;
-  // Non-causal load balancing: two-tile units [0, n_full) run whole; each of
-  // the remaining units runs as `splits` CTAs over K/V sub-ranges writing
-  // fp32 partials (opart [slots·256, d], lpart [slots·256]) that a combine
-  // kernel merges.  splits = 1 (or n_full = all units) disables it.
+  // Non-causal load balancing: units [0, n_full) run whole; each of the
+  // remaining units runs as `splits` CTAs over K/V sub-ranges writing fp32
+  // partials (opart [slots·unit_rows, d], lpart [slots·unit_rows]) that a
+  // combine kernel merges.  splits = 1 (or n_full = all units) disables it.
   int n_full, splits;
   float* opart;
   float* lpart;
 };
-// Two-tile (256-query) work units of the forward.
-int fwd_units(int B, int H, int Nq);
+// Work units of the forward: 256 query rows (two tiles) per CTA, 128 at d = 256.
+int fwd_unit_rows(int d);
+int fwd_units(int B, int H, int Nq, int d);
 // Split plan for `units` equal units of `n_kv` K/V tiles on `num_sms` SMs: the
 // units of the last, partial wave are split when that fills the GPU better.
 void fwd_split_plan(int units, int num_sms, int n_kv, int* n_full, int* splits);
 size_t fwd_bf16_smem_bytes(int d);
+// Dispatches on d (64, 96, 128; 256 goes to launch_fwd_d256).
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s);
+// d = 256: one 128-row query tile per CTA, double-buffered scores.
+cudaError_t launch_fwd_d256(const FwdArgs& a, cudaStream_t s);
+// Merges the fp32 partials of the `tail` split units (unit_rows rows each).
+cudaError_t launch_fwd_combine(const FwdArgs& a, int tail, int unit_rows, cudaStream_t s);
 
 // Backward tiled loop.  Tensor maps as in the forward (128-row boxes).
 // The workspace arrays hold n_pad = 128·⌈Nq/128⌉ rows per head.
@@ -51,7 +57,8 @@ struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
   const float* lse2;      // workspace: −LSE · log2(e), [B·H·n_pad]
   const float* dvec;      // workspace: −D = −rowsum(dO ⊙ O), [B·H·n_pad]
-  float* dqacc;           // workspace: fp32 dQ accumulator, [B·H·n_pad, d]
+  float* dqacc;           // workspace: fp32 dQ accumulator, [B·H·n_pad, d] (not used at d = 256)
+  void* dq;               // [B·H, Nq, d], written directly at d = 256 (else by the finish pass)
   void* dk;               // [B·H, Nk, d] in the 16-bit type
   void* dv;
   int B, H, Nq, Nk, d;
@@ -63,10 +70,17 @@ struct BwdArgs {
 };
 int bwd_bf16_block_m(int d);
 size_t bwd_bf16_smem_bytes(int d);
+// Dispatches on d (64, 96, 128; 256 goes to launch_bwd_d256).
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t s);
+// d = 256: a dK/dV kernel over 64-key tiles and a dQ kernel over 128-query
+// tiles (K and V maps with 64-row boxes); dQ is written scaled, in the 16-bit
+// type, so no accumulator and no finish pass.
+cudaError_t launch_bwd_d256(const BwdArgs& a, cudaStream_t s);
+// Rows of the K/V boxes the backward's tensor maps use.
+int bwd_kv_box_rows(int d);
 
 // Backward pre-pass: −D = −rowsum(dO ⊙ O) and −LSE·log2(e) per query row, dQ
-// accumulator zeroed.  The workspace arrays hold n_pad ≥ Nq rows per head
+// accumulator zeroed (dqacc may be null: d = 256 has none).  The workspace arrays hold n_pad ≥ Nq rows per head
 // (whole 128-row tiles); padding rows get −LSE = −∞ (so P = 0) and D = 0.
 cudaError_t launch_bwd_prep_bf16(const void* o, const void* dO, const float* lse, float* dvec, float* lse2,
                                  float* dqacc, long long heads, int Nq, int n_pad, int d, int f16, cudaStream_t s);

@@ -22,9 +22,9 @@
  *               visible keys.  All pointers are DEVICE pointers.
  *   dtype       FA_DTYPE_BF16: every [B,H,N,d] tensor is bfloat16; arithmetic
  *               is fp32 accumulation on the tensor cores, P and dS are rounded
- *               to bf16 before their products.  Supported: d ∈ {64, 96, 128},
- *               any N ≥ 1 (tiles of 128 rows; a ragged last tile reads zero
- *               rows past N and masks those keys), base pointers 16-byte
+ *               to bf16 before their products.  Supported: d ∈ {64, 96, 128,
+ *               256}, any N ≥ 1 (tiles of 128 rows; a ragged last tile reads
+ *               zero rows past N and masks those keys), base pointers 16-byte
  *               aligned.
  *               FA_DTYPE_FP16: the same with IEEE half precision (P and dS
  *               rounded to fp16; outputs that pass ±65504 become ±inf).
@@ -70,7 +70,7 @@ typedef struct CUstream_st* fa_stream_t;
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad scale/causal/dtype */
-  FA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (bf16/fp16 d∉{64,96,128}, fp32 d>128, sizes past the grid limits) */
+  FA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (bf16/fp16 d∉{64,96,128,256}, fp32 d>128, sizes past the grid limits) */
   FA_ERR_MISALIGNED = 3,   /* bf16/fp16 base pointer not 16-byte aligned */
   FA_ERR_WORKSPACE = 4,    /* workspace NULL, misaligned (256 B) or too small */
   FA_ERR_CUDA = 5,         /* a CUDA runtime/driver call or launch failed */
@@ -130,8 +130,8 @@ fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float*
 /*
  * Bytes of device workspace fa_bwd needs for this problem (0 for an empty
  * one).  BF16: D and the base-2 LSE (4·B·H·Np bytes each) plus a float32 dQ
- * accumulator (4·B·H·Np·d bytes), Np = 128·⌈N/128⌉ (whole tiles per head),
- * each part padded to 256 bytes.  FP32: D and
+ * accumulator (4·B·H·Np·d bytes; none at d = 256), Np = 128·⌈N/128⌉ (whole
+ * tiles per head), each part padded to 256 bytes.  FP32: D and
  * a copy of LSE (4·B·H·N bytes each, padded to 256).
  * Pure host arithmetic; returns 0 for invalid arguments.
  */
@@ -143,7 +143,8 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d, fa_dtype dtype);
  * at least fa_bwd_workspace_size() bytes, 256-byte aligned; its contents on
  * entry do not matter and are clobbered.  The bf16 path accumulates dQ in
  * float32 with reductions whose order varies, so dQ is not bitwise
- * reproducible run to run; O, LSE, dK and dV are.
+ * reproducible run to run; O, LSE, dK and dV are.  At d = 256 dQ comes from
+ * its own pass over the keys (no reductions) and is reproducible too.
  * Cited: "Flash Attention" tutorial, 4.附录A "反向传播的公式推导" 六 (tiled
  * backward with the D precompute; here K/V tiles are the outer loop).
  * Equivalent to fa_bwd_prep + fa_bwd_tiles + fa_bwd_dq_finish on one stream.
@@ -202,8 +203,9 @@ fa_status fa_merge(const void* const* o_parts, const float* const* lse_parts, in
  *                      dV += Pᵀ dO, dP = dO Vᵀ, dS = P ⊙ (dP - D), dK += dSᵀ Q
  *                      and dQ += dS K (into the accumulator); writes dk, dv.
  *   fa_bwd_dq_finish — dQ = scale · accumulator, rounded to the output dtype.
- * For FA_DTYPE_FP32, fa_bwd_tiles writes dq directly and fa_bwd_dq_finish is
- * a no-op.
+ * For FA_DTYPE_FP32, and for d = 256 (where fa_bwd_tiles runs a dK/dV kernel
+ * over 64-key tiles and a dQ kernel over 128-query tiles), fa_bwd_tiles
+ * writes dq directly and fa_bwd_dq_finish is a no-op.
  */
 fa_status fa_bwd_prep(const void* o, const void* dO, const float* lse,
                       int B, int H, int N, int d, fa_dtype dtype,

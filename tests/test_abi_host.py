@@ -57,6 +57,9 @@ def test_workspace_size(L):
     assert L.fa_bwd_workspace_size(2, 1, 200, 64, 0) == 2 * (2 * 256 * 4) + 2 * 256 * 64 * 4
     assert L.fa_bwd_workspace_size(0, 1, 128, 64, 0) == 0
     assert L.fa_bwd_workspace_size(-1, 1, 128, 64, 0) == 0
+    # d = 256 writes dQ directly: D and LSE2 only (200 -> 256 rows per head)
+    assert L.fa_bwd_workspace_size(2, 3, 200, 256, 0) == 2 * (6 * 256 * 4)
+    assert L.fa_bwd_workspace_size(2, 3, 200, 256, 2) == 2 * (6 * 256 * 4)
 
 
 FAKE = ctypes.c_void_p(0x10000)       # 16-byte aligned, never dereferenced
@@ -77,6 +80,8 @@ def _fwd(L, ptr=FAKE, B=1, H=1, N=128, d=128, scale=0.1, causal=0, dtype=0, ws=N
     (dict(N=0), 0), (dict(B=0, ptr=ctypes.c_void_p(0)), 0), (dict(dtype=2, ws=ctypes.c_void_p(0x10010)), 4),
     (dict(dtype=2, ptr=ODD), 3), (dict(dtype=2, d=80), 2), (dict(dtype=3), 1),
     (dict(N=200, ws=ctypes.c_void_p(0x10010)), 4),   # ragged N passes the shape check
+    (dict(d=256, ws=ctypes.c_void_p(0x10010)), 4),   # d = 256 passes the shape check (bf16, fp16)
+    (dict(d=256, dtype=2, ws=ctypes.c_void_p(0x10010)), 4), (dict(d=192), 2), (dict(d=512), 2),
 ])
 def test_forward_argument_checks(L, kwargs, code):
     assert _fwd(L, **kwargs) == code

@@ -23,12 +23,12 @@
 //
 //  * dq: a CTA owns 128 queries and walks 64-key tiles, recomputing S and dP:
 //      S_b = Q K_jᵀ, dP_b = dO V_jᵀ into buffer b = j mod 2
-//      dQ += dS K_j                        (A = dS from tensor memory, N = 64 per box)
+//      dQ += dS K_j                        (A = dS from tensor memory, N = 256)
 //    Tensor memory: S_b [64b, 64b + 64), dP_b [128 + 64b, ...), dQ [256, 512);
 //    dS (16-bit) is written over the dP columns its thread read.  The MMA
 //    order dQ_j, dP_{j+2}, S_{j+2} overlaps the elementwise work of tile
-//    j + 1 with the products; K streams through a ring of two tiles (each box
-//    released once dQ_j has read it), V through one.
+//    j + 1 with the products; K streams through a ring of two tiles (released
+//    once dQ_j has read them), V through one.
 //
 // Both kernels: warps 0-7 do the elementwise work, thread (w, lane) owning
 // query row 32(w mod 4) + lane and key columns 32⌊w/4⌋ .. +31 of a 64-key
@@ -305,16 +305,21 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
       constexpr uint32_t kIdT = idesc_f16kind(128, kBN, true, true, F16);    // dVᵀ += dOᵀ P, dKᵀ += Qᵀ dS
       // S (A = Q) or dP (A = dO) of query tile i, box by box as the boxes land.
       auto issue_sd = [&](int i, uint32_t col, uint32_t a_tile, uint32_t b_tile, int full) -> bool {
+        const uint64_t ad = sdesc_sw128(a_tile, 16, 1024), bd = sdesc_sw128(b_tile, 16, 1024);
+        const uint32_t dcol = tmem + col;
         for (int bx = 0; bx < 4; ++bx) {
           if (!mbar_wait(bar(full + bx), (uint32_t)(i & 1), wc, site(8))) return false;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + col, sdesc_sw128(a_tile + bx * kQBox + 32u * k, 16, 1024),
-                   sdesc_sw128(b_tile + bx * kKBox + 32u * k, 16, 1024), kIdS, (bx > 0 || k > 0) ? 1u : 0u);
+            mma_ss(dcol, sdesc_add(ad, bx * kQBox + 32u * k), sdesc_add(bd, bx * kKBox + 32u * k), kIdS,
+                   (bx > 0 || k > 0) ? 1u : 0u);
         }
         return true;
       };
+      // dKᵀ / dVᵀ operands: Q, dO read MN-major (A), dS, P read MN-major (B).
+      const uint64_t q_mn = sdesc_sw128(sbase + kQ, kQBox, 1024), do_mn = sdesc_sw128(sbase + kDO, kQBox, 1024);
+      const uint64_t ds_mn = sdesc_sw128(sbase + kDS, kQBox, 1024), p_mn = sdesc_sw128(sbase + kP, kQBox, 1024);
       bool ok = mbar_wait(bar(kKVFull), 0, wc, site(9));
       if (ok && n > 0) {
         ok = issue_sd(0, kColS, sbase + kQ, sbase + kK, kQFull);
@@ -332,19 +337,21 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
         tc_fence_after();
         // dKᵀ_h += Q_hᵀ dS, then dVᵀ_h += dO_hᵀ P: A MN-major over the two
         // boxes of half h, B = dS / P [query][key] MN-major; K-steps of 16 queries.
+#pragma unroll
         for (int h = 0; h < 2; ++h) {
 #pragma unroll
           for (int ks = 0; ks < kBM / 16; ++ks)
-            mma_ss(tmem + kColDK + 64u * h, sdesc_sw128(sbase + kQ + 2 * h * kQBox + ks * 2048, kQBox, 1024),
-                   sdesc_sw128(sbase + kDS + ks * 2048, kQBox, 1024), kIdT, (i > 0 || ks > 0) ? 1u : 0u);
+            mma_ss(tmem + kColDK + 64u * h, sdesc_add(q_mn, 2 * h * kQBox + ks * 2048), sdesc_add(ds_mn, ks * 2048),
+                   kIdT, (i > 0 || ks > 0) ? 1u : 0u);
           tc_commit(bar(kQEmpty + 2 * h));
           tc_commit(bar(kQEmpty + 2 * h + 1));
         }
+#pragma unroll
         for (int h = 0; h < 2; ++h) {
 #pragma unroll
           for (int ks = 0; ks < kBM / 16; ++ks)
-            mma_ss(tmem + kColDV + 64u * h, sdesc_sw128(sbase + kDO + 2 * h * kQBox + ks * 2048, kQBox, 1024),
-                   sdesc_sw128(sbase + kP + ks * 2048, kQBox, 1024), kIdT, (i > 0 || ks > 0) ? 1u : 0u);
+            mma_ss(tmem + kColDV + 64u * h, sdesc_add(do_mn, 2 * h * kQBox + ks * 2048), sdesc_add(p_mn, ks * 2048),
+                   kIdT, (i > 0 || ks > 0) ? 1u : 0u);
           tc_commit(bar(kDOEmpty + 2 * h));
           tc_commit(bar(kDOEmpty + 2 * h + 1));
         }
@@ -597,48 +604,50 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16kind(128, kBN, false, false, F16);   // S = Q Kᵀ, dP = dO Vᵀ
-      constexpr uint32_t kIdQ = idesc_f16kind(128, 64, false, true, F16);     // dQ += dS K, one box of K per product
+      constexpr uint32_t kIdQ = idesc_f16kind(128, kD, false, true, F16);     // dQ += dS K, N = 256 over the four K boxes
+      const uint64_t q_k = sdesc_sw128(sbase + kQ, 16, 1024), do_k = sdesc_sw128(sbase + kDO, 16, 1024);
+      const uint64_t k_k = sdesc_sw128(sbase + kK, 16, 1024), v_k = sdesc_sw128(sbase + kV, 16, 1024);
+      const uint64_t k_mn = sdesc_sw128(sbase + kK, kKBox, 1024);
       auto issue_s = [&](int j) -> bool {
-        const uint32_t col = kColS + 64u * (uint32_t)(j & 1);
+        const uint32_t col = tmem + kColS + 64u * (uint32_t)(j & 1);
         for (int bx = 0; bx < 4; ++bx) {
           const int gi = 4 * j + bx, slot = gi % kKSlots;
           if (!mbar_wait(bar(kKFull + slot), (uint32_t)((gi / kKSlots) & 1), wc, site(8))) return false;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + col, sdesc_sw128(sbase + kQ + bx * kQBox + 32u * k, 16, 1024),
-                   sdesc_sw128(sbase + kK + slot * kKBox + 32u * k, 16, 1024), kIdS, (bx > 0 || k > 0) ? 1u : 0u);
+            mma_ss(col, sdesc_add(q_k, bx * kQBox + 32u * k), sdesc_add(k_k, slot * kKBox + 32u * k), kIdS,
+                   (bx > 0 || k > 0) ? 1u : 0u);
         }
         tc_commit(bar(kSFull + (j & 1)));
         return true;
       };
       auto issue_dp = [&](int j) -> bool {
-        const uint32_t col = kColDP + 64u * (uint32_t)(j & 1);
+        const uint32_t col = tmem + kColDP + 64u * (uint32_t)(j & 1);
         for (int bx = 0; bx < 4; ++bx) {
           if (!mbar_wait(bar(kVFull + bx), (uint32_t)(j & 1), wc, site(9))) return false;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + col, sdesc_sw128(sbase + kDO + bx * kQBox + 32u * k, 16, 1024),
-                   sdesc_sw128(sbase + kV + bx * kKBox + 32u * k, 16, 1024), kIdS, (bx > 0 || k > 0) ? 1u : 0u);
+            mma_ss(col, sdesc_add(do_k, bx * kQBox + 32u * k), sdesc_add(v_k, bx * kKBox + 32u * k), kIdS,
+                   (bx > 0 || k > 0) ? 1u : 0u);
           tc_commit(bar(kVEmpty + bx));
         }
         tc_commit(bar(kDPFull + (j & 1)));
         return true;
       };
-      // dQ[:, 64bx .. +64) += dS_j K_j[:, 64bx .. +64): A = dS from tensor
-      // memory (keys 0-31 in the first 16 columns written by warps 0-3, keys
-      // 32-63 in those written by warps 4-7), B = the K box, MN-major.
+      // dQ += dS_j K_j: A = dS from tensor memory (keys 0-31 in the first 16
+      // columns written by warps 0-3, keys 32-63 in those written by warps
+      // 4-7), B = K_j MN-major, N = 256 over its four boxes, which sit in
+      // consecutive ring slots 4(j mod 2) .. +3.
       auto issue_dq = [&](int j) {
-        const uint32_t ds_col = kColDP + 64u * (uint32_t)(j & 1);
-        for (int bx = 0; bx < 4; ++bx) {
-          const int slot = (4 * j + bx) % kKSlots;
+        const uint32_t ds_col = tmem + kColDP + 64u * (uint32_t)(j & 1);
+        const uint32_t slot0 = (uint32_t)((4 * j) % kKSlots);
 #pragma unroll
-          for (int ks = 0; ks < kBN / 16; ++ks)
-            mma_ts(tmem + kColDQ + 64u * bx, tmem + ds_col + (uint32_t)(ks < 2 ? 8 * ks : 32 + 8 * (ks - 2)),
-                   sdesc_sw128(sbase + kK + slot * kKBox + ks * 2048, kKBox, 1024), kIdQ, (j > 0 || ks > 0) ? 1u : 0u);
-          tc_commit(bar(kKEmpty + slot));
-        }
+        for (int ks = 0; ks < kBN / 16; ++ks)
+          mma_ts(tmem + kColDQ, ds_col + (uint32_t)(ks < 2 ? 8 * ks : 32 + 8 * (ks - 2)),
+                 sdesc_add(k_mn, slot0 * kKBox + ks * 2048), kIdQ, (j > 0 || ks > 0) ? 1u : 0u);
+        for (int bx = 0; bx < 4; ++bx) tc_commit(bar(kKEmpty + slot0 + bx));
       };
       bool ok = mbar_wait(bar(kQFull), 0, wc, site(10));
       if (ok && n > 0) ok = issue_s(0) && issue_dp(0);

@@ -389,13 +389,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
           k_ready = j;
         }
         tc_fence_after();
-        const uint32_t qa = sbase + L::kQ + t * L::kTile;
-        const uint32_t kb = sbase + L::kK + (j & 1) * L::kTile;
+        const uint64_t qd = sdesc_sw128(sbase + L::kQ + t * L::kTile, 16, 1024);
+        const uint64_t kd = sdesc_sw128(sbase + L::kK + (j & 1) * L::kTile, 16, 1024);
+        const uint32_t dcol = tmem + s_col(t);
 #pragma unroll
         for (int ks = 0; ks < DR / 16; ++ks) {
           const uint32_t off = (uint32_t)((ks >> 2) * kBoxBytes + (ks & 3) * 32);
-          mma_ss(tmem + s_col(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdS,
-                 ks > 0 ? 1u : 0u);
+          mma_ss(dcol, sdesc_add(qd, off), sdesc_add(kd, off), kIdS, ks > 0 ? 1u : 0u);
         }
         tc_commit(bar(kSFull + t));
         return true;
@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
           ok = false;
           break;
         }
-        const uint32_t vb = sbase + L::kV + (j & 1) * L::kTile;
+        const uint64_t vd = sdesc_sw128(sbase + L::kV + (j & 1) * L::kTile, kBoxBytes, 1024);
         for (int t = 0; t < 2 && ok; ++t) {
           if (j >= n_t[t]) continue;
           if (!mbar_wait(bar(kPFull + t), (uint32_t)(j & 1), wc, site(9))) {
@@ -418,10 +418,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
             break;
           }
           tc_fence_after();
+          const uint32_t ocol = tmem + o_col(t), pcol = tmem + s_col(t);
 #pragma unroll
           for (int ks = 0; ks < kBN / 16; ++ks)
-            mma_ts(tmem + o_col(t), tmem + s_col(t) + (uint32_t)(8 * ks),
-                   sdesc_sw128(vb + (uint32_t)(ks * 2048), kBoxBytes, 1024), kIdO, (j > 0 || ks > 0) ? 1u : 0u);
+            mma_ts(ocol, pcol + (uint32_t)(8 * ks), sdesc_add(vd, (uint32_t)(ks * 2048)), kIdO,
+                   (j > 0 || ks > 0) ? 1u : 0u);
           if (j == n_t[t] - 1) tc_commit(bar(kOFull + t));
           if (j + 1 < n_t[t]) ok = issue_s(t, j + 1);
         }

@@ -267,6 +267,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// The descriptor of an operand `bytes` further on in shared memory: the start
+// address field holds address >> 4 in 14 bits and every shared-memory address
+// is below 2^18, so adding bytes >> 4 never carries into the next field.
+// Building a tile's descriptor once and stepping it with constant offsets
+// keeps the MMA-issuing thread's work between two MMAs to a few instructions.
+// (Measured on GB300 with a stream of independent products: rebuilding both
+// descriptors before every MMA in a dependent chain stretched an M = 128,
+// K = 16 product to ~95 cycles, against 48 / 64 / 128 cycles for N = 64 /
+// 128 / 256 when issued back to back.)
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); }
+
 // Instruction descriptor for kind::f16 with 16-bit A/B (both bf16, or both
 // f16: one MMA never mixes them) and fp32 accumulation.
 // Bits: [4,6) D format (1 = f32), [7,10) A format (0 = f16, 1 = bf16),

@@ -10,6 +10,7 @@
 #include <atomic>
 
 #include "fa.h"
+#include "fa_decode.h"
 #include "fa_kernels.h"
 
 namespace {
@@ -191,6 +192,15 @@ int forward_causal(int causal, const Shape& s) { return causal && s.Nq > 1 ? 1 :
 size_t fwd_workspace_bytes(const Shape& s, int causal, fa_dtype dtype, FwdPlan* plan) {
   causal = forward_causal(causal, s);
   if (s.empty() || causal || !is16(dtype)) return 0;
+  if (s.Nq == 1) {
+    // A decoding step: the streaming kernel's key ranges per head.
+    const int splits = fa::decode_splits((int)s.heads(), sm_count_current_device(), (int)s.Nk);
+    if (splits <= 1) return 0;
+    const size_t rows = (size_t)s.heads() * (size_t)splits;
+    const size_t opart = pad256(rows * (size_t)s.d * 4);
+    if (plan) *plan = FwdPlan{0, splits, opart};
+    return opart + pad256(rows * 4);
+  }
   const int units = fa::fwd_units((int)s.B, (int)s.H, (int)s.Nq, (int)s.d);
   int n_full, splits;
   fa::fwd_split_plan(units, sm_count_current_device(), (int)(s.nk_pad() / 128), &n_full, &splits);
@@ -225,10 +235,25 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
     return from_cuda(fa::launch_fwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
                                         static_cast<const float*>(v), static_cast<float*>(o), lse, (int)s.heads(), Nq,
                                         Nk, d, scale, causal, cs));
+  const bool f16 = dtype == FA_DTYPE_FP16;
+  if (Nq == 1) {
+    // A decoding step (the causal mask was dropped above: one query sees
+    // every key): streamed on the CUDA cores, keys split over CTAs when a
+    // workspace is given.
+    fa::DecodeArgs da{q, k, v, o, lse, (int)s.heads(), Nk, d, f16 ? 1 : 0, scale * kLog2e, 1, nullptr, nullptr};
+    FwdPlan plan;
+    const size_t need = fwd_workspace_bytes(s, causal, dtype, &plan);
+    if (need > 0 && workspace != nullptr) {
+      if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+      da.splits = plan.splits;
+      da.opart = static_cast<float*>(workspace);
+      da.lpart = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.opart_bytes);
+    }
+    return from_cuda(fa::launch_fwd_decode(da, cs));
+  }
   fa::FwdArgs a;
   const long long heads = s.heads();
   const bool rv = s.rows_view();
-  const bool f16 = dtype == FA_DTYPE_FP16;
   if (!encode_bf16_heads(&a.tm_q, q, heads, Nq, d, 128, rv, f16) ||
       !encode_bf16_heads(&a.tm_k, k, heads, Nk, d, 128, rv, f16) ||
       !encode_bf16_heads(&a.tm_v, v, heads, Nk, d, 128, rv, f16))

@@ -120,6 +120,12 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
  * positions (see "causal" above): e.g. a decode step is Nq = 1 over the Nk
  * cached keys plus itself, and prefix caching runs the new tokens' queries
  * over all keys.
+ * Nq = 1 with a 16-bit dtype (a decoding step; the causal flag changes
+ * nothing there, the one query sees every key) runs a streaming kernel that
+ * reads K and V once with 16-byte loads on the CUDA cores: the step is bound
+ * by HBM bandwidth.  With the workspace each head's keys are cut into ranges
+ * (about four CTAs per SM, ≥ 256 keys each) merged as above; with NULL one
+ * CTA per head does all of its keys.
  */
 size_t fa_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int causal, fa_dtype dtype);
 fa_status fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,

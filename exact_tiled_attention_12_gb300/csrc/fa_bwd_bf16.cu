@@ -355,9 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
     const uint32_t lane_off = (uint32_t)(g * 32) << 16;
     // Pacing of the reductions issued after the columns are released: they
     // run beside the next dPᵀ product and the compute warps' next tile, and
-    // issued in one burst they slow both (measured on GB300: +7 % for the
+    // issued in one burst they slow both (measured on GB300: +8 % for the
     // whole backward when spread).  Each thread sleeps between groups of 8
-    // so that its 64 reductions span about half of the previous step, as
+    // so that its 64 reductions span about a third of the previous step, as
     // timed between its own dQ hand-overs (no pause on the first step).
     uint32_t t_prev = 0;
     uint32_t pause_ns = 0;
@@ -367,12 +367,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       ok = __all_sync(kFull, ok);
       if (!ok) break;
       {
-        // step / 2 spread over 8 pauses; clock cycles read as ns at ~2 GHz
-        // (32-bit clock: the unsigned difference survives a wrap)
+        // 7 pauses of step / 40 (cycles read as ns at ~2 GHz: about a third
+        // of the step).  Pauses feed back into the step they are measured
+        // on: on GB300 step / 25 already ran away (the backward 15 % slower,
+        // step / 20 35 %), so the pause stays well short of that and is
+        // capped.  32-bit clock: the unsigned difference survives a wrap.
         const uint32_t t_now = (uint32_t)clock();
         if (i > 0) {
-          const uint32_t p = (t_now - t_prev) / 32u;
-          pause_ns = p < 300u ? p : 300u;
+          const uint32_t p = (t_now - t_prev) / 40u;
+          pause_ns = p < 200u ? p : 200u;
         }
         t_prev = t_now;
       }

@@ -240,7 +240,9 @@ def run_ours(args, w, rank, world):
     # the uploads, the attention calls and the downloads on three streams, so
     # step i's compute overlaps step i+1's upload and step i-1's download.
     # The timed region runs from the first upload to the last download.
-    n_e2e = 0 if args.no_e2e else max(3, min(args.steps, 10))
+    # 30 steps (fewer if --steps is smaller): the first upload and the last
+    # download, which nothing overlaps, then weigh 1/30 of the region.
+    n_e2e = 0 if args.no_e2e else max(3, min(args.steps, 30))
     elem_bytes = q.numel() * q.element_size()
     e2e = None
     if n_e2e:

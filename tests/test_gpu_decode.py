@@ -1,4 +1,5 @@
-"""GPU parity of the decoding step (one query per head over Nk keys).
+"""GPU parity of the decoding step (one query per head over Nk keys), and of
+a few queries per head over a long cache.
 
 A single query runs a streaming kernel on the CUDA cores (the step is bound
 by reading K and V, not by arithmetic), its keys split over several CTAs when
@@ -7,6 +8,8 @@ dimension, bf16 and fp16, key counts from 1 to tens of thousands (ragged
 against every split), with and without the workspace (one CTA per head),
 the causal flag (one query sees every key), large scores, and the state a
 decoding loop keeps (each step's O and LSE merged with the next chunk's).
+Two to five queries per head (e.g. checking draft tokens; under the mask
+the last positions) run the tensor-core forward.
 """
 
 import numpy as np
@@ -115,3 +118,40 @@ def test_decode_loop_keeps_running_state():
             o, lse = fa.merge([o, oc], [lse, lc])
     assert fa.sync_status() == 0
     _check(o, lse, *_oracle(q, k, v, d ** -0.5))
+
+
+@pytest.mark.parametrize("d", [64, 96, 128])
+@pytest.mark.parametrize("Nq", [2, 3, 4])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nk", [4, 300, 9000])
+def test_decode_few_queries(d, Nq, causal, Nk):
+    """Two to four queries per head (e.g. checking draft tokens); under the
+    mask they are the last Nq positions."""
+    import exact_tiled_attention_12_gb300 as fa
+
+    B, H = 2, 3
+    q, k, v, _ = make_inputs_kv(B, H, Nq, Nk, d, "bf16", "normal", 700 + d + Nq + Nk, device="cuda")
+    o, lse = fa.fwd(q, k, v, causal=causal)
+    assert fa.sync_status() == 0
+    _check(o, lse, *_oracle(q, k, v, d ** -0.5, causal))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_decode_few_queries_without_workspace_and_equal_lengths(dtype):
+    import exact_tiled_attention_12_gb300 as fa
+
+    for Nq, Nk in ((4, 4), (3, 3), (4, 5000)):
+        q, k, v, _ = make_inputs_kv(1, 2, Nq, Nk, 128, dtype, "normal", 17 + Nk, device="cuda")
+        for ws in (None, False):
+            o, lse = fa.fwd(q, k, v, causal=True, workspace=ws)
+            assert fa.sync_status() == 0
+            _check(o, lse, *_oracle(q, k, v, 128 ** -0.5, True))
+
+
+def test_five_queries():
+    import exact_tiled_attention_12_gb300 as fa
+
+    q, k, v, _ = make_inputs_kv(1, 2, 5, 3000, 128, "bf16", "normal", 23, device="cuda")
+    o, lse = fa.fwd(q, k, v, causal=True)
+    assert fa.sync_status() == 0
+    _check(o, lse, *_oracle(q, k, v, 128 ** -0.5, True))

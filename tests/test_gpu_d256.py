@@ -126,3 +126,19 @@ def test_d256_more_queries_than_keys_without_mask(dtype):
     gpu = {"O": to64(o), "LSE": to64(lse), "dQ": to64(dq), "dK": to64(dk), "dV": to64(dv)}
     ref = run_oracle_heads(q, k, v, do, False, d ** -0.5, _heads(B, H))
     compare(_flat(gpu), ref, "bf16")
+
+
+def test_d256_autograd():
+    """attention() at d = 256: gradients through .backward() against the oracle."""
+    import exact_tiled_attention_12_gb300 as fa
+
+    B, H, Nq, Nk, d = 1, 2, 150, 420, 256
+    q, k, v, do = make_inputs_kv(B, H, Nq, Nk, d, "bf16", "normal", 81, device="cuda")
+    q, k, v = (t.clone().requires_grad_(True) for t in (q, k, v))
+    o = fa.attention(q, k, v, causal=True)
+    o.backward(do)
+    assert fa.sync_status() == 0
+    ref = run_oracle_heads(q.detach(), k.detach(), v.detach(), do, True, d ** -0.5, _heads(B, H))
+    gpu = {"O": to64(o.detach()[0]), "LSE": ref["LSE"], "dQ": to64(q.grad[0]), "dK": to64(k.grad[0]),
+           "dV": to64(v.grad[0])}
+    compare(gpu, ref, "bf16")

@@ -54,6 +54,7 @@ def _noalloc(fa, q, k, v, o, do, lse, causal):
 @pytest.mark.parametrize("dtype,shape,causal", [
     ("bf16", (1, 2, 512, 128), True),
     ("bf16", (2, 2, 384, 64), False),
+    ("bf16", (1, 2, 300, 256), True),   # d = 256: dQ from its own kernel, no accumulator in the scratch
     ("fp32", (1, 2, 200, 64), True),
 ])
 def test_noalloc_matches_fa_bwd_twice(fa, dtype, shape, causal):

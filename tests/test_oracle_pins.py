@@ -16,8 +16,10 @@ import numpy as np
 import pytest
 
 from oracle import (
+    attention_backward,
     attention_backward_head,
     attention_backward_rows,
+    attention_forward,
     attention_forward_head,
     attention_forward_rows,
     causal_mask,
@@ -558,3 +560,98 @@ def test_merge_partials_two_parts_closed_form():
     wa = math.exp(a) / (math.exp(a) + math.exp(b))
     np.testing.assert_allclose(om, wa * o_a + (1 - wa) * o_b, atol=1e-15, rtol=0)
     assert abs(lsem[0] - math.log(math.exp(a) + math.exp(b))) <= 1e-15
+
+
+# ---------------------------------------------------------------- batched wrappers over [B, H, N, d]
+#
+# "1.FlashAttention 整体结构" 一 states attention per head; a [B, H, N, d] call is
+# that definition applied to every (batch, head) slice independently.  Each head
+# below gets its own values, so a swapped b/h index, a slice written to the
+# wrong head or an output slot left unfilled fails one of these.
+
+_BATCH_SHAPE = (2, 3, 9, 4)   # B, H, N, d: six heads that differ
+
+
+def _distinct_heads(seed):
+    rng = _rng(seed)
+    B, H, n, d = _BATCH_SHAPE
+    q, k, v, do = (rng.normal(size=_BATCH_SHAPE) for _ in range(4))
+    # scale every head differently so that no two heads can stand in for each other
+    for b in range(B):
+        for h in range(H):
+            f = 1.0 + 0.25 * (H * b + h)
+            q[b, h] *= f
+            v[b, h] += 3.0 * (H * b + h)
+            do[b, h] -= 2.0 * (H * b + h)
+    return q, k, v, do
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_batched_wrappers_equal_the_per_head_definition(causal):
+    """Every [b, h] slice of the batched result is the per-head result of that slice, bit for bit."""
+    q, k, v, do = _distinct_heads(40)
+    scale = _BATCH_SHAPE[3] ** -0.5
+    o, lse = attention_forward(q, k, v, scale, causal)
+    dq, dk, dv = attention_backward(q, k, v, do, scale, causal)
+    assert o.shape == q.shape and lse.shape == q.shape[:3]
+    assert dq.shape == q.shape and dk.shape == k.shape and dv.shape == v.shape
+    for b in range(_BATCH_SHAPE[0]):
+        for h in range(_BATCH_SHAPE[1]):
+            ro, rl = attention_forward_head(q[b, h], k[b, h], v[b, h], scale, causal)
+            rdq, rdk, rdv = attention_backward_head(q[b, h], k[b, h], v[b, h], do[b, h], scale, causal)
+            assert np.array_equal(o[b, h], ro) and np.array_equal(lse[b, h], rl)
+            assert np.array_equal(dq[b, h], rdq) and np.array_equal(dk[b, h], rdk) and np.array_equal(dv[b, h], rdv)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_batched_constant_v_per_head(causal):
+    """V[b, h, j] = c_bh for every key gives O[b, h, i] = c_bh (rows of P sum to one),
+    with a different constant vector in each head."""
+    q, k, _, _ = _distinct_heads(41)
+    B, H, n, d = _BATCH_SHAPE
+    c = np.arange(B * H * d, dtype=np.float64).reshape(B, H, 1, d) * 0.37 - 5.0
+    v = np.broadcast_to(c, (B, H, n, d)).copy()
+    o, _ = attention_forward(q, k, v, d ** -0.5, causal)
+    assert np.max(np.abs(o - c)) <= 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_batched_identical_keys_per_head(causal):
+    """K[b, h, j] = k_bh for every key makes P uniform over the visible keys of that
+    head: O is the (running, under the mask) mean of that head's V, LSE is
+    scale·q·k_bh + ln(count), dQ = 0 (Σ_j dS_ij = 0 and every key is the same),
+    and without the mask dV[b, h, j] = mean_i dO[b, h, i] for every key."""
+    q, _, v, do = _distinct_heads(42)
+    B, H, n, d = _BATCH_SHAPE
+    rng = _rng(43)
+    kvec = rng.normal(size=(B, H, 1, d))
+    k = np.broadcast_to(kvec, (B, H, n, d)).copy()
+    scale = d ** -0.5
+    o, lse = attention_forward(q, k, v, scale, causal)
+    dq, dk, dv = attention_backward(q, k, v, do, scale, causal)
+    count = np.arange(1, n + 1) if causal else np.full(n, n)
+    for b in range(B):
+        for h in range(H):
+            if causal:
+                want = np.cumsum(v[b, h], axis=0) / count[:, None]
+            else:
+                want = np.tile(v[b, h].mean(axis=0), (n, 1))
+            assert np.max(np.abs(o[b, h] - want)) <= 1e-12
+            s = scale * (q[b, h] @ kvec[b, h, 0])
+            np.testing.assert_allclose(lse[b, h], s + np.log(count), atol=1e-12, rtol=0)
+            assert np.max(np.abs(dq[b, h])) <= 1e-12
+            if not causal:
+                np.testing.assert_allclose(dv[b, h], np.tile(do[b, h].mean(axis=0), (n, 1)), atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_batched_gradient_invariants_per_head(causal):
+    """Per head: Σ_j dV_j = Σ_i dO_i (rows of P sum to one) and Σ_j dK_j = 0; each
+    head's dO is shifted differently, so dV's column sums identify the head."""
+    q, k, v, do = _distinct_heads(44)
+    B, H, n, d = _BATCH_SHAPE
+    dq, dk, dv = attention_backward(q, k, v, do, d ** -0.5, causal)
+    for b in range(B):
+        for h in range(H):
+            np.testing.assert_allclose(dv[b, h].sum(axis=0), do[b, h].sum(axis=0), atol=1e-10, rtol=0)
+            assert np.max(np.abs(dk[b, h].sum(axis=0))) <= 1e-10

@@ -18,19 +18,25 @@ namespace {
 // One fault word per device; kernels record the first timed-out wait here.
 __device__ unsigned int g_fault_word;
 
-constexpr int kMaxDevices = 64;
-std::atomic<unsigned int*> g_fault_ptr[kMaxDevices];
+void* lookup_fault_word() {
+  void* addr = nullptr;
+  return cudaGetSymbolAddress(&addr, g_fault_word) == cudaSuccess ? addr : nullptr;
+}
+
+fa::SymbolCache g_fault_cache;
 
 unsigned int* fault_word_for_current_device() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  unsigned int* p = g_fault_ptr[dev].load(std::memory_order_acquire);
-  if (p) return p;
-  void* addr = nullptr;
-  if (cudaGetSymbolAddress(&addr, g_fault_word) != cudaSuccess) return nullptr;
-  p = static_cast<unsigned int*>(addr);
-  g_fault_ptr[dev].store(p, std::memory_order_release);
-  return p;
+  return static_cast<unsigned int*>(fa::cached_symbol_address(g_fault_cache, lookup_fault_word));
+}
+
+template <class PFN>
+PFN driver_entry(const char* name, int version) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<PFN>(p);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -168,9 +174,9 @@ inline fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA
 
 // SM count of the current device (0 if it cannot be queried), cached per device.
 int sm_count_current_device() {
-  static std::atomic<int> cache[kMaxDevices];
+  static std::atomic<int> cache[fa::kMaxDevices];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= fa::kMaxDevices) return 0;
   int n = cache[dev].load(std::memory_order_relaxed);
   if (n > 0) return n;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
@@ -396,6 +402,41 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, c
 }
 
 }  // namespace
+
+namespace fa {
+
+unsigned long long current_context_id() {
+  static const auto get_current = driver_entry<PFN_cuCtxGetCurrent_v4000>("cuCtxGetCurrent", 4000);
+  static const auto get_id = driver_entry<PFN_cuCtxGetId_v12000>("cuCtxGetId", 12000);
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+void* cached_symbol_address(SymbolCache& cache, void* (*lookup)()) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(cache.mu);
+  const unsigned long long id = current_context_id();
+  if (id != 0 && cache.ctx[dev] == id && cache.ptr[dev] != nullptr) return cache.ptr[dev];
+  // The lookup makes the device's primary context current if none was yet.
+  void* p = lookup();
+  if (p == nullptr) {
+    cudaGetLastError();   // leave no stale error for the next launch to report as its own
+    return nullptr;
+  }
+  cache.ctx[dev] = current_context_id();
+  cache.ptr[dev] = p;
+  return p;
+}
+
+}  // namespace fa
 
 extern "C" {
 

@@ -8,7 +8,31 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace fa {
+
+// ---------------------------------------------------------------- device addresses of library arrays
+
+// A device address that cudaGetSymbolAddress returns belongs to the context
+// that was current: after cudaDeviceReset (or any teardown of the primary
+// context) the next context loads the module again and the array may sit
+// elsewhere.  So a cached address is kept together with the id of the context
+// it was looked up in, per device, and looked up again when that id changes.
+constexpr int kMaxDevices = 64;
+struct SymbolCache {
+  std::mutex mu;
+  unsigned long long ctx[kMaxDevices] = {};
+  void* ptr[kMaxDevices] = {};
+};
+// Id of the context current on the calling thread (cuCtxGetId), 0 if there is
+// none yet or it cannot be queried.
+unsigned long long current_context_id();
+// The address cached for the current device and context, or the result of
+// `lookup` (a function in the array's own translation unit that calls
+// cudaGetSymbolAddress on it), cached.  Returns null, with the runtime's
+// last error cleared, if the lookup fails.
+void* cached_symbol_address(SymbolCache& cache, void* (*lookup)());
 
 // ---------------------------------------------------------------- bf16 tensor-core path
 

@@ -14,10 +14,10 @@
 // process exits.  Host code cannot use the array's name as a device address
 // (on the host it names a shadow object), so the first call on each device
 // asks the runtime for the device address with cudaGetSymbolAddress, with that
-// device current, and caches it.  That first call should therefore come before
-// any stream capture starts.  No call here allocates memory.
-#include <atomic>
-
+// device current, and caches it together with the id of the context it was
+// looked up in (after cudaDeviceReset the array is looked up again).  That
+// first call should therefore come before any stream capture starts.  No call
+// here allocates memory.
 #include "fa.h"
 #include "fa_kernels.h"
 
@@ -25,19 +25,13 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_ptr[kMaxDevices];
-
-// Device address of the scratch array on the current device (set-up on first use).
-void* scratch_for_current_device() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
-  if (p) return p;
-  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return nullptr;
-  g_scratch_ptr[dev].store(p, std::memory_order_release);
-  return p;
+// Device address of the scratch array in the current context.
+void* lookup_scratch() {
+  void* p = nullptr;
+  return cudaGetSymbolAddress(&p, g_noalloc_scratch) == cudaSuccess ? p : nullptr;
 }
+
+fa::SymbolCache g_scratch_cache;
 
 }  // namespace
 
@@ -48,7 +42,7 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   if (need > (size_t)FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;   // problem larger than the built-in scratch
   if (need == 0)   // empty or invalid: fa_bwd returns the same status it would with any workspace
     return fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, dtype, nullptr, 0, stream);
-  void* scratch = scratch_for_current_device();
+  void* scratch = fa::cached_symbol_address(g_scratch_cache, lookup_scratch);
   if (scratch == nullptr) return FA_ERR_CUDA;
   // fa_bwd's pre-pass overwrites D and the LSE copy and zeroes the dQ
   // accumulator, so whatever an earlier call left in the array is harmless.

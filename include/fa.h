@@ -264,8 +264,10 @@ fa_status fa_selftest_wait_timeout(fa_stream_t stream);
  *     bf16 that is 4·B·H·Np·(d + 2) bytes plus padding, e.g. B·H·Np up to
  *     about 64,000 rows at d = 128);
  *   - the first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current and caches it; make
- *     that first call before any stream capture begins;
+ *     (cudaGetSymbolAddress) with that device current and caches it with the
+ *     id of the current context (a call after cudaDeviceReset, in a new
+ *     context, looks it up again); make that first call before any stream
+ *     capture begins;
  *   - every call on a device shares the one array and it keeps the last
  *     call's contents (the pre-pass rewrites what must start at zero), so
  *     calls whose work can overlap on the GPU — on different streams, or from

@@ -143,3 +143,45 @@ def test_merge_argument_checks(L):
     assert merge(N=0) == 0 and merge(B=0) == 0
     null = (ctypes.c_void_p * 2)(0x10000, 0)
     assert merge(lparts=ctypes.cast(null, ctypes.c_void_p)) == 1
+
+
+# ---------------------------------------------------------------- build key
+
+
+def test_build_key_rejects_a_library_built_for_another_cpu(tmp_path, monkeypatch):
+    """A libfa.so whose ELF machine is not this host's is rebuilt, not loaded,
+    and so is one whose recorded key (sources, flags, arch, host) differs."""
+    import json
+    import platform
+
+    import exact_tiled_attention_12_gb300.build as b
+
+    lib, key = tmp_path / "libfa.so", tmp_path / "libfa.key"
+    monkeypatch.setattr(b, "LIB", str(lib))
+    monkeypatch.setattr(b, "KEY", str(key))
+    assert b._stale()                                          # nothing built
+    mine = b._ELF_MACHINE.get(platform.machine())
+    if mine is None:
+        pytest.skip("unknown host machine")
+    other = 183 if mine == 62 else 62
+
+    def elf(machine):
+        head = bytearray(64)
+        head[:4] = b"\x7fELF"
+        head[4], head[5] = 2, 1                                # 64-bit, little endian
+        head[18:20] = machine.to_bytes(2, "little")
+        return bytes(head)
+
+    lib.write_bytes(elf(mine))
+    key.write_text(json.dumps(b.build_key()))
+    assert b.elf_machine(str(lib)) == mine
+    assert not b._stale()                                      # same host, same key
+    lib.write_bytes(elf(other))
+    assert b._stale()                                          # foreign CPU architecture
+    lib.write_bytes(elf(mine))
+    k = b.build_key()
+    k["flags"] = k["flags"] + ["-G"]
+    key.write_text(json.dumps(k))
+    assert b._stale()                                          # other compiler flags
+    key.write_text("not json")
+    assert b._stale()

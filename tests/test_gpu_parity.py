@@ -229,3 +229,50 @@ def test_autograd_attention_matches_oracle(dtype, causal):
     gpu = {"O": to64(o.detach()[0]), "LSE": ref["LSE"], "dQ": to64(q.grad[0]), "dK": to64(k.grad[0]),
            "dV": to64(v.grad[0])}
     compare(gpu, ref, dtype)
+
+
+# ------------------------------------------------------------------ the square entry points, called directly
+
+_DT = {"bf16": 0, "fp32": 1, "fp16": 2}
+
+
+@pytest.mark.parametrize("dtype,B,H,N,d,causal", [
+    ("bf16", 1, 2, 512, 128, False),
+    ("bf16", 2, 1, 384, 64, True),
+    ("bf16", 1, 2, 300, 128, True),     # ragged N through the square symbols
+    ("fp16", 1, 1, 256, 128, False),
+    ("fp32", 1, 2, 96, 64, True),
+])
+def test_square_entry_points_fa_fwd_fa_bwd(dtype, B, H, N, d, causal):
+    """fa_fwd and fa_bwd (the square C-ABI symbols, not the Nq/Nk ones the
+    binding uses) called through ctypes with caller-owned outputs and
+    workspaces, compared with the oracle on every head."""
+    import ctypes
+
+    import exact_tiled_attention_12_gb300 as fa
+
+    L = fa.lib()
+    q, k, v, do = make_inputs(B, H, N, d, dtype, "normal", 70 + N, device="cuda")
+    scale = d ** -0.5
+    code = _DT[dtype]
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    sp = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    fws_n = L.fa_fwd_workspace_size(B, H, N, d, int(causal), code)
+    fws = torch.empty(max(fws_n, 1), dtype=torch.uint8, device="cuda")
+    st = L.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, int(causal), code,
+                  P(fws) if fws_n else None, fws_n, sp)
+    assert st == 0, fa.status_string(st)
+    bws_n = L.fa_bwd_workspace_size(B, H, N, d, code)
+    bws = torch.empty(max(bws_n, 1), dtype=torch.uint8, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    st = L.fa_bwd(P(q), P(k), P(v), P(o), P(do), P(lse), P(dq), P(dk), P(dv), B, H, N, d, scale, int(causal), code,
+                  P(bws), bws_n, sp)
+    assert st == 0, fa.status_string(st)
+    assert L.fa_sync_status(sp) == 0
+    gpu = {"O": to64(o), "LSE": to64(lse), "dQ": to64(dq), "dK": to64(dk), "dV": to64(dv)}
+    heads = _all_heads(B, H)
+    ref = run_oracle_heads(q, k, v, do, causal, scale, heads)
+    flat = {key: val.reshape((-1,) + val.shape[2:]) for key, val in gpu.items()}
+    compare(flat, ref, "fp32" if dtype == "fp32" else "bf16")

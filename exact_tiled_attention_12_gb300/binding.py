@@ -8,6 +8,7 @@ If libfa.so is missing the calls raise: there is no fallback.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -22,7 +23,7 @@ FA_DTYPE_FP16 = 2
 _CODES = {torch.bfloat16: FA_DTYPE_BF16, torch.float32: FA_DTYPE_FP32, torch.float16: FA_DTYPE_FP16}
 _STATUS = {
     0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_MISALIGNED",
-    4: "FA_ERR_WORKSPACE", 5: "FA_ERR_CUDA", 6: "FA_ERR_TIMEOUT",
+    4: "FA_ERR_WORKSPACE", 5: "FA_ERR_CUDA", 6: "FA_ERR_TIMEOUT", 7: "FA_ERR_BOUNDS",
 }
 # Every function include/fa.h declares, with (restype, argtypes).
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -44,7 +45,10 @@ SIGNATURES = {
     "fa_bwd_kv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _Z, _P]),
     "fa_merge": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P]),
     "fa_selftest_wait_timeout": (_I, [_P]),
+    "fa_debug_checks_enabled": (_I, []),
+    "fa_selftest_bounds_check": (_I, [_P, _P]),
 }
+FA_SELFTEST_BOUNDS_CASES = 8
 MERGE_MAX_PARTS = 16
 
 
@@ -60,21 +64,54 @@ def library_path() -> str:
     return os.path.join(_HERE, "libfa.so")
 
 
+def _load(path):
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    handle = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
+
+
 def lib():
     """Loads libfa.so once (raises if it has not been built)."""
     global _LIB
     if _LIB is None:
-        path = library_path()
-        if not os.path.exists(path):
-            raise RuntimeError(
-                f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
-        handle = ctypes.CDLL(path)
-        for name, (res, args) in SIGNATURES.items():
-            fn = getattr(handle, name)
-            fn.restype = res
-            fn.argtypes = args
-        _LIB = handle
+        _LIB = _load(library_path())
     return _LIB
+
+
+_DEBUG_LIB = None
+
+
+def debug_library_path() -> str:
+    return os.path.join(_HERE, "libfa_debug.so")
+
+
+def debug_lib():
+    """Loads libfa_debug.so once: the same entry points with device-side bounds
+    and alignment checks compiled into the kernels (raises if not built)."""
+    global _DEBUG_LIB
+    if _DEBUG_LIB is None:
+        _DEBUG_LIB = _load(debug_library_path())
+    return _DEBUG_LIB
+
+
+@contextlib.contextmanager
+def debug_checks():
+    """Within the block, every call of this module runs the debug build
+    (libfa_debug.so); a failed device-side check then shows up as
+    FA_ERR_BOUNDS from sync_status().  Not thread-safe: it swaps the library
+    handle this module uses."""
+    global _LIB
+    saved = lib()
+    _LIB = debug_lib()
+    try:
+        yield
+    finally:
+        _LIB = saved
 
 
 def status_string(code: int) -> str:

@@ -10,6 +10,7 @@
 #include <atomic>
 
 #include "fa.h"
+#include "fa_checks.h"
 #include "fa_decode.h"
 #include "fa_kernels.h"
 
@@ -449,6 +450,7 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing, misaligned (256 B) or too small";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call or kernel launch failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel abandoned a pipeline wait";
+    case FA_ERR_BOUNDS: return "FA_ERR_BOUNDS: a device-side bounds or alignment check failed (debug build)";
   }
   return "unknown fa_status";
 }
@@ -564,9 +566,19 @@ fa_status fa_sync_status(fa_stream_t stream) {
   if (word != 0) {
     const unsigned int zero = 0;
     if (cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
-    return FA_ERR_TIMEOUT;
+    return fa::is_check_code(word) ? FA_ERR_BOUNDS : FA_ERR_TIMEOUT;
   }
   return FA_OK;
+}
+
+int fa_debug_checks_enabled(void) { return fa::kDebugChecks ? 1 : 0; }
+
+fa_status fa_selftest_bounds_check(int* results, fa_stream_t stream) {
+  if (!fa::kDebugChecks) return FA_ERR_UNSUPPORTED;
+  if (results == nullptr) return FA_ERR_INVALID_ARG;
+  unsigned int* fault = fault_word_for_current_device();
+  if (!fault) return FA_ERR_CUDA;
+  return from_cuda(fa::launch_bounds_check_selftest(fault, results, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

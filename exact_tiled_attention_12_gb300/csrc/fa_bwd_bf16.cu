@@ -62,16 +62,19 @@ constexpr int kPolyEvery = 0;
 
 template <int D>
 struct BwdCfg {
+  // Stages of the Q / dO / LSE / D ring (measured on GB300: four stages at
+  // d = 64, where shared memory has room for them, were slower than two).
+  static constexpr int kQS = 2;
   // shared memory (offsets from a 1024-byte aligned base)
   static constexpr int kTile = 128 * D * 2;        // one 128 × D bf16 tile (D/64 boxes)
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTile;
-  static constexpr int kQ = kV + kTile;            // 2 stages
-  static constexpr int kDO = kQ + 2 * kTile;       // 2 stages
-  static constexpr int kDS = kDO + 2 * kTile;      // dSᵀ [128 keys][128 queries] bf16: 2 boxes
-  static constexpr int kLSE = kDS + 2 * kBox;      // 2 stages of 128 floats
-  static constexpr int kDV = kLSE + 2 * kBM * 4;   // 2 stages of 128 floats
-  static constexpr int kBar = kDV + 2 * kBM * 4;
+  static constexpr int kQ = kV + kTile;            // kQS stages
+  static constexpr int kDO = kQ + kQS * kTile;     // kQS stages
+  static constexpr int kDS = kDO + kQS * kTile;    // dSᵀ [128 keys][128 queries] bf16: 2 boxes
+  static constexpr int kLSE = kDS + 2 * kBox;      // kQS stages of 128 floats
+  static constexpr int kDV = kLSE + kQS * kBM * 4; // kQS stages of 128 floats
+  static constexpr int kBar = kDV + kQS * kBM * 4;
   static constexpr int kBytes = kBar + 256;
   // tensor memory columns
   static constexpr uint32_t kColDV = 0;
@@ -80,18 +83,21 @@ struct BwdCfg {
   static constexpr uint32_t kColDP = 2 * D + 128;
 };
 
-enum BwdBar : int {
-  kKVFull = 0,
-  kQFull = 1,      // +stage
-  kQEmpty = 3,     // +stage
-  kSFull = 5,
-  kDPFull = 6,
-  kPdsFull = 7,
-  kDqFull = 8,
-  kDqDrained = 9,
-  kDKVFull = 10,
-  kMmaDone = 11,
-  kNumBars = 12,
+// Barrier slots (8 bytes each) inside the barrier block.
+template <int QS>
+struct BwdBars {
+  static constexpr int kKVFull = 0;
+  static constexpr int kQFull = 1;             // +stage
+  static constexpr int kQEmpty = 1 + QS;       // +stage
+  static constexpr int kSFull = 1 + 2 * QS;
+  static constexpr int kDPFull = kSFull + 1;
+  static constexpr int kPdsFull = kSFull + 2;
+  static constexpr int kDqFull = kSFull + 3;
+  static constexpr int kDqDrained = kSFull + 4;
+  static constexpr int kDKVFull = kSFull + 5;
+  static constexpr int kMmaDone = kSFull + 6;
+  static constexpr int kNumBars = kSFull + 7;
+  static_assert(8 * kNumBars + 8 <= 256, "barrier block too small");
 };
 
 __device__ __forceinline__ uint32_t site(int s) { return 0x0200u | (uint32_t)s; }
@@ -150,6 +156,12 @@ template <int DR, bool CAUSAL, bool RAGGED, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_constant__ BwdArgs a) {
   constexpr int D = DR <= 64 ? 64 : 128;
   using C = BwdCfg<D>;
+  constexpr int QS = C::kQS;
+  using Bar = BwdBars<QS>;
+  constexpr int kKVFull = Bar::kKVFull, kQFull = Bar::kQFull, kQEmpty = Bar::kQEmpty, kSFull = Bar::kSFull,
+                kDPFull = Bar::kDPFull, kPdsFull = Bar::kPdsFull, kDqFull = Bar::kDqFull,
+                kDqDrained = Bar::kDqDrained, kDKVFull = Bar::kDKVFull, kMmaDone = Bar::kMmaDone,
+                kNumBars = Bar::kNumBars;
   // Dynamic shared memory starts on a 1024-byte boundary (no static shared
   // memory is declared); 128-byte swizzled tiles need that alignment.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -183,17 +195,43 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
   // reaches keys up to 128i + 127 + off, so i ≥ ⌊(kv0 − off) / 128⌋ (kBM == kBN).
   const int i0 = CAUSAL ? (kv0 > off ? (kv0 - off) / kBM : 0) : 0;
   // Loads rows [pos, pos + 128) of this head from a map over heads of `nrows` rows.
+  // A debug build checks the destination and the coordinates first and, if a
+  // check fails, completes the box's bytes on the barrier without copying.
   auto load_rows = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar_addr, int x, int pos, int nrows) {
+    bool chk = dcheck(smem_ok(dst - sbase, kBox, (uint32_t)C::kBar, 1024), wc, kChkSmem, 16) &&
+               dcheck(tma_x_ok(x, 64, D), wc, kChkTmaX, 16);
+    if constexpr (RAGGED)
+      chk = chk && dcheck(tma_head_ok(pos, nrows, bh, a.B * a.H), wc, kChkTmaRows, 16);
+    else
+      chk = chk && dcheck(tma_rows_ok((long long)bh * nrows + pos, 128, (long long)a.B * a.H * nrows), wc,
+                          kChkTmaRows, 16);
+    if (!chk) {
+      mbar_complete_tx(bar_addr, kBox);
+      return;
+    }
     if constexpr (RAGGED)
       tma_load_3d(dst, map, bar_addr, x, pos, bh);
     else
       tma_load_2d(dst, map, bar_addr, x, bh * nrows + pos);
   };
+  // Bulk copy of `bytes` of a workspace row array; checked like the tile loads.
+  auto load_bulk = [&](uint32_t dst, const float* src, uint32_t bytes, uint32_t bar_addr) {
+    if (!dcheck(smem_ok(dst - sbase, bytes, (uint32_t)C::kBar, 16) &&
+                    bulk_ok(reinterpret_cast<uint64_t>(src), dst, bytes), wc, kChkBulk, 17)) {
+      mbar_complete_tx(bar_addr, bytes);
+      return;
+    }
+    bulk_load(dst, src, bytes, bar_addr);
+  };
   const int n = n_tiles - i0;                // query tiles visited
+  // Step i works on query tile qtile(i).  (Measured on GB300: starting each
+  // CTA of a head at its own query tile, so that concurrent CTAs add into
+  // different dQ rows, was slower than all walking the tiles in order.)
+  auto qtile = [&](int i) -> int { return i0 + i; };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kKVFull), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < QS; ++s) {
       mbar_init(bar(kQFull + s), 1);
       mbar_init(bar(kQEmpty + s), 1 + 32 * kComputeWarps);
     }
@@ -236,11 +274,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
     const uint32_t ds_tile = sbase + C::kDS;
     bool ok = true;
     for (int i = 0; i < n; ++i) {
-      const int st = i & 1;
+      const int st = i % QS;
       const uint32_t par = (uint32_t)(i & 1);
-      const int q0 = (i0 + i) * kBM;
+      const int q0 = qtile(i) * kBM;
       ok = mbar_wait_inl(bar(kSFull), par, wc, site(1)) &&
-           mbar_wait_inl(bar(kQFull + st), (uint32_t)((i >> 1) & 1), wc, site(3));
+           mbar_wait_inl(bar(kQFull + st), (uint32_t)((i / QS) & 1), wc, site(3));
       ok = __all_sync(kFull, ok);
       // The pre-pass stored −LSE·log2(e) and −D, so each pair of columns is
       // one packed FMA (the exponent) and one packed add/multiply (dS).
@@ -259,7 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         for (int ch = 0; ch < 2; ++ch) {
           const int c0 = h * 64 + ch * 32;
           uint32_t s[32];
-          tmem_ld_x32(tmem + lane_off + C::kColS + (uint32_t)c0, s);
+          if (dcheck(tmem_ok(C::kColS + c0, 32, 512), wc, kChkTmem, 18))
+            tmem_ld_x32(tmem + lane_off + C::kColS + (uint32_t)c0, s);
           if (masked)
             p_chunk<true, kPolyEvery>(s, sl2x2, nlse + (c0 >> 1), r - c0 - delta, p + ch * 16);
           else if (ragged_cta)
@@ -285,13 +324,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
           f2_unpack(p[half * 16 + e], a0, a1);
           pk[e] = pack2<F16>(a0, a1);
         }
-        tmem_st_x16(tmem + lane_off + C::kColS + (uint32_t)(h * 32 + 16 * half), pk);
+        if (dcheck(tmem_ok(C::kColS + h * 32 + 16 * half, 16, 512), wc, kChkTmem, 19))
+          tmem_st_x16(tmem + lane_off + C::kColS + (uint32_t)(h * 32 + 16 * half), pk);
       }
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int c0 = h * 64 + ch * 32;
         uint32_t dp[32];
-        tmem_ld_x32(tmem + lane_off + C::kColDP + (uint32_t)c0, dp);
+        if (dcheck(tmem_ok(C::kColDP + c0, 32, 512), wc, kChkTmem, 20))
+          tmem_ld_x32(tmem + lane_off + C::kColDP + (uint32_t)c0, dp);
         uint32_t dk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -303,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         // 32 query columns = four 16-byte chunks of this key row, in box h
         // (queries 64h..64h+63), placed with the 128-byte swizzle.
         const uint32_t row_addr = ds_tile + (uint32_t)(h * kBox + r * 128);
+        if (!dcheck(smem_ok(row_addr - sbase, 128, (uint32_t)C::kBar, 128), wc, kChkSmem, 21)) continue;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int chunk = ch * 4 + u;
@@ -329,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
 #pragma unroll
       for (int cc = 0; cc < DR / 32; ++cc) {
         uint32_t v[32];
+        if (!dcheck(tmem_ok(col + 32 * cc, 32, 512), wc, kChkTmem, 22)) continue;
         tmem_ld_x32(tmem + lane_off + col + 32 * cc, v);   // warp-collective: every lane loads
         uint32_t pk[16];
 #pragma unroll
@@ -362,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
     uint32_t t_prev = 0;
     uint32_t pause_ns = 0;
     for (int i = 0; i < n; ++i) {
-      const int q0 = (i0 + i) * kBM;
+      const int q0 = qtile(i) * kBM;
       bool ok = mbar_wait_inl(bar(kDqFull), (uint32_t)(i & 1), wc, site(6));
       ok = __all_sync(kFull, ok);
       if (!ok) break;
@@ -388,6 +431,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         if (g * 32 < DR) {
           float* base = a.dqacc + ((size_t)wrow0 + (size_t)q0) * DR + (size_t)r;
           uint32_t v[64];
+          if (!dcheck(tmem_ok(C::kColDP, 128, 512), wc, kChkTmem, 23)) {
+            tc_fence_before();
+            mbar_arrive(bar(kDqDrained));
+            continue;
+          }
           tmem_ld_x64(tmem + lane_off + C::kColDP, v);
 #pragma unroll
           for (int c = 0; c < 64; ++c) red_add_f32(base + (size_t)c * DR, u2f(v[c]));
@@ -407,9 +455,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         // dQ: lane = query row r, columns = the 64 head dims; 16-byte vector
         // reductions along the row.
         uint32_t v[64];
-        tmem_ld_x64(tmem + lane_off + C::kColDP, v);
+        const bool chk = dcheck(tmem_ok(C::kColDP, 64, 512), wc, kChkTmem, 24);
+        if (chk) tmem_ld_x64(tmem + lane_off + C::kColDP, v);
         tc_fence_before();
         mbar_arrive(bar(kDqDrained));
+        if (!chk) continue;
         float* base = a.dqacc + ((size_t)wrow0 + (size_t)q0 + (size_t)r) * D;
 #pragma unroll
         for (int c = 0; c < 64; c += 4) red_add_v4_f32(base + c, u2f(v[c]), u2f(v[c + 1]), u2f(v[c + 2]), u2f(v[c + 3]));
@@ -433,22 +483,22 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         load_rows(sbase + C::kK + bx * kBox, &a.tm_k, bar(kKVFull), 64 * bx, kv0, Nk);
         load_rows(sbase + C::kV + bx * kBox, &a.tm_v, bar(kKVFull), 64 * bx, kv0, Nk);
       }
-      int issued[2] = {0, 0};
+      int issued[QS] = {};
       for (int i = 0; i < n; ++i) {
-        const int s = i & 1;
-        if (i >= 2 && !mbar_wait_inl(bar(kQEmpty + s), (uint32_t)(((i >> 1) - 1) & 1), wc, site(7))) break;
-        const int q0 = (i0 + i) * kBM;
+        const int s = i % QS;
+        if (i >= QS && !mbar_wait_inl(bar(kQEmpty + s), (uint32_t)((i / QS - 1) & 1), wc, site(7))) break;
+        const int q0 = qtile(i) * kBM;
         mbar_arrive_expect_tx(bar(kQFull + s), 2u * C::kTile + 2u * kBM * 4);
         for (int bx = 0; bx < D / 64; ++bx) {
           load_rows(sbase + C::kQ + s * C::kTile + bx * kBox, &a.tm_q, bar(kQFull + s), 64 * bx, q0, Nq);
           load_rows(sbase + C::kDO + s * C::kTile + bx * kBox, &a.tm_do, bar(kQFull + s), 64 * bx, q0, Nq);
         }
-        bulk_load(sbase + C::kLSE + s * kBM * 4, a.lse2 + wrow0 + q0, kBM * 4, bar(kQFull + s));
-        bulk_load(sbase + C::kDV + s * kBM * 4, a.dvec + wrow0 + q0, kBM * 4, bar(kQFull + s));
+        load_bulk(sbase + C::kLSE + s * kBM * 4, a.lse2 + wrow0 + q0, kBM * 4, bar(kQFull + s));
+        load_bulk(sbase + C::kDV + s * kBM * 4, a.dvec + wrow0 + q0, kBM * 4, bar(kQFull + s));
         ++issued[s];
       }
       mbar_wait_drain_inl(bar(kKVFull), 0, wc, site(8));
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < QS; ++s)
         if (issued[s] > 0) mbar_wait_drain_inl(bar(kQFull + s), (uint32_t)((issued[s] - 1) & 1), wc, site(8));
     }
     __syncwarp();
@@ -462,8 +512,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       constexpr uint32_t kIdQ =
           D == 128 ? idesc_f16kind(128, kBM, true, true, F16) : idesc_f16kind(128, D, true, true, F16);
       auto issue_sd = [&](int i, uint32_t col, uint32_t a_tile) {    // Sᵀ (A = K) or dPᵀ (A = V)
-        const int st = i & 1;
+        const int st = i % QS;
         const uint32_t b_tile = (a_tile == sbase + C::kK ? sbase + C::kQ : sbase + C::kDO) + st * C::kTile;
+        if (!(dcheck(tmem_ok(col, kBM, 512), wc, kChkTmem, 25) &&
+              dcheck(smem_ok(a_tile - sbase, C::kTile, C::kBar, 1024), wc, kChkSmem, 25) &&
+              dcheck(smem_ok(b_tile - sbase, C::kTile, C::kBar, 1024), wc, kChkSmem, 25)))
+          return;
 #pragma unroll
         for (int ks = 0; ks < DR / 16; ++ks) {
           const uint32_t off = (uint32_t)((ks >> 2) * kBox + (ks & 3) * 32);
@@ -480,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         tc_commit(bar(kDPFull));
       }
       for (int i = 0; ok && i < n; ++i) {
-        const int st = i & 1;
+        const int st = i % QS;
         if (!mbar_wait_inl(bar(kPdsFull), (uint32_t)(i & 1), wc, site(11))) {
           ok = false;
           break;
@@ -489,10 +543,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         const uint32_t ds = sbase + C::kDS;
         const uint32_t qb = sbase + C::kQ + st * C::kTile;
         const uint32_t ob = sbase + C::kDO + st * C::kTile;
+        // Debug build: every column range and operand tile of this step's products.
+        const bool chk = dcheck(tmem_ok(C::kColDP, D == 128 ? kBM : D, 512) && tmem_ok(C::kColDV, DR, 512) &&
+                                    tmem_ok(C::kColDK, DR, 512) && tmem_ok(C::kColS, kBM / 2, 512),
+                                wc, kChkTmem, 26) &&
+                         dcheck(smem_ok(C::kDS, 2 * kBox, C::kBar, 1024) && smem_ok(qb - sbase, C::kTile, C::kBar, 1024) &&
+                                    smem_ok(ob - sbase, C::kTile, C::kBar, 1024),
+                                wc, kChkSmem, 26);
         // dQ into the dPᵀ columns first, so its drain overlaps dV and dK.
         // Both operands are read MN-major, dSᵀ [keys][queries] and K [keys][dims].
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks) {
+          if (!chk) break;
           const uint64_t dsd = sdesc_sw128(ds + (uint32_t)(ks * 2048), kBox, 1024);
           const uint64_t kd = sdesc_sw128(sbase + C::kK + (uint32_t)(ks * 2048), kBox, 1024);
           if constexpr (D == 128)
@@ -504,14 +566,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         // dV += Pᵀ dO, Pᵀ from tensor memory
 #pragma unroll
         for (int ks = 0; ks < kBM / 16; ++ks)
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + (uint32_t)(8 * ks),
+          if (chk) mma_ts(tmem + C::kColDV, tmem + C::kColS + (uint32_t)(8 * ks),
                  sdesc_sw128(ob + (uint32_t)(ks * 2048), kBox, 1024), kIdKV, (i > 0 || ks > 0) ? 1u : 0u);
         // Sᵀ of the next tile overwrites Pᵀ: issued right after dV, which
         // reads it (the products run in issue order), and before dK, so the
         // compute warps can start on it sooner.
         const bool next = i + 1 < n;
         if (next) {
-          if (!mbar_wait_inl(bar(kQFull + ((i + 1) & 1)), (uint32_t)(((i + 1) >> 1) & 1), wc, site(12))) {
+          if (!mbar_wait_inl(bar(kQFull + (i + 1) % QS), (uint32_t)(((i + 1) / QS) & 1), wc, site(12))) {
             ok = false;
             break;
           }
@@ -522,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         // dK += dSᵀ Q
 #pragma unroll
         for (int ks = 0; ks < kBM / 16; ++ks)
-          mma_ss(tmem + C::kColDK, sdesc_sw128(ds + (uint32_t)((ks >> 2) * kBox + (ks & 3) * 32), 16, 1024),
+          if (chk) mma_ss(tmem + C::kColDK, sdesc_sw128(ds + (uint32_t)((ks >> 2) * kBox + (ks & 3) * 32), 16, 1024),
                  sdesc_sw128(qb + (uint32_t)(ks * 2048), kBox, 1024), kIdKV, (i > 0 || ks > 0) ? 1u : 0u);
         tc_commit(bar(kQEmpty + st));
         if (next) {

@@ -145,11 +145,35 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
   // First query tile with a query that sees key kv0: q + off ≥ kv0.
   const int i0 = CAUSAL ? (kv0 > off ? (kv0 - off) / kBM : 0) : 0;
   const int n = n_tiles - i0;
+  // A debug build checks each box's destination and coordinates first (K and V
+  // boxes are 64 rows, Q and dO boxes 128) and, if a check fails, completes its
+  // bytes on the barrier without copying; bulk copies likewise.
   auto load_rows = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar_addr, int x, int pos, int nrows) {
+    const bool kv_map = map == &a.tm_k || map == &a.tm_v;
+    const uint32_t box = kv_map ? (uint32_t)kKBox : (uint32_t)kQBox;
+    bool chk = dcheck(smem_ok(dst - sbase, box, (uint32_t)kBar, 1024), wc, kChkSmem, 48) &&
+               dcheck(tma_x_ok(x, 64, kD), wc, kChkTmaX, 48);
+    if constexpr (RAGGED)
+      chk = chk && dcheck(tma_head_ok(pos, nrows, bh, a.B * a.H), wc, kChkTmaRows, 48);
+    else
+      chk = chk && dcheck(tma_rows_ok((long long)bh * nrows + pos, (int)(box / 128), (long long)a.B * a.H * nrows),
+                          wc, kChkTmaRows, 48);
+    if (!chk) {
+      mbar_complete_tx(bar_addr, box);
+      return;
+    }
     if constexpr (RAGGED)
       tma_load_3d(dst, map, bar_addr, x, pos, bh);
     else
       tma_load_2d(dst, map, bar_addr, x, bh * nrows + pos);
+  };
+  auto load_bulk = [&](uint32_t dst, const float* src, uint32_t bytes, uint32_t bar_addr) {
+    if (!dcheck(smem_ok(dst - sbase, bytes, (uint32_t)kBar, 16) && bulk_ok(reinterpret_cast<uint64_t>(src), dst, bytes),
+                wc, kChkBulk, 48 + 1)) {
+      mbar_complete_tx(bar_addr, bytes);
+      return;
+    }
+    bulk_load(dst, src, bytes, bar_addr);
   };
 
   if (threadIdx.x == 0) {
@@ -204,7 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
       float p[32];
       {
         uint32_t s[32];
-        tmem_ld_x32(tmem + lane_off + kColS + 32u * (uint32_t)c, s);
+        if (dcheck(tmem_ok(kColS + 32u * c, 32, 512), wc, kChkTmem, 50))
+          tmem_ld_x32(tmem + lane_off + kColS + 32u * (uint32_t)c, s);
         if (CAUSAL && delta < kBN - 1)
           p_row32<true>(s, sl2, nlse, r + delta - 32 * c, p);
         else if (ragged_cta)
@@ -217,13 +242,16 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
       if (!ok) break;
       tc_fence_after();
       uint32_t dp[32];
-      tmem_ld_x32(tmem + lane_off + kColDP + 32u * (uint32_t)c, dp);
+      if (dcheck(tmem_ok(kColDP + 32u * c, 32, 512), wc, kChkTmem, 51))
+        tmem_ld_x32(tmem + lane_off + kColDP + 32u * (uint32_t)c, dp);
       uint32_t pk[16], dk[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) pk[e] = pack2<F16>(p[2 * e], p[2 * e + 1]);
       ds_row32<F16>(p, dp, nd, dk);
-      st_row_sw128(sbase + kP, r, c, pk);
-      st_row_sw128(sbase + kDS, r, c, dk);
+      if (dcheck(smem_ok(kP + r * 128, 128, kBar, 128) && smem_ok(kDS + r * 128, 128, kBar, 128), wc, kChkSmem, 52)) {
+        st_row_sw128(sbase + kP, r, c, pk);
+        st_row_sw128(sbase + kDS, r, c, dk);
+      }
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(bar(kPdsFull));
@@ -242,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         uint32_t v[64];
+        if (!dcheck(tmem_ok((c == 0 ? kColDV : kColDK) + 64u * h, 64, 512), wc, kChkTmem, 53)) continue;
         tmem_ld_x64(tmem + lane_off + (c == 0 ? kColDV : kColDK) + 64u * (uint32_t)h, v);   // warp-collective
         const int dim = 128 * h + r;
 #pragma unroll
@@ -276,8 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
           mbar_arrive_expect_tx(bar(kQFull + bx), (uint32_t)kQBox + (bx == 0 ? 2u * kBM * 4 : 0u));
           load_rows(sbase + kQ + bx * kQBox, &a.tm_q, bar(kQFull + bx), 64 * bx, q0, Nq);
           if (bx == 0) {
-            bulk_load(sbase + kLSE, a.lse2 + wrow0 + q0, kBM * 4, bar(kQFull));
-            bulk_load(sbase + kDV, a.dvec + wrow0 + q0, kBM * 4, bar(kQFull));
+            load_bulk(sbase + kLSE, a.lse2 + wrow0 + q0, kBM * 4, bar(kQFull));
+            load_bulk(sbase + kDV, a.dvec + wrow0 + q0, kBM * 4, bar(kQFull));
           }
           ++issued_q[bx];
         }
@@ -307,12 +336,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
       auto issue_sd = [&](int i, uint32_t col, uint32_t a_tile, uint32_t b_tile, int full) -> bool {
         const uint64_t ad = sdesc_sw128(a_tile, 16, 1024), bd = sdesc_sw128(b_tile, 16, 1024);
         const uint32_t dcol = tmem + col;
+        const bool chk = dcheck(tmem_ok(col, kBN, 512), wc, kChkTmem, 54) &&
+                         dcheck(smem_ok(a_tile - sbase, 4 * kQBox, kBar, 1024) &&
+                                    smem_ok(b_tile - sbase, 4 * kKBox, kBar, 1024), wc, kChkSmem, 54);
         for (int bx = 0; bx < 4; ++bx) {
           if (!mbar_wait(bar(full + bx), (uint32_t)(i & 1), wc, site(8))) return false;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(dcol, sdesc_add(ad, bx * kQBox + 32u * k), sdesc_add(bd, bx * kKBox + 32u * k), kIdS,
+            if (chk) mma_ss(dcol, sdesc_add(ad, bx * kQBox + 32u * k), sdesc_add(bd, bx * kKBox + 32u * k), kIdS,
                    (bx > 0 || k > 0) ? 1u : 0u);
         }
         return true;
@@ -335,13 +367,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
           break;
         }
         tc_fence_after();
+        const bool chk = dcheck(tmem_ok(kColDK, 2 * kBN, 512) && tmem_ok(kColDV, 2 * kBN, 512), wc, kChkTmem, 55);
         // dKᵀ_h += Q_hᵀ dS, then dVᵀ_h += dO_hᵀ P: A MN-major over the two
         // boxes of half h, B = dS / P [query][key] MN-major; K-steps of 16 queries.
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
 #pragma unroll
           for (int ks = 0; ks < kBM / 16; ++ks)
-            mma_ss(tmem + kColDK + 64u * h, sdesc_add(q_mn, 2 * h * kQBox + ks * 2048), sdesc_add(ds_mn, ks * 2048),
+            if (chk) mma_ss(tmem + kColDK + 64u * h, sdesc_add(q_mn, 2 * h * kQBox + ks * 2048), sdesc_add(ds_mn, ks * 2048),
                    kIdT, (i > 0 || ks > 0) ? 1u : 0u);
           tc_commit(bar(kQEmpty + 2 * h));
           tc_commit(bar(kQEmpty + 2 * h + 1));
@@ -350,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
         for (int h = 0; h < 2; ++h) {
 #pragma unroll
           for (int ks = 0; ks < kBM / 16; ++ks)
-            mma_ss(tmem + kColDV + 64u * h, sdesc_add(do_mn, 2 * h * kQBox + ks * 2048), sdesc_add(p_mn, ks * 2048),
+            if (chk) mma_ss(tmem + kColDV + 64u * h, sdesc_add(do_mn, 2 * h * kQBox + ks * 2048), sdesc_add(p_mn, ks * 2048),
                    kIdT, (i > 0 || ks > 0) ? 1u : 0u);
           tc_commit(bar(kDOEmpty + 2 * h));
           tc_commit(bar(kDOEmpty + 2 * h + 1));
@@ -446,11 +479,35 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
   const int last_key = (q0 + kBM - 1 < Nq ? q0 + kBM - 1 : Nq - 1) + off;
   const int n_all = (Nk + kBN - 1) / kBN;
   const int n = CAUSAL ? last_key / kBN + 1 : n_all;
+  // A debug build checks each box's destination and coordinates first (K and V
+  // boxes are 64 rows, Q and dO boxes 128) and, if a check fails, completes its
+  // bytes on the barrier without copying; bulk copies likewise.
   auto load_rows = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar_addr, int x, int pos, int nrows) {
+    const bool kv_map = map == &a.tm_k || map == &a.tm_v;
+    const uint32_t box = kv_map ? (uint32_t)kKBox : (uint32_t)kQBox;
+    bool chk = dcheck(smem_ok(dst - sbase, box, (uint32_t)kBar, 1024), wc, kChkSmem, 56) &&
+               dcheck(tma_x_ok(x, 64, kD), wc, kChkTmaX, 56);
+    if constexpr (RAGGED)
+      chk = chk && dcheck(tma_head_ok(pos, nrows, bh, a.B * a.H), wc, kChkTmaRows, 56);
+    else
+      chk = chk && dcheck(tma_rows_ok((long long)bh * nrows + pos, (int)(box / 128), (long long)a.B * a.H * nrows),
+                          wc, kChkTmaRows, 56);
+    if (!chk) {
+      mbar_complete_tx(bar_addr, box);
+      return;
+    }
     if constexpr (RAGGED)
       tma_load_3d(dst, map, bar_addr, x, pos, bh);
     else
       tma_load_2d(dst, map, bar_addr, x, bh * nrows + pos);
+  };
+  auto load_bulk = [&](uint32_t dst, const float* src, uint32_t bytes, uint32_t bar_addr) {
+    if (!dcheck(smem_ok(dst - sbase, bytes, (uint32_t)kBar, 16) && bulk_ok(reinterpret_cast<uint64_t>(src), dst, bytes),
+                wc, kChkBulk, 56 + 1)) {
+      mbar_complete_tx(bar_addr, bytes);
+      return;
+    }
+    bulk_load(dst, src, bytes, bar_addr);
   };
 
   if (threadIdx.x == 0) {
@@ -505,7 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
       float p[32];
       {
         uint32_t s[32];
-        tmem_ld_x32(tmem + lane_off + kColS + 64u * (uint32_t)b + 32u * (uint32_t)c, s);
+        if (dcheck(tmem_ok(kColS + 64u * b + 32u * c, 32, 512), wc, kChkTmem, 58))
+          tmem_ld_x32(tmem + lane_off + kColS + 64u * (uint32_t)b + 32u * (uint32_t)c, s);
         if (CAUSAL && delta < kBN - 1)
           p_row32<true>(s, sl2, nlse, r + delta - 32 * c, p);
         else if (RAGGED && !CAUSAL && kv0 + kBN > Nk)
@@ -519,11 +577,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
       tc_fence_after();
       const uint32_t dp_col = kColDP + 64u * (uint32_t)b + 32u * (uint32_t)c;
       uint32_t dp[32];
-      tmem_ld_x32(tmem + lane_off + dp_col, dp);
+      const bool chk = dcheck(tmem_ok(dp_col, 32, 512), wc, kChkTmem, 59);
+      if (chk) tmem_ld_x32(tmem + lane_off + dp_col, dp);
       uint32_t ds[16];
       ds_row32<F16>(p, dp, nd, ds);
       // dS over the first 16 of the 32 dP columns this thread has just read.
-      tmem_st_x16(tmem + lane_off + dp_col, ds);
+      if (chk) tmem_st_x16(tmem + lane_off + dp_col, ds);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kDsFull + b));
@@ -541,6 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t v[32];
+        if (!dcheck(tmem_ok(kColDQ + 128u * c + 32u * cc, 32, 512), wc, kChkTmem, 60)) continue;
         tmem_ld_x32(tmem + lane_off + kColDQ + 128u * (uint32_t)c + 32u * (uint32_t)cc, v);   // warp-collective
         uint32_t pk[16];
 #pragma unroll
@@ -564,8 +624,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
         load_rows(sbase + kQ + bx * kQBox, &a.tm_q, bar(kQFull), 64 * bx, q0, Nq);
         load_rows(sbase + kDO + bx * kQBox, &a.tm_do, bar(kQFull), 64 * bx, q0, Nq);
       }
-      bulk_load(sbase + kLSE, a.lse2 + wrow0 + q0, kBM * 4, bar(kQFull));
-      bulk_load(sbase + kDV, a.dvec + wrow0 + q0, kBM * 4, bar(kQFull));
+      load_bulk(sbase + kLSE, a.lse2 + wrow0 + q0, kBM * 4, bar(kQFull));
+      load_bulk(sbase + kDV, a.dvec + wrow0 + q0, kBM * 4, bar(kQFull));
       int k_boxes = 0, v_loads[4] = {0, 0, 0, 0};
       auto load_k = [&](int j) -> bool {
         for (int bx = 0; bx < 4; ++bx) {
@@ -610,13 +670,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
       const uint64_t k_mn = sdesc_sw128(sbase + kK, kKBox, 1024);
       auto issue_s = [&](int j) -> bool {
         const uint32_t col = tmem + kColS + 64u * (uint32_t)(j & 1);
+        const bool chk = dcheck(tmem_ok(kColS + 64u * (j & 1), kBN, 512), wc, kChkTmem, 61);
         for (int bx = 0; bx < 4; ++bx) {
           const int gi = 4 * j + bx, slot = gi % kKSlots;
           if (!mbar_wait(bar(kKFull + slot), (uint32_t)((gi / kKSlots) & 1), wc, site(8))) return false;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(col, sdesc_add(q_k, bx * kQBox + 32u * k), sdesc_add(k_k, slot * kKBox + 32u * k), kIdS,
+            if (chk) mma_ss(col, sdesc_add(q_k, bx * kQBox + 32u * k), sdesc_add(k_k, slot * kKBox + 32u * k), kIdS,
                    (bx > 0 || k > 0) ? 1u : 0u);
         }
         tc_commit(bar(kSFull + (j & 1)));
@@ -624,12 +685,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
       };
       auto issue_dp = [&](int j) -> bool {
         const uint32_t col = tmem + kColDP + 64u * (uint32_t)(j & 1);
+        const bool chk = dcheck(tmem_ok(kColDP + 64u * (j & 1), kBN, 512), wc, kChkTmem, 62);
         for (int bx = 0; bx < 4; ++bx) {
           if (!mbar_wait(bar(kVFull + bx), (uint32_t)(j & 1), wc, site(9))) return false;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(col, sdesc_add(do_k, bx * kQBox + 32u * k), sdesc_add(v_k, bx * kKBox + 32u * k), kIdS,
+            if (chk) mma_ss(col, sdesc_add(do_k, bx * kQBox + 32u * k), sdesc_add(v_k, bx * kKBox + 32u * k), kIdS,
                    (bx > 0 || k > 0) ? 1u : 0u);
           tc_commit(bar(kVEmpty + bx));
         }
@@ -643,9 +705,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
       auto issue_dq = [&](int j) {
         const uint32_t ds_col = tmem + kColDP + 64u * (uint32_t)(j & 1);
         const uint32_t slot0 = (uint32_t)((4 * j) % kKSlots);
+        const bool chk = dcheck(tmem_ok(kColDQ, kD, 512) && tmem_ok(kColDP + 64u * (j & 1), kBN, 512), wc, kChkTmem,
+                                63) &&
+                         dcheck(smem_ok(kK + slot0 * kKBox, 4 * kKBox, kBar, 1024), wc, kChkSmem, 63);
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks)
-          mma_ts(tmem + kColDQ, ds_col + (uint32_t)(ks < 2 ? 8 * ks : 32 + 8 * (ks - 2)),
+          if (chk) mma_ts(tmem + kColDQ, ds_col + (uint32_t)(ks < 2 ? 8 * ks : 32 + 8 * (ks - 2)),
                  sdesc_add(k_mn, slot0 * kKBox + ks * 2048), kIdQ, (j > 0 || ks > 0) ? 1u : 0u);
         for (int bx = 0; bx < 4; ++bx) tc_commit(bar(kKEmpty + slot0 + bx));
       };

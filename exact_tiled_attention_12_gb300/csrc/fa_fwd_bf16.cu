@@ -16,7 +16,9 @@
 //   O_t  = cols [256 + d t, 256 + d t + d)   fp32 unnormalised output
 // Per K/V tile the MMA thread issues, for each query tile, O_t += P_t V_j (A
 // from tensor memory) and then S_t = Q_t K_{j+1}ᵀ, so the softmax of one
-// tile overlaps the products of the other.
+// tile overlaps the products of the other.  That order matters: issuing each
+// tile's products from its own thread (two issuers, the tensor pipe then
+// interleaving them) measured 7-14 % slower on GB300.
 //
 // Rescaling is lazy: the reference max m only moves when a row's new max
 // exceeds it by more than 8 (base 2), so P ≤ 2^8 and ℓ and Õ keep sharing one
@@ -41,29 +43,42 @@ constexpr int kBoxBytes = 128 * 128;   // one TMA box: 128 rows × 128 bytes
 // (it is issue-bound, not MUFU-bound), so all stay on MUFU.
 constexpr int kPolyEvery = 0;
 
+// K and V ring depths.  Measured on GB300 (clock64 trace): the loads arrive
+// well before the MMA thread needs them, and deeper rings (three to six
+// stages at d = 64, a third V stage at d = 128) were no faster or slower.
+template <int D>
+struct FwdStages {
+  static constexpr int kK = 2;
+  static constexpr int kV = 2;
+};
+
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 template <int D>
 struct FwdLayout {
+  static constexpr int kKS = FwdStages<D>::kK;
+  static constexpr int kVS = FwdStages<D>::kV;
   static constexpr int kTile = kBM * D * 2;       // bytes of one 128 × D bf16 tile
   static constexpr int kQ = 0;                    // Q tile t at kQ + t·kTile
-  static constexpr int kK = kQ + 2 * kTile;       // K stage s
-  static constexpr int kV = kK + 2 * kTile;       // V stage s
-  static constexpr int kBar = kV + 2 * kTile;
-  static constexpr int kBytes = kBar + 256;
+  static constexpr int kK = kQ + 2 * kTile;       // K stage s at kK + s·kTile
+  static constexpr int kV = kK + kKS * kTile;     // V stage s at kV + s·kTile
+  static constexpr int kBar = kV + kVS * kTile;
+  static constexpr int kBytes = kBar + 512;
 };
 
 // Barrier slots (8 bytes each) inside the barrier block.
-enum FwdBar : int {
-  kQFull = 0,
-  kKFull = 1,    // +stage
-  kKEmpty = 3,   // +stage
-  kVFull = 5,    // +stage
-  kVEmpty = 7,   // +stage
-  kSFull = 9,    // +tile
-  kPFull = 11,   // +tile
-  kOFull = 13,   // +tile
-  kMmaDone = 15,
-  kNumBars = 16,
+template <int KS, int VS>
+struct FwdBars {
+  static constexpr int kQFull = 0;
+  static constexpr int kKFull = 1;               // +stage
+  static constexpr int kKEmpty = kKFull + KS;    // +stage
+  static constexpr int kVFull = kKEmpty + KS;    // +stage
+  static constexpr int kVEmpty = kVFull + VS;    // +stage
+  static constexpr int kSFull = kVEmpty + VS;    // +tile
+  static constexpr int kPFull = kSFull + 2;      // +tile
+  static constexpr int kOFull = kPFull + 2;      // +tile
+  static constexpr int kMmaDone = kOFull + 2;
+  static constexpr int kNumBars = kMmaDone + 1;
+  static_assert(8 * kNumBars + 8 <= 512, "barrier block too small");
 };
 
 // Fault codes recorded when a wait runs out of time (kernel id 1 in the high byte).
@@ -120,6 +135,11 @@ template <int DR, bool CAUSAL, bool RAGGED, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_constant__ FwdArgs a) {
   constexpr int D = DR <= 64 ? 64 : 128;
   using L = FwdLayout<D>;
+  constexpr int KS = L::kKS, VS = L::kVS;
+  using Bar = FwdBars<KS, VS>;
+  constexpr int kQFull = Bar::kQFull, kKFull = Bar::kKFull, kKEmpty = Bar::kKEmpty, kVFull = Bar::kVFull,
+                kVEmpty = Bar::kVEmpty, kSFull = Bar::kSFull, kPFull = Bar::kPFull, kOFull = Bar::kOFull,
+                kMmaDone = Bar::kMmaDone, kNumBars = Bar::kNumBars;
   // Dynamic shared memory starts on a 1024-byte boundary (no static shared
   // memory is declared); 128-byte swizzled tiles need that alignment.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -172,7 +192,19 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
   const int kv_tail = Nk - (n_kv_all - 1) * kBN;
   const bool ragged_last = RAGGED && !CAUSAL && kv_tail < kBN && kv_begin + n_kv == n_kv_all;
   // Loads rows [pos, pos + 128) of this head from a map over heads of `n` rows.
+  // A debug build checks the destination and the coordinates first and, if a
+  // check fails, completes the box's bytes on the barrier without copying.
   auto load_rows = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar_addr, int x, int pos, int n) {
+    bool chk = dcheck(smem_ok(dst - sbase, kBoxBytes, (uint32_t)L::kBar, 1024), wc, kChkSmem, 1) &&
+               dcheck(tma_x_ok(x, 64, D), wc, kChkTmaX, 1);
+    if constexpr (RAGGED)
+      chk = chk && dcheck(tma_head_ok(pos, n, bh, a.B * a.H), wc, kChkTmaRows, 1);
+    else
+      chk = chk && dcheck(tma_rows_ok((long long)bh * n + pos, kBM, (long long)a.B * a.H * n), wc, kChkTmaRows, 1);
+    if (!chk) {
+      mbar_complete_tx(bar_addr, kBoxBytes);
+      return;
+    }
     if constexpr (RAGGED)
       tma_load_3d(dst, map, bar_addr, x, pos, bh);
     else
@@ -196,14 +228,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kQFull), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < KS; ++s) {
       mbar_init(bar(kKFull + s), 1);
       mbar_init(bar(kKEmpty + s), 1);
+    }
+    for (int s = 0; s < VS; ++s) {
       mbar_init(bar(kVFull + s), 1);
       mbar_init(bar(kVEmpty + s), 1);
-      mbar_init(bar(kSFull + s), 1);
-      mbar_init(bar(kPFull + s), 128);
-      mbar_init(bar(kOFull + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(kSFull + t), 1);
+      mbar_init(bar(kPFull + t), 128);
+      mbar_init(bar(kOFull + t), 1);
     }
     mbar_init(bar(kMmaDone), 1);
     *abort_flag = 0;
@@ -238,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
       if (!ok) break;
       tc_fence_after();
       uint32_t s[128];
-      tmem_ld_x128(tmem + lane_off + s_col(t), s);
+      if (dcheck(tmem_ok(s_col(t), 128, 512), wc, kChkTmem, 2)) tmem_ld_x128(tmem + lane_off + s_col(t), s);
       if (CAUSAL && j >= fm) {
         // A tile crossing the diagonal: key 128j + c is visible to query
         // qt + r iff c ≤ r + qt + off − 128j (c ≤ r for square problems).
@@ -271,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
         // for P_full, so this row of O_t is ours to rescale.
 #pragma unroll
         for (int cc = 0; cc < DR / 32; ++cc) {
+          if (!dcheck(tmem_ok(o_col(t) + 32 * cc, 32, 512), wc, kChkTmem, 3)) continue;
           uint32_t o[32];
           tmem_ld_x32(tmem + lane_off + o_col(t) + 32 * cc, o);
 #pragma unroll
@@ -283,7 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
       // Masked tiles take every exponential on MUFU, so masked scores give
       // exactly 0.
       const uint32_t p_addr = tmem + lane_off + s_col(t);
-      if ((CAUSAL && j >= fm) || (ragged_last && j == nt - 1))
+      if (!dcheck(tmem_ok(s_col(t), kBN / 2, 512), wc, kChkTmem, 4)) {
+      } else if ((CAUSAL && j >= fm) || (ragged_last && j == nt - 1))
         ell += exp_tile_to_p<0, F16>(s, sl2, m_ref, p_addr);
       else
         ell += exp_tile_to_p<kPolyEvery, F16>(s, sl2, m_ref, p_addr);
@@ -307,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
           uint16_t* orow = static_cast<uint16_t*>(a.o) + ((size_t)row0 + (size_t)q) * DR;
 #pragma unroll
           for (int cc = 0; cc < DR / 32; ++cc) {
+            if (!dcheck(tmem_ok(o_col(t) + 32 * cc, 32, 512), wc, kChkTmem, 5)) continue;
             uint32_t o[32];
             tmem_ld_x32(tmem + lane_off + o_col(t) + 32 * cc, o);
             uint32_t pk[16];
@@ -325,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
           float* orow = a.opart + prow * DR;
 #pragma unroll
           for (int cc = 0; cc < DR / 32; ++cc) {
+            if (!dcheck(tmem_ok(o_col(t) + 32 * cc, 32, 512), wc, kChkTmem, 6)) continue;
             uint32_t o[32];
             tmem_ld_x32(tmem + lane_off + o_col(t) + 32 * cc, o);
 #pragma unroll
@@ -342,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
       prefetch_tmap(&a.tm_q);
       prefetch_tmap(&a.tm_k);
       prefetch_tmap(&a.tm_v);
-      int issued_k[2] = {0, 0}, issued_v[2] = {0, 0};
+      int issued_k[KS] = {}, issued_v[VS] = {};
       const uint32_t tile = (uint32_t)L::kTile;
       const uint32_t qbytes = (n_t[0] > 0 ? tile : 0u) + (n_t[1] > 0 ? tile : 0u);
       const bool have_q = qbytes > 0;
@@ -353,28 +393,31 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
             for (int b = 0; b < D / 64; ++b)
               load_rows(sbase + L::kQ + t * L::kTile + b * kBoxBytes, &a.tm_q, bar(kQFull), 64 * b, q0 + t * kBM, Nq);
       }
+      // Tile j goes to K stage j % KS and V stage j % VS; its n-th use of a
+      // stage (n = j / stages) completes phase n of that stage's barriers, so a
+      // reuse waits for the release of use n − 1 (parity (n − 1) & 1).
       for (int j = 0; j < J; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(bar(kKEmpty + s), (uint32_t)(((j >> 1) - 1) & 1), wc, site(3))) break;
-        mbar_arrive_expect_tx(bar(kKFull + s), tile);
+        const int sk = j % KS, sv = j % VS;
+        if (j >= KS && !mbar_wait(bar(kKEmpty + sk), (uint32_t)((j / KS - 1) & 1), wc, site(3))) break;
+        mbar_arrive_expect_tx(bar(kKFull + sk), tile);
         for (int b = 0; b < D / 64; ++b)
-          load_rows(sbase + L::kK + s * L::kTile + b * kBoxBytes, &a.tm_k, bar(kKFull + s), 64 * b,
+          load_rows(sbase + L::kK + sk * L::kTile + b * kBoxBytes, &a.tm_k, bar(kKFull + sk), 64 * b,
                     (kv_begin + j) * kBN, Nk);
-        ++issued_k[s];
-        if (j >= 2 && !mbar_wait(bar(kVEmpty + s), (uint32_t)(((j >> 1) - 1) & 1), wc, site(4))) break;
-        mbar_arrive_expect_tx(bar(kVFull + s), tile);
+        ++issued_k[sk];
+        if (j >= VS && !mbar_wait(bar(kVEmpty + sv), (uint32_t)((j / VS - 1) & 1), wc, site(4))) break;
+        mbar_arrive_expect_tx(bar(kVFull + sv), tile);
         for (int b = 0; b < D / 64; ++b)
-          load_rows(sbase + L::kV + s * L::kTile + b * kBoxBytes, &a.tm_v, bar(kVFull + s), 64 * b,
+          load_rows(sbase + L::kV + sv * L::kTile + b * kBoxBytes, &a.tm_v, bar(kVFull + sv), 64 * b,
                     (kv_begin + j) * kBN, Nk);
-        ++issued_v[s];
+        ++issued_v[sv];
       }
       // Never leave the CTA with copies in flight: wait for the last load of
       // every stage (already complete in the normal case).
       if (have_q) mbar_wait_drain(bar(kQFull), 0, wc, site(5));
-      for (int s = 0; s < 2; ++s) {
+      for (int s = 0; s < KS; ++s)
         if (issued_k[s] > 0) mbar_wait_drain(bar(kKFull + s), (uint32_t)((issued_k[s] - 1) & 1), wc, site(5));
+      for (int s = 0; s < VS; ++s)
         if (issued_v[s] > 0) mbar_wait_drain(bar(kVFull + s), (uint32_t)((issued_v[s] - 1) & 1), wc, site(5));
-      }
     }
   } else {
     // ------------------------------------------------------------ MMA issuer
@@ -385,15 +428,19 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
       int k_ready = -1;
       auto issue_s = [&](int t, int j) -> bool {
         if (k_ready < j) {
-          if (!mbar_wait(bar(kKFull + (j & 1)), (uint32_t)((j >> 1) & 1), wc, site(7))) return false;
+          if (!mbar_wait(bar(kKFull + j % KS), (uint32_t)((j / KS) & 1), wc, site(7))) return false;
           k_ready = j;
         }
         tc_fence_after();
         const uint64_t qd = sdesc_sw128(sbase + L::kQ + t * L::kTile, 16, 1024);
-        const uint64_t kd = sdesc_sw128(sbase + L::kK + (j & 1) * L::kTile, 16, 1024);
+        const uint64_t kd = sdesc_sw128(sbase + L::kK + (j % KS) * L::kTile, 16, 1024);
         const uint32_t dcol = tmem + s_col(t);
+        const bool chk = dcheck(tmem_ok(s_col(t), kBN, 512), wc, kChkTmem, 7) &&
+                         dcheck(smem_ok(L::kQ + t * L::kTile, L::kTile, L::kBar, 1024), wc, kChkSmem, 7) &&
+                         dcheck(smem_ok(L::kK + (j % KS) * L::kTile, L::kTile, L::kBar, 1024), wc, kChkSmem, 7);
 #pragma unroll
         for (int ks = 0; ks < DR / 16; ++ks) {
+          if (!chk) break;
           const uint32_t off = (uint32_t)((ks >> 2) * kBoxBytes + (ks & 3) * 32);
           mma_ss(dcol, sdesc_add(qd, off), sdesc_add(kd, off), kIdS, ks > 0 ? 1u : 0u);
         }
@@ -406,11 +453,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
         if (ok) tc_commit(bar(kKEmpty + 0));
       }
       for (int j = 0; ok && j < J; ++j) {
-        if (!mbar_wait(bar(kVFull + (j & 1)), (uint32_t)((j >> 1) & 1), wc, site(8))) {
+        if (!mbar_wait(bar(kVFull + j % VS), (uint32_t)((j / VS) & 1), wc, site(8))) {
           ok = false;
           break;
         }
-        const uint64_t vd = sdesc_sw128(sbase + L::kV + (j & 1) * L::kTile, kBoxBytes, 1024);
+        const uint64_t vd = sdesc_sw128(sbase + L::kV + (j % VS) * L::kTile, kBoxBytes, 1024);
         for (int t = 0; t < 2 && ok; ++t) {
           if (j >= n_t[t]) continue;
           if (!mbar_wait(bar(kPFull + t), (uint32_t)(j & 1), wc, site(9))) {
@@ -419,16 +466,20 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
           }
           tc_fence_after();
           const uint32_t ocol = tmem + o_col(t), pcol = tmem + s_col(t);
+          const bool chk = dcheck(tmem_ok(o_col(t), DR, 512), wc, kChkTmem, 8) &&
+                           dcheck(tmem_ok(s_col(t), kBN / 2, 512), wc, kChkTmem, 8) &&
+                           dcheck(smem_ok(L::kV + (j % VS) * L::kTile, L::kTile, L::kBar, 1024), wc, kChkSmem, 8);
 #pragma unroll
           for (int ks = 0; ks < kBN / 16; ++ks)
-            mma_ts(ocol, pcol + (uint32_t)(8 * ks), sdesc_add(vd, (uint32_t)(ks * 2048)), kIdO,
-                   (j > 0 || ks > 0) ? 1u : 0u);
+            if (chk)
+              mma_ts(ocol, pcol + (uint32_t)(8 * ks), sdesc_add(vd, (uint32_t)(ks * 2048)), kIdO,
+                     (j > 0 || ks > 0) ? 1u : 0u);
           if (j == n_t[t] - 1) tc_commit(bar(kOFull + t));
           if (j + 1 < n_t[t]) ok = issue_s(t, j + 1);
         }
         if (!ok) break;
-        tc_commit(bar(kVEmpty + (j & 1)));
-        if (j + 1 < J) tc_commit(bar(kKEmpty + ((j + 1) & 1)));
+        tc_commit(bar(kVEmpty + j % VS));
+        if (j + 1 < J) tc_commit(bar(kKEmpty + (j + 1) % KS));
       }
       // Every product must be finished before tensor memory is released.
       tc_commit(bar(kMmaDone));

@@ -150,7 +150,19 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
   const int row0 = bh * Nq;
   const int kv_tail = Nk - (n_kv_all - 1) * kBN;   // keys of the head's last tile that exist
   const bool ragged_last = RAGGED && !CAUSAL && kv_tail < kBN && kv_begin + n_kv == n_kv_all;
+  // A debug build checks each box's destination and coordinates first and, if
+  // a check fails, completes its bytes on the barrier without copying.
   auto load_rows = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar_addr, int x, int pos, int n) {
+    bool chk = dcheck(smem_ok(dst - sbase, kBox, (uint32_t)kBar, 1024), wc, kChkSmem, 32) &&
+               dcheck(tma_x_ok(x, 64, kD), wc, kChkTmaX, 32);
+    if constexpr (RAGGED)
+      chk = chk && dcheck(tma_head_ok(pos, n, bh, a.B * a.H), wc, kChkTmaRows, 32);
+    else
+      chk = chk && dcheck(tma_rows_ok((long long)bh * n + pos, kBM, (long long)a.B * a.H * n), wc, kChkTmaRows, 32);
+    if (!chk) {
+      mbar_complete_tx(bar_addr, kBox);
+      return;
+    }
     if constexpr (RAGGED)
       tma_load_3d(dst, map, bar_addr, x, pos, bh);
     else
@@ -211,7 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
       float mxh = -INFINITY;
       if (okj) {
         tc_fence_after();
-        tmem_ld_x64(tmem + lane_off + 128u * (uint32_t)b + 64u * (uint32_t)c, s);
+        if (dcheck(tmem_ok(128u * b + 64u * c, 64, 512), wc, kChkTmem, 33))
+          tmem_ld_x64(tmem + lane_off + 128u * (uint32_t)b + 64u * (uint32_t)c, s);
         if (CAUSAL && j >= fm) {
           const int lim = r + q0 + off - j * kBN - 64 * c;
 #pragma unroll
@@ -256,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t o[32];
             const uint32_t col = 256u + 128u * (uint32_t)c + 32u * (uint32_t)cc;
+            if (!dcheck(tmem_ok(col, 32, 512), wc, kChkTmem, 34)) continue;
             tmem_ld_x32(tmem + lane_off + col, o);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
@@ -268,7 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
       }
       ell *= alpha;
       m_ref = m_new;
-      ell += exp_half_to_p<F16>(s, sl2, m_ref, tmem + lane_off + 128u * (uint32_t)b + 32u * (uint32_t)c);
+      if (dcheck(tmem_ok(128u * b + 32u * c, 32, 512), wc, kChkTmem, 35))
+        ell += exp_half_to_p<F16>(s, sl2, m_ref, tmem + lane_off + 128u * (uint32_t)b + 32u * (uint32_t)c);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kPFull + b));
@@ -295,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t o[32];
+            if (!dcheck(tmem_ok(256u + 128u * c + 32u * cc, 32, 512), wc, kChkTmem, 36)) continue;
             tmem_ld_x32(tmem + lane_off + 256u + 128u * (uint32_t)c + 32u * (uint32_t)cc, o);
             uint32_t pk[16];
 #pragma unroll
@@ -313,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t o[32];
+            if (!dcheck(tmem_ok(256u + 128u * c + 32u * cc, 32, 512), wc, kChkTmem, 36)) continue;
             tmem_ld_x32(tmem + lane_off + 256u + 128u * (uint32_t)c + 32u * (uint32_t)cc, o);
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4)
@@ -386,9 +403,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
           if (!mbar_wait(bar(kKFull + slot), (uint32_t)((gi / kKSlots) & 1), wc, site(8))) return false;
           tc_fence_after();
           const uint32_t qa = sbase + kQ + bx * kBox, kb = sbase + kK + slot * kBox;
+          const bool chk = dcheck(tmem_ok(col, kBN, 512), wc, kChkTmem, 37) &&
+                           dcheck(smem_ok(qa - sbase, kBox, kBar, 1024) && smem_ok(kb - sbase, kBox, kBar, 1024), wc,
+                                  kChkSmem, 37);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + col, sdesc_sw128(qa + 32u * k, 16, 1024), sdesc_sw128(kb + 32u * k, 16, 1024), kIdS,
+            if (chk) mma_ss(tmem + col, sdesc_sw128(qa + 32u * k, 16, 1024), sdesc_sw128(kb + 32u * k, 16, 1024), kIdS,
                    (bx > 0 || k > 0) ? 1u : 0u);
           tc_commit(bar(kKEmpty + slot));
         }
@@ -405,9 +425,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
         }
         tc_fence_after();
         const uint32_t pcol = 128u * (uint32_t)(j & 1);
+        const bool chk = dcheck(tmem_ok(256u, kD, 512) && tmem_ok(pcol, kBN / 2, 512), wc, kChkTmem, 38) &&
+                         dcheck(smem_ok(kV, 4 * kBox, kBar, 1024), wc, kChkSmem, 38);
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks)
-          mma_ts(tmem + 256u, tmem + pcol + (uint32_t)(8 * ks), sdesc_sw128(sbase + kV + (uint32_t)(ks * 2048), kBox, 1024),
+          if (chk) mma_ts(tmem + 256u, tmem + pcol + (uint32_t)(8 * ks), sdesc_sw128(sbase + kV + (uint32_t)(ks * 2048), kBox, 1024),
                  kIdO, (j > 0 || ks > 0) ? 1u : 0u);
         tc_commit(bar(kVEmpty));
         tc_commit(bar(kPVDone));

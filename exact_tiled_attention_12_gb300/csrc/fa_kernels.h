@@ -136,6 +136,9 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
 // One CTA whose pipeline wait can never complete: the bounded wait gives up
 // after its time limit and records a fault code in `fault` (no trap, no hang).
 cudaError_t launch_wait_timeout_selftest(unsigned int* fault, cudaStream_t s);
+// One thread evaluates the debug-build checks on FA_SELFTEST_BOUNDS_CASES fixed
+// cases and writes 1 (passed) / 0 (failed) for each into `results`.
+cudaError_t launch_bounds_check_selftest(unsigned int* fault, int* results, cudaStream_t s);
 
 // ---------------------------------------------------------------- fp32 SIMT path
 

@@ -15,6 +15,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "fa_checks.h"
+
 namespace fa {
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
@@ -123,6 +125,37 @@ __device__ __forceinline__ bool mbar_wait_inl(uint32_t bar, uint32_t parity, Wai
 __device__ __forceinline__ bool mbar_wait_drain_inl(uint32_t bar, uint32_t parity, WaitCtx c, uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow_inline(bar, parity, c, site, false);
+}
+
+// Completes `bytes` of the transaction count of the current phase of `bar`
+// without a copy: a debug-build check that skips a load still lets the phase
+// complete, so no wait is left on bytes that will never arrive.
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// ------------------------------------------------------------------ debug-build checks
+
+// Evaluates one of the fa_checks.h predicates at a call site.  In a debug
+// build a failed check records check_code(kind, site) in the fault word
+// (the first fault wins), raises the CTA's abort flag so that every role
+// unwinds through its bounded waits, and returns false so that the call site
+// skips the access.  In the release build it is `true` and the predicate is
+// never evaluated.
+__device__ __forceinline__ bool dcheck(bool ok, WaitCtx c, uint32_t kind, uint32_t site) {
+  if constexpr (kDebugChecks) {
+    if (!ok) {
+      *c.abort_flag = 1;
+      atomicCAS(c.fault, 0u, check_code(kind, site));
+    }
+    return ok;
+  } else {
+    (void)ok;
+    (void)c;
+    (void)kind;
+    (void)site;
+    return true;
+  }
 }
 
 // ------------------------------------------------------------------ TMA / bulk copies

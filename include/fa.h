@@ -74,7 +74,8 @@ typedef enum {
   FA_ERR_MISALIGNED = 3,   /* bf16/fp16 base pointer not 16-byte aligned */
   FA_ERR_WORKSPACE = 4,    /* workspace NULL, misaligned (256 B) or too small */
   FA_ERR_CUDA = 5,         /* a CUDA runtime/driver call or launch failed */
-  FA_ERR_TIMEOUT = 6       /* a kernel abandoned a pipeline wait (see fa_sync_status) */
+  FA_ERR_TIMEOUT = 6,      /* a kernel abandoned a pipeline wait (see fa_sync_status) */
+  FA_ERR_BOUNDS = 7        /* debug build only: a device-side bounds or alignment check failed */
 } fa_status;
 
 typedef enum { FA_DTYPE_BF16 = 0, FA_DTYPE_FP32 = 1, FA_DTYPE_FP16 = 2 } fa_dtype;
@@ -228,8 +229,9 @@ fa_status fa_bwd_dq_finish(void* dq, int B, int H, int N, int d, float scale,
 /*
  * Synchronises `stream`, then reports and clears the kernels' fault words on
  * the current device: FA_ERR_TIMEOUT if any kernel abandoned a pipeline wait
- * since the last call, FA_ERR_CUDA if the stream reports an error, else FA_OK.
- * The only entry point that blocks the host.
+ * since the last call, FA_ERR_BOUNDS if (debug build) a device-side check
+ * failed, FA_ERR_CUDA if the stream reports an error, else FA_OK.  The only
+ * entry point that blocks the host.
  */
 fa_status fa_sync_status(fa_stream_t stream);
 
@@ -244,6 +246,42 @@ fa_status fa_sync_status(fa_stream_t stream);
  * path every tensor-core kernel takes when a wait runs out.
  */
 fa_status fa_selftest_wait_timeout(fa_stream_t stream);
+
+/*
+ * Debug build.  The library also builds as libfa_debug.so (same symbols,
+ * compiled with FA_DEBUG_CHECKS) whose tensor-core kernels check, before
+ * each access, that every TMA tile load starts its innermost coordinate on a
+ * 16-byte boundary inside the row and its rows inside the tensor, that every
+ * shared-memory destination or MMA operand lies inside the kernel's dynamic
+ * shared memory with its alignment, that every tensor-memory load, store and
+ * MMA accumulator stays inside the 512 allocated columns, and that every bulk
+ * copy is 16-byte aligned.  A failed check records its code in the fault
+ * word, raises the CTA's abort flag and skips the access (a skipped load
+ * still completes its bytes on the barrier), so the CTA unwinds through its
+ * bounded waits: nothing traps, and fa_sync_status() returns FA_ERR_BOUNDS.
+ * Results of a debug build are bit-identical to the release build's except
+ * for dQ's float32 summation order.  (compute-sanitizer is not available
+ * everywhere; this is the substitute.)
+ *
+ * fa_debug_checks_enabled() returns 1 in libfa_debug.so and 0 in libfa.so.
+ */
+int fa_debug_checks_enabled(void);
+
+/*
+ * Self-test of the debug build's device-side checks (not part of the
+ * computation).  One thread evaluates FA_SELFTEST_BOUNDS_CASES checks on
+ * fixed integer arguments — alternately valid and invalid: a TMA coordinate
+ * off its 16-byte boundary, box rows past the tensor, tensor-memory columns
+ * past the allocation, a misaligned shared-memory operand — and writes 1
+ * (passed) or 0 (failed) for each into `results` (device memory, at least
+ * FA_SELFTEST_BOUNDS_CASES ints).  The kernel performs no access with those
+ * arguments: it only evaluates the checks.  The first failed check's code is
+ * recorded, so a following fa_sync_status() returns FA_ERR_BOUNDS.  Returns
+ * FA_ERR_UNSUPPORTED from the release library (checks compiled out) and
+ * FA_ERR_INVALID_ARG for a NULL `results`.
+ */
+#define FA_SELFTEST_BOUNDS_CASES 8
+fa_status fa_selftest_bounds_check(int* results, fa_stream_t stream);
 
 /*
  * Size of the scratch array compiled into libfa.so for fa_bwd_noalloc:

@@ -186,35 +186,54 @@ int sm_count_current_device() {
 }
 
 struct FwdPlan {
-  int n_full, splits;
+  int n_full, splits, part_rows;
   size_t opart_bytes;
 };
 
 // Workspace the forward's load balancing needs on the current device (0 when
-// it does not split: causal, fp32, or no partial last wave worth splitting).
-// One query (a decoding step) sees every key under the causal mask, so it
-// runs as the unmasked problem, which may split its keys over several CTAs.
+// it does not split: fp32, or a long problem with no partial last wave worth
+// splitting, or a long causal one).  One query (a decoding step) sees every
+// key under the causal mask, so it runs as the unmasked problem, which may
+// split its keys over several CTAs.  A problem with 2 to 128 queries per
+// head and fewer units than SMs streams its K/V far more than it computes
+// and would leave SMs idle: every unit is split over its K/V tiles so the
+// grid fills whole waves (under the mask too, except at d = 256), and each
+// part keeps one partial row per query.  (Measured on GB300: with as many
+// units as SMs or more, the unsplit grid already keeps HBM busy and
+// splitting every unit only adds start-up and merge work.)
 int forward_causal(int causal, const Shape& s) { return causal && s.Nq > 1 ? 1 : 0; }
 
 size_t fwd_workspace_bytes(const Shape& s, int causal, fa_dtype dtype, FwdPlan* plan) {
   causal = forward_causal(causal, s);
-  if (s.empty() || causal || !is16(dtype)) return 0;
+  if (s.empty() || !is16(dtype)) return 0;
+  const int sms = sm_count_current_device();
+  const bool short_q =
+      s.Nq >= 2 && s.Nq <= 128 && fa::fwd_units((int)s.B, (int)s.H, (int)s.Nq, (int)s.d) < sms;
+  if (causal && !(short_q && s.d != 256)) return 0;
   if (s.Nq == 1) {
     // A decoding step: the streaming kernel's key ranges per head.
     const int splits = fa::decode_splits((int)s.heads(), sm_count_current_device(), (int)s.Nk);
     if (splits <= 1) return 0;
     const size_t rows = (size_t)s.heads() * (size_t)splits;
     const size_t opart = pad256(rows * (size_t)s.d * 4);
-    if (plan) *plan = FwdPlan{0, splits, opart};
+    if (plan) *plan = FwdPlan{0, splits, 1, opart};
     return opart + pad256(rows * 4);
   }
   const int units = fa::fwd_units((int)s.B, (int)s.H, (int)s.Nq, (int)s.d);
-  int n_full, splits;
-  fa::fwd_split_plan(units, sm_count_current_device(), (int)(s.nk_pad() / 128), &n_full, &splits);
+  int n_full, splits, part_rows = fa::fwd_unit_rows((int)s.d);
+  if (short_q) {
+    // Every query row of a head sees (under the mask) keys up to Nk − 1, so
+    // each unit's visible K/V tiles are all of them.
+    n_full = 0;
+    splits = fa::fwd_split_short(units, sms, (int)(s.nk_pad() / 128));
+    part_rows = (int)s.Nq;
+  } else {
+    fa::fwd_split_plan(units, sms, (int)(s.nk_pad() / 128), &n_full, &splits);
+  }
   if (splits <= 1 || n_full >= units) return 0;
-  const size_t rows = (size_t)(units - n_full) * (size_t)splits * (size_t)fa::fwd_unit_rows((int)s.d);
+  const size_t rows = (size_t)(units - n_full) * (size_t)splits * (size_t)part_rows;
   const size_t opart = pad256(rows * (size_t)s.d * 4);
-  if (plan) *plan = FwdPlan{n_full, splits, opart};
+  if (plan) *plan = FwdPlan{n_full, splits, part_rows, opart};
   return opart + pad256(rows * 4);
 }
 
@@ -281,12 +300,14 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
   const size_t need = fwd_workspace_bytes(s, causal, dtype, &plan);
   a.n_full = fa::fwd_units(B, H, Nq, d);
   a.splits = 1;
+  a.part_rows = fa::fwd_unit_rows(d);
   a.opart = nullptr;
   a.lpart = nullptr;
   if (need > 0 && workspace != nullptr) {
     if (workspace_bytes < need) return FA_ERR_WORKSPACE;
     a.n_full = plan.n_full;
     a.splits = plan.splits;
+    a.part_rows = plan.part_rows;
     a.opart = static_cast<float*>(workspace);
     a.lpart = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.opart_bytes);
   }

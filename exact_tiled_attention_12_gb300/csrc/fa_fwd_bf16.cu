@@ -26,6 +26,8 @@
 // still exact.  When it moves, the softmax thread rescales its row of O_t in
 // tensor memory; the commit that signalled S_t also guarantees the previous
 // O_t += P_t V product has finished.
+#include <cmath>
+
 #include "fa_kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -160,29 +162,38 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
   const int Nq = a.Nq, Nk = a.Nk;
   const int off = Nk - Nq;                               // causal: query i sees keys j ≤ i + off
   const int pairs = (Nq + 2 * kBM - 1) / (2 * kBM);      // two-tile units per head
-  // Work of this CTA (1-D grid).  Causal: batch·head fastest with the
-  // heaviest pairs first across the whole grid (longest tiles scheduled
-  // first).  Non-causal: head-major (pair fastest), so a wave touches few
-  // heads' K/V and they stay in L2; the last `tail` units are split into
-  // `splits` CTAs over equal K/V sub-ranges, each writing a partial result
-  // (normalised O and LSE of its keys) that fwd_combine merges.
+  // Work of this CTA (1-D grid).  Causal without a split: batch·head fastest
+  // with the heaviest pairs first across the whole grid (longest tiles
+  // scheduled first).  Otherwise head-major (pair fastest), so a wave touches
+  // few heads' K/V and they stay in L2; units [n_full, units) are split into
+  // `splits` CTAs over equal ranges of the K/V tiles they see, each writing a
+  // partial result (normalised O and LSE of its keys) that fwd_combine
+  // merges: the last partial wave of a long problem, or every unit of a
+  // problem with few queries (which streams K/V far more than it computes).
   const int n_kv_all = (Nk + kBN - 1) / kBN;
   int bh, pair, kv_begin = 0, n_kv = n_kv_all, part_slot = -1;
   const int idx = (int)blockIdx.x;
-  if (CAUSAL) {
+  if (CAUSAL && a.splits <= 1) {
     bh = idx % (a.B * a.H);
     pair = pairs - 1 - idx / (a.B * a.H);
   } else if (idx < a.n_full) {
     bh = idx / pairs;
     pair = idx % pairs;
   } else {
-    part_slot = idx - a.n_full;                            // = tail unit · splits + part
+    part_slot = idx - a.n_full;                            // = split unit · splits + part
     const int unit = a.n_full + part_slot / a.splits;
     const int part = part_slot % a.splits;
     bh = unit / pairs;
     pair = unit % pairs;
-    kv_begin = part * n_kv / a.splits;
-    n_kv = (part + 1) * n_kv / a.splits - kv_begin;
+    // K/V tiles the unit's queries see: all of them without the mask; with
+    // it, up to the last key of the unit's last query.
+    int n_vis = n_kv_all;
+    if (CAUSAL) {
+      const int last_q = pair * 2 * kBM + 2 * kBM - 1 < Nq ? pair * 2 * kBM + 2 * kBM - 1 : Nq - 1;
+      n_vis = (last_q + off) / kBN + 1;
+    }
+    kv_begin = part * n_vis / a.splits;
+    n_kv = (part + 1) * n_vis / a.splits - kv_begin;
   }
   const int q0 = pair * 2 * kBM;
   const int row0 = bh * Nq;                                // first row of this head in the [B·H·Nq, d] view
@@ -221,8 +232,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
   for (int t = 0; t < 2; ++t) {
     const int qt = q0 + t * kBM;
     const int last_key = (qt + kBM - 1 < Nq ? qt + kBM - 1 : Nq - 1) + off;
-    n_t[t] = qt >= Nq ? 0 : (CAUSAL ? last_key / kBN + 1 : n_kv);
-    first_masked[t] = (qt + off + 1) / kBN;
+    // K/V tiles this query tile visits within [kv_begin, kv_begin + n_kv),
+    // and the first of them (relative to kv_begin) that masks a score.
+    int vis = CAUSAL ? last_key / kBN + 1 - kv_begin : n_kv;
+    vis = vis < 0 ? 0 : (vis > n_kv ? n_kv : vis);
+    n_t[t] = qt >= Nq ? 0 : vis;
+    first_masked[t] = (qt + off + 1) / kBN - kv_begin;
   }
   const int J = n_t[0] > n_t[1] ? n_t[0] : n_t[1];
 
@@ -278,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
       if (CAUSAL && j >= fm) {
         // A tile crossing the diagonal: key 128j + c is visible to query
         // qt + r iff c ≤ r + qt + off − 128j (c ≤ r for square problems).
-        const int lim = r + qt + off - j * kBN;
+        const int lim = r + qt + off - (kv_begin + j) * kBN;
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c > lim) s[c] = f2u(-INFINITY);
@@ -359,20 +374,25 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
           }
           if (live) a.lse[(size_t)row0 + (size_t)q] = lse;
         } else {
-          // Partial over this CTA's keys: normalised O and LSE in fp32.
-          const size_t prow = (size_t)part_slot * (2 * kBM) + (size_t)(t * kBM + r);
+          // Partial over this CTA's keys: normalised O and LSE in fp32, one
+          // row per query of the unit that exists (a slot holds part_rows
+          // rows: 256, or the query count of a problem with few queries).
+          const int urow = t * kBM + r;
+          const bool live = urow < a.part_rows && q < Nq;
+          const size_t prow = (size_t)part_slot * (size_t)a.part_rows + (size_t)urow;
           float* orow = a.opart + prow * DR;
 #pragma unroll
           for (int cc = 0; cc < DR / 32; ++cc) {
             if (!dcheck(tmem_ok(o_col(t) + 32 * cc, 32, 512), wc, kChkTmem, 6)) continue;
             uint32_t o[32];
-            tmem_ld_x32(tmem + lane_off + o_col(t) + 32 * cc, o);
+            tmem_ld_x32(tmem + lane_off + o_col(t) + 32 * cc, o);   // warp-collective: every lane loads
+            if (!live) continue;
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4)
               st_global_v4(orow + 32 * cc + 4 * v4, f2u(u2f(o[4 * v4]) * inv), f2u(u2f(o[4 * v4 + 1]) * inv),
                            f2u(u2f(o[4 * v4 + 2]) * inv), f2u(u2f(o[4 * v4 + 3]) * inv));
           }
-          a.lpart[prow] = lse;
+          if (live) a.lpart[prow] = lse;
         }
       }
     }
@@ -502,10 +522,10 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long long units = (long long)fwd_units(a.B, a.H, a.Nq, DR);
-  const long long ctas = CAUSAL ? units : a.n_full + (units - a.n_full) * a.splits;
+  const long long ctas = a.splits > 1 ? a.n_full + (units - a.n_full) * a.splits : units;
   kern<<<(unsigned)ctas, kThreads, smem, s>>>(a);
   e = cudaGetLastError();
-  if (e != cudaSuccess || CAUSAL || a.splits <= 1 || a.n_full >= units) return e;
+  if (e != cudaSuccess || a.splits <= 1 || a.n_full >= units) return e;
   return launch_fwd_combine(a, (int)(units - a.n_full), 2 * kBM, s);
 }
 
@@ -515,32 +535,33 @@ cudaError_t launch_impl(const FwdArgs& a, cudaStream_t s) {
 // O = Σ_k e^{L_k − L} O_k.  One warp per row; lanes over the head dims.
 // A work unit covers `unit_rows` query rows of one head (256 for the
 // two-tile kernel, 128 at d = 256); partial row p of unit slot u·splits + k
-// is opart row (u·splits + k)·unit_rows + p.
+// is opart row (u·splits + k)·part_rows + p, for the part_rows ≤ unit_rows
+// rows a slot holds.
 template <int DR, bool F16>
 __global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restrict__ opart,
                                                           const float* __restrict__ lpart, uint16_t* __restrict__ o,
                                                           float* __restrict__ lse, int Nq, int n_full, int splits,
-                                                          int tail, int unit_rows) {
+                                                          int tail, int unit_rows, int part_rows) {
   constexpr int V = DR / 32;   // consecutive head dims per lane
   const int row = (int)(blockIdx.x * 8 + (threadIdx.x >> 5));
   const int lane = threadIdx.x & 31;
-  if (row >= tail * unit_rows) return;
-  const int u = row / unit_rows, rr = row % unit_rows;
+  if (row >= tail * part_rows) return;
+  const int u = row / part_rows, rr = row % part_rows;
   const int per_head = (Nq + unit_rows - 1) / unit_rows;
   const int unit = n_full + u;
   const int q = (unit % per_head) * unit_rows + rr;
   if (q >= Nq) return;
   const size_t orow = (size_t)(unit / per_head) * Nq + (size_t)q;
   float mx = -INFINITY;
-  for (int k = 0; k < splits; ++k) mx = fmaxf(mx, lpart[(size_t)(u * splits + k) * unit_rows + rr]);
+  for (int k = 0; k < splits; ++k) mx = fmaxf(mx, lpart[(size_t)(u * splits + k) * part_rows + rr]);
   float sum = 0.f;
-  for (int k = 0; k < splits; ++k) sum += expf(lpart[(size_t)(u * splits + k) * unit_rows + rr] - mx);
+  for (int k = 0; k < splits; ++k) sum += expf(lpart[(size_t)(u * splits + k) * part_rows + rr] - mx);
   const float total = mx + logf(sum);
   float acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
   for (int k = 0; k < splits; ++k) {
-    const size_t pr = (size_t)(u * splits + k) * unit_rows + rr;
+    const size_t pr = (size_t)(u * splits + k) * part_rows + rr;
     const float w = expf(lpart[pr] - total);
     const float* src = opart + pr * DR + lane * V;
 #pragma unroll
@@ -559,9 +580,9 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(const float* __restric
 
 template <int DR, bool F16>
 cudaError_t combine_impl(const FwdArgs& a, int tail, int unit_rows, cudaStream_t s) {
-  const int rows = tail * unit_rows;
+  const int rows = tail * a.part_rows;
   fwd_combine_kernel<DR, F16><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
-      a.opart, a.lpart, static_cast<uint16_t*>(a.o), a.lse, a.Nq, a.n_full, a.splits, tail, unit_rows);
+      a.opart, a.lpart, static_cast<uint16_t*>(a.o), a.lse, a.Nq, a.n_full, a.splits, tail, unit_rows, a.part_rows);
   return cudaGetLastError();
 }
 
@@ -608,6 +629,26 @@ void fwd_split_plan(int units, int num_sms, int n_kv, int* n_full, int* splits) 
   if (s < 2) return;
   *splits = s;
   *n_full = units - tail;
+}
+
+int fwd_split_short(int units, int num_sms, int n_kv) {
+  // Parts of at least 8 K/V tiles (shorter ones cost more in start-up than
+  // they spread) and at most 16; among those, the count whose grid fills its
+  // last wave best, with fewer than two waves weighed down (the CTAs of one
+  // wave finish at different times too); ties (within 1 %) go to fewer parts.
+  if (num_sms <= 0 || units <= 0) return 1;
+  int best = 1;
+  double best_score = -1.0;
+  for (int s = 1; s <= 16 && n_kv / s >= 8; ++s) {
+    const double waves = (double)units * s / num_sms;
+    double score = waves / std::ceil(waves);
+    if (waves < 2.0) score *= waves / 2.0;
+    if (score > best_score * 1.01) {
+      best_score = score;
+      best = s;
+    }
+  }
+  return best;
 }
 
 size_t fwd_bf16_smem_bytes(int d) {

@@ -324,19 +324,21 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_d256_kernel(const __grid_c
           if (live && c == 0) a.lse[(size_t)row0 + (size_t)q] = lse;
         } else {
           // Partial over this CTA's keys: normalised O and LSE in fp32.
-          const size_t prow = (size_t)part_slot * kBM + (size_t)r;
+          const bool live_part = r < a.part_rows && q < Nq;
+          const size_t prow = (size_t)part_slot * (size_t)a.part_rows + (size_t)r;
           float* orow = a.opart + prow * kD + 128 * c;
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t o[32];
             if (!dcheck(tmem_ok(256u + 128u * c + 32u * cc, 32, 512), wc, kChkTmem, 36)) continue;
-            tmem_ld_x32(tmem + lane_off + 256u + 128u * (uint32_t)c + 32u * (uint32_t)cc, o);
+            tmem_ld_x32(tmem + lane_off + 256u + 128u * (uint32_t)c + 32u * (uint32_t)cc, o);   // warp-collective
+            if (!live_part) continue;
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4)
               st_global_v4(orow + 32 * cc + 4 * v4, f2u(u2f(o[4 * v4]) * inv), f2u(u2f(o[4 * v4 + 1]) * inv),
                            f2u(u2f(o[4 * v4 + 2]) * inv), f2u(u2f(o[4 * v4 + 3]) * inv));
           }
-          if (c == 0) a.lpart[prow] = lse;
+          if (c == 0 && live_part) a.lpart[prow] = lse;
         }
       }
     }

@@ -53,11 +53,14 @@ struct FwdArgs {
   float scale_log2;       // scale · log2(e): scores are handled in base 2
   int causal;
   unsigned int* fault;
-  // Non-causal load balancing: units [0, n_full) run whole; each of the
-  // remaining units runs as `splits` CTAs over K/V sub-ranges writing fp32
-  // partials (opart [slots·unit_rows, d], lpart [slots·unit_rows]) that a
-  // combine kernel merges.  splits = 1 (or n_full = all units) disables it.
-  int n_full, splits;
+  // Load balancing: units [0, n_full) run whole; each of the remaining
+  // units runs as `splits` CTAs over K/V sub-ranges writing fp32 partials
+  // (opart [slots·part_rows, d], lpart [slots·part_rows]; part_rows ≤ the
+  // unit's rows: every row of a unit, or only the queries that exist when a
+  // problem has at most 128) that a combine kernel merges.  splits = 1 (or
+  // n_full = all units) disables it.  Under the causal mask only problems
+  // with at most 128 queries split (the d ≤ 128 kernel).
+  int n_full, splits, part_rows;
   float* opart;
   float* lpart;
 };
@@ -67,6 +70,9 @@ int fwd_units(int B, int H, int Nq, int d);
 // Split plan for `units` equal units of `n_kv` K/V tiles on `num_sms` SMs: the
 // units of the last, partial wave are split when that fills the GPU better.
 void fwd_split_plan(int units, int num_sms, int n_kv, int* n_full, int* splits);
+// Parts per unit for a problem with at most 128 queries and fewer units
+// than SMs, every unit split over its n_kv visible K/V tiles.
+int fwd_split_short(int units, int num_sms, int n_kv);
 size_t fwd_bf16_smem_bytes(int d);
 // Dispatches on d (64, 96, 128; 256 goes to launch_fwd_d256).
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s);

@@ -228,3 +228,48 @@ def test_d96_kv_and_split(dtype, causal):
         gpu = _run(q, k, v, do, causal)
         ref = run_oracle_heads(q, k, v, do, causal, 96 ** -0.5, _heads(B, H))
         compare({key: val.reshape((-1,) + val.shape[2:]) for key, val in gpu.items()}, ref, dtype)
+
+
+# ------------------------------------------------------------------ few queries over many keys
+#
+# With 2 to 128 queries per head and fewer units than SMs, every unit of the
+# forward is split over ranges of its K/V tiles (with and without the mask;
+# d = 256 only without) and merged on the device; each part keeps one
+# partial row per query.
+
+SHORT_SHAPES = [
+    # B, H, Nq, Nk, d
+    (2, 4, 16, 4096, 128),
+    (1, 3, 2, 2000, 64),     # two queries, ragged keys
+    (1, 2, 128, 2048, 128),  # a full 128-query tile (16 K/V tiles: two parts of 8)
+    (1, 2, 100, 2100, 96),   # d = 96, ragged
+    (4, 8, 7, 3000, 128),    # more heads, ragged
+    (1, 2, 16, 2048, 256),   # d = 256 (split without the mask only)
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d", SHORT_SHAPES)
+@pytest.mark.parametrize("causal", [False, True])
+def test_few_queries_split_over_keys(B, H, Nq, Nk, d, causal):
+    import exact_tiled_attention_12_gb300 as fa
+
+    splits = fa.fwd_workspace_size(B, H, Nq, d, causal, torch.bfloat16, Nk=Nk) > 0
+    assert splits == (not (causal and d == 256))   # every shape here has fewer units than SMs
+    q, k, v, do = make_inputs_kv(B, H, Nq, Nk, d, "bf16", "normal", 300 + Nq + Nk + d, device="cuda")
+    gpu = _run(q, k, v, do, causal)
+    ref = run_oracle_heads(q, k, v, do, causal, d ** -0.5, _heads(B, H))
+    compare({key: val.reshape((-1,) + val.shape[2:]) for key, val in gpu.items()}, ref, "bf16")
+
+
+def test_few_queries_split_equals_unsplit_forward():
+    """The split forward (workspace given) and the whole-unit forward (no
+    workspace) agree on O within bf16 rounding and on LSE within 1e-5."""
+    import exact_tiled_attention_12_gb300 as fa
+
+    q, k, v, _ = make_inputs_kv(2, 8, 16, 8192, 128, "bf16", "normal", 77, device="cuda")
+    for causal in (False, True):
+        o1, l1 = fa.fwd(q, k, v, causal=causal)
+        o2, l2 = fa.fwd(q, k, v, causal=causal, workspace=False)
+        assert fa.sync_status() == 0
+        assert float((o1.float() - o2.float()).abs().max()) <= 2 ** -8
+        assert float((l1 - l2).abs().max()) <= 1e-5

@@ -110,6 +110,7 @@ class NvmlClockSampler:
             tag = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
             found = self.lib.nvmlDeviceGetHandleByUUID(tag.encode(), ctypes.byref(self.h)) == 0
         if not found and self.lib.nvmlDeviceGetHandleByIndex_v2(device.index, ctypes.byref(self.h)) != 0:
+            self.lib.nvmlShutdown()
             raise OSError("no NVML handle for the device")
         self._reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
             self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
@@ -141,6 +142,7 @@ class NvmlClockSampler:
     def stop(self):
         self._stop.set()
         self._thread.join()
+        self.lib.nvmlShutdown()
         sm = [m for m, _ in self.samples]
         reasons = sorted({name for _, bits in self.samples for b, name in _REASON_BITS.items() if bits & b})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_min_mhz": min(sm) if sm else None,

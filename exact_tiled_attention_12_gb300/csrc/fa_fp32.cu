@@ -11,7 +11,10 @@
 // Each warp owns one output row (a query row in the forward and in the dQ
 // pass, a key row in the dK/dV pass); lane j scores key/query j of the
 // current 32-row block staged in shared memory, and each lane accumulates
-// head dimensions lane, lane+32, lane+64, lane+96.
+// head dimensions lane, lane+32, lane+64, lane+96.  The next 32-row block is
+// fetched into registers while the current one is used, so its global-load
+// latency overlaps the arithmetic (these problems are small and latency
+// bound: one load round trip per block instead of one per element).
 #include "fa_kernels.h"
 
 namespace fa {
@@ -33,14 +36,57 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-// Stages rows [r0, r0 + 32) of a [N, d] matrix into shared memory with a
-// padded stride of d + 1 floats (rows past N are zero).
-__device__ __forceinline__ void stage_rows(float* dst, const float* src, int r0, int N, int d) {
-  const int ld = d + 1;
-  for (int idx = threadIdx.x; idx < kTile * d; idx += blockDim.x) {
-    const int r = idx / d, c = idx - r * d;
-    dst[r * ld + c] = (r0 + r < N) ? src[(size_t)(r0 + r) * d + c] : 0.f;
+constexpr int kThreadsF32 = 32 * kRowsPerBlock;
+constexpr int kBlockRegs = kTile * kMaxD / kThreadsF32;   // floats of one 32-row block per thread
+
+// Rows [r0, r0 + 32) of a row-major [N, d] matrix, held in registers: the
+// block is 32·d contiguous floats and thread t holds elements t, t + 256, …
+// (rows past N read as zero).
+struct RowBlock {
+  float x[kBlockRegs];
+};
+
+__device__ __forceinline__ void fetch_rows(RowBlock& b, const float* __restrict__ src, int r0, int N, int d) {
+  const int n = min(N - r0, kTile) * d;
+  const float* base = src + (size_t)r0 * d;
+#pragma unroll
+  for (int u = 0; u < kBlockRegs; ++u) {
+    const int idx = (int)threadIdx.x + u * kThreadsF32;
+    b.x[u] = idx < n ? base[idx] : 0.f;
   }
+}
+
+// Writes a fetched block into shared memory with a padded row stride of
+// d + 1 floats (element idx goes to row idx / d, column idx % d; both are
+// stepped, not divided, per element).
+__device__ __forceinline__ void put_rows(float* dst, const RowBlock& b, int d) {
+  const int ld = d + 1;
+  const int step_r = kThreadsF32 / d, step_c = kThreadsF32 % d;
+  int r = (int)threadIdx.x / d, c = (int)threadIdx.x % d;
+#pragma unroll
+  for (int u = 0; u < kBlockRegs; ++u) {
+    if (r < kTile) dst[r * ld + c] = b.x[u];
+    r += step_r;
+    c += step_c;
+    if (c >= d) {
+      c -= d;
+      ++r;
+    }
+  }
+}
+
+// Σ_c a[c]·b[c] over d terms with four independent partial sums.
+__device__ __forceinline__ float dot_f32(const float* a, const float* b, int d) {
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+  int c = 0;
+  for (; c + 4 <= d; c += 4) {
+    s0 = fmaf(a[c], b[c], s0);
+    s1 = fmaf(a[c + 1], b[c + 1], s1);
+    s2 = fmaf(a[c + 2], b[c + 2], s2);
+    s3 = fmaf(a[c + 3], b[c + 3], s3);
+  }
+  for (; c < d; ++c) s0 = fmaf(a[c], b[c], s0);
+  return (s0 + s1) + (s2 + s3);
 }
 
 // Forward.  grid = (ceil(Nq / 8), B·H); one warp per query row.
@@ -67,20 +113,23 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) fwd_f32_kernel(const float
   const int key_end = causal ? last_row + off + 1 : Nk;   // keys any row of this block can see
   float m = -INFINITY, ell = 0.f;
   float acc[kMaxD / 32] = {0.f, 0.f, 0.f, 0.f};
+  RowBlock nk, nv;   // the next block of K and V, in flight
+  fetch_rows(nk, kh, 0, Nk, d);
+  fetch_rows(nv, vh, 0, Nk, d);
   for (int j0 = 0; j0 < key_end; j0 += kTile) {
+    __syncthreads();   // every warp is done with the previous block
+    put_rows(sK, nk, d);
+    put_rows(sV, nv, d);
     __syncthreads();
-    stage_rows(sK, kh, j0, Nk, d);
-    stage_rows(sV, vh, j0, Nk, d);
-    __syncthreads();
+    if (j0 + kTile < key_end) {
+      fetch_rows(nk, kh, j0 + kTile, Nk, d);
+      fetch_rows(nv, vh, j0 + kTile, Nk, d);
+    }
     if (!live) continue;
     const int j = j0 + lane;
     const bool vis = j < Nk && (!causal || j <= i + off);
     float s = -INFINITY;
-    if (vis) {
-      float dot = 0.f;
-      for (int c = 0; c < d; ++c) dot = fmaf(sQ[warp * d + c], sK[lane * ld + c], dot);
-      s = dot * scale;
-    }
+    if (vis) s = dot_f32(sQ + warp * d, sK + lane * ld, d) * scale;
     const float mt = warp_max(s);
     if (mt == -INFINITY) continue;            // nothing visible in this block (warp-uniform)
     const float m_new = fmaxf(m, mt);
@@ -153,21 +202,25 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) dq_f32_kernel(
   const int last_row = min(Nq - 1, (int)blockIdx.x * kRowsPerBlock + kRowsPerBlock - 1);
   const int key_end = causal ? last_row + off + 1 : Nk;
   float acc[kMaxD / 32] = {0.f, 0.f, 0.f, 0.f};
+  RowBlock nk, nv;   // the next block of K and V, in flight
+  fetch_rows(nk, k + kbase, 0, Nk, d);
+  fetch_rows(nv, v + kbase, 0, Nk, d);
   for (int j0 = 0; j0 < key_end; j0 += kTile) {
     __syncthreads();
-    stage_rows(sK, k + kbase, j0, Nk, d);
-    stage_rows(sV, v + kbase, j0, Nk, d);
+    put_rows(sK, nk, d);
+    put_rows(sV, nv, d);
     __syncthreads();
+    if (j0 + kTile < key_end) {
+      fetch_rows(nk, k + kbase, j0 + kTile, Nk, d);
+      fetch_rows(nv, v + kbase, j0 + kTile, Nk, d);
+    }
     if (!live) continue;
     const int j = j0 + lane;
     const bool vis = j < Nk && (!causal || j <= i + off);
     float ds = 0.f;
     if (vis) {
-      float s = 0.f, dp = 0.f;
-      for (int c = 0; c < d; ++c) {
-        s = fmaf(sQ[warp * d + c], sK[lane * ld + c], s);
-        dp = fmaf(sG[warp * d + c], sV[lane * ld + c], dp);
-      }
+      const float s = dot_f32(sQ + warp * d, sK + lane * ld, d);
+      const float dp = dot_f32(sG + warp * d, sV + lane * ld, d);
       const float p = expf(s * scale - Li);
       ds = p * (dp - Di);
     }
@@ -218,26 +271,35 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) dkv_f32_kernel(
   const int q_begin = causal ? (max(first_key - off, 0) / kTile) * kTile : 0;
   float acc_v[kMaxD / 32] = {0.f, 0.f, 0.f, 0.f};
   float acc_k[kMaxD / 32] = {0.f, 0.f, 0.f, 0.f};
+  RowBlock nq, ng;   // the next block of Q and dO, in flight
+  float nl = 0.f, nd = 0.f;
+  auto fetch = [&](int i0) {
+    fetch_rows(nq, q + qbase, i0, Nq, d);
+    fetch_rows(ng, dO + qbase, i0, Nq, d);
+    if (threadIdx.x < kTile) {
+      const int ii = i0 + (int)threadIdx.x;
+      nl = ii < Nq ? lse[head * Nq + ii] : 0.f;
+      nd = ii < Nq ? dvec[head * Nq + ii] : 0.f;
+    }
+  };
+  if (q_begin < Nq) fetch(q_begin);
   for (int i0 = q_begin; i0 < Nq; i0 += kTile) {
     __syncthreads();
-    stage_rows(sQ, q + qbase, i0, Nq, d);
-    stage_rows(sG, dO + qbase, i0, Nq, d);
+    put_rows(sQ, nq, d);
+    put_rows(sG, ng, d);
     if (threadIdx.x < kTile) {
-      const int ii = i0 + threadIdx.x;
-      sL[threadIdx.x] = ii < Nq ? lse[head * Nq + ii] : 0.f;
-      sD[threadIdx.x] = ii < Nq ? dvec[head * Nq + ii] : 0.f;
+      sL[threadIdx.x] = nl;
+      sD[threadIdx.x] = nd;
     }
     __syncthreads();
+    if (i0 + kTile < Nq) fetch(i0 + kTile);
     if (!live) continue;
     const int i = i0 + lane;
     const bool vis = i < Nq && (!causal || j <= i + off);
     float p = 0.f, ds = 0.f;
     if (vis) {
-      float s = 0.f, dp = 0.f;
-      for (int c = 0; c < d; ++c) {
-        s = fmaf(sQ[lane * ld + c], sK[warp * d + c], s);
-        dp = fmaf(sG[lane * ld + c], sV[warp * d + c], dp);
-      }
+      const float s = dot_f32(sQ + lane * ld, sK + warp * d, d);
+      const float dp = dot_f32(sG + lane * ld, sV + warp * d, d);
       p = expf(s * scale - sL[lane]);
       ds = p * (dp - sD[lane]);
     }

@@ -31,8 +31,11 @@
 // and query columns 64(w/4)..+63); warps 8-11 drain each tile's dQ from
 // tensor memory into the fp32 accumulator with global reductions, so those
 // run while the compute warps work on the next tile; warp 12 issues TMA,
-// warp 13 issues the MMAs and owns tensor memory.  The grid is head-major
-// (K/V tile fastest).
+// warp 13 issues the MMAs (except dK) and owns tensor memory, warp 14
+// issues dK += dSᵀ Q once warp 13 has issued the next Sᵀ — the products
+// keep their order in the pipe, and the main issuing thread, which sets the
+// pace (clock64 traces on GB300), has 8 fewer products a step (+1.4 %).  The
+// grid is head-major (K/V tile fastest).
 #include "fa_kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -45,8 +48,9 @@ constexpr int kThreads = 512;       // four warpgroups
 constexpr int kComputeWarps = 8;    // warpgroups 0, 1: Pᵀ and dSᵀ
 constexpr int kRedWarp = 8;         // warpgroup 2: dQ reductions
 constexpr int kRedWarps = 4;
-constexpr int kTmaWarp = 12;        // warpgroup 3: TMA, MMA (warps 14, 15 idle)
+constexpr int kTmaWarp = 12;        // warpgroup 3: TMA, MMA, dK MMA (warp 15 idle)
 constexpr int kMmaWarp = 13;
+constexpr int kDkWarp = 14;
 // Registers per thread of each warpgroup (setmaxnreg).  The CTA's pool is
 // fixed at launch: kThreads × (65536 / kThreads) = 65536; the four
 // warpgroups' shares must fit in it or an increase would wait forever.
@@ -96,7 +100,10 @@ struct BwdBars {
   static constexpr int kDqDrained = kSFull + 4;
   static constexpr int kDKVFull = kSFull + 5;
   static constexpr int kMmaDone = kSFull + 6;
-  static constexpr int kNumBars = kSFull + 7;
+  static constexpr int kSIssued = kSFull + 7;    // warp 13 has issued step i's products before dK
+  static constexpr int kDkDone = kSFull + 8;     // dK of step i done: dSᵀ may be overwritten
+  static constexpr int kMmaDone2 = kSFull + 9;   // every product of the dK warp has finished
+  static constexpr int kNumBars = kSFull + 10;
   static_assert(8 * kNumBars + 8 <= 256, "barrier block too small");
 };
 
@@ -157,11 +164,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
   constexpr int D = DR <= 64 ? 64 : 128;
   using C = BwdCfg<D>;
   constexpr int QS = C::kQS;
+  // dK from its own warp where it measured faster (the 128-column layout:
+  // d = 96, 128); at d = 64 the extra hand-over costs more than it saves.
+  constexpr bool kDkSplit = D == 128;
   using Bar = BwdBars<QS>;
   constexpr int kKVFull = Bar::kKVFull, kQFull = Bar::kQFull, kQEmpty = Bar::kQEmpty, kSFull = Bar::kSFull,
                 kDPFull = Bar::kDPFull, kPdsFull = Bar::kPdsFull, kDqFull = Bar::kDqFull,
                 kDqDrained = Bar::kDqDrained, kDKVFull = Bar::kDKVFull, kMmaDone = Bar::kMmaDone,
-                kNumBars = Bar::kNumBars;
+                kNumBars = Bar::kNumBars, kSIssued = Bar::kSIssued, kDkDone = Bar::kDkDone, kMmaDone2 = Bar::kMmaDone2;
   // Dynamic shared memory starts on a 1024-byte boundary (no static shared
   // memory is declared); 128-byte swizzled tiles need that alignment.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -233,14 +243,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
     mbar_init(bar(kKVFull), 1);
     for (int s = 0; s < QS; ++s) {
       mbar_init(bar(kQFull + s), 1);
-      mbar_init(bar(kQEmpty + s), 1 + 32 * kComputeWarps);
+      mbar_init(bar(kQEmpty + s), (kDkSplit ? 2 : 1) + 32 * kComputeWarps);   // the issuing thread(s), the compute warps
     }
     mbar_init(bar(kSFull), 1);
     mbar_init(bar(kDPFull), 1);
     mbar_init(bar(kPdsFull), 32 * kComputeWarps);
     mbar_init(bar(kDqFull), 1);
     mbar_init(bar(kDqDrained), 32 * kRedWarps);
-    mbar_init(bar(kDKVFull), 1);
+    mbar_init(bar(kDKVFull), kDkSplit ? 2 : 1);   // dV (warp 13) and dK (warp 14, or 13)
+    mbar_init(bar(kSIssued), 1);
+    mbar_init(bar(kDkDone), 1);
+    mbar_init(bar(kMmaDone2), 1);
     mbar_init(bar(kMmaDone), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -327,6 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         if (dcheck(tmem_ok(C::kColS + h * 32 + 16 * half, 16, 512), wc, kChkTmem, 19))
           tmem_st_x16(tmem + lane_off + C::kColS + (uint32_t)(h * 32 + 16 * half), pk);
       }
+      // dK of the previous step reads dSᵀ from shared memory: it must be done
+      // before this step's dSᵀ is written there.
+      if (kDkSplit && i > 0) mbar_wait_inl(bar(kDkDone), (uint32_t)((i - 1) & 1), wc, site(15));
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int c0 = h * 64 + ch * 32;
@@ -581,11 +597,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
           issue_sd(i + 1, C::kColS, sbase + C::kK);
           tc_commit(bar(kSFull));
         }
-        // dK += dSᵀ Q
+        if constexpr (kDkSplit) {
+          // dK += dSᵀ Q of this step is issued by warp 14, after these products.
+          mbar_arrive(bar(kSIssued));
+        } else {
 #pragma unroll
-        for (int ks = 0; ks < kBM / 16; ++ks)
-          if (chk) mma_ss(tmem + C::kColDK, sdesc_sw128(ds + (uint32_t)((ks >> 2) * kBox + (ks & 3) * 32), 16, 1024),
-                 sdesc_sw128(qb + (uint32_t)(ks * 2048), kBox, 1024), kIdKV, (i > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < kBM / 16; ++ks)
+            if (chk) mma_ss(tmem + C::kColDK, sdesc_sw128(ds + (uint32_t)((ks >> 2) * kBox + (ks & 3) * 32), 16, 1024),
+                   sdesc_sw128(qb + (uint32_t)(ks * 2048), kBox, 1024), kIdKV, (i > 0 || ks > 0) ? 1u : 0u);
+        }
         tc_commit(bar(kQEmpty + st));
         if (next) {
           if (!mbar_wait_inl(bar(kDqDrained), (uint32_t)(i & 1), wc, site(13))) {
@@ -607,8 +627,40 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
     named_bar_sync(kEndBarrier, kThreads);
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  } else if (kDkSplit && warp == kDkWarp) {
+    // ------------------------------------------------------------ dK issuer
+    // dK += dSᵀ Q of step i, once warp 13 has issued step i's dQ, dV and the
+    // next Sᵀ (so the pipe sees the products in the single-thread order).
+    if (lane == 0) {
+      constexpr uint32_t kIdKV = idesc_f16kind(128, DR, false, true, F16);
+      bool ok = true;
+      for (int i = 0; ok && i < n; ++i) {
+        const int st = i % QS;
+        if (!mbar_wait_inl(bar(kSIssued), (uint32_t)(i & 1), wc, site(16))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ds = sbase + C::kDS;
+        const uint32_t qb = sbase + C::kQ + st * C::kTile;
+        const bool chk = dcheck(tmem_ok(C::kColDK, DR, 512), wc, kChkTmem, 27) &&
+                         dcheck(smem_ok(C::kDS, 2 * kBox, C::kBar, 1024) && smem_ok(qb - sbase, C::kTile, C::kBar, 1024),
+                                wc, kChkSmem, 27);
+#pragma unroll
+        for (int ks = 0; ks < kBM / 16; ++ks)
+          if (chk) mma_ss(tmem + C::kColDK, sdesc_sw128(ds + (uint32_t)((ks >> 2) * kBox + (ks & 3) * 32), 16, 1024),
+                 sdesc_sw128(qb + (uint32_t)(ks * 2048), kBox, 1024), kIdKV, (i > 0 || ks > 0) ? 1u : 0u);
+        tc_commit(bar(kDkDone));
+        tc_commit(bar(kQEmpty + st));
+      }
+      if (ok) tc_commit(bar(kDKVFull));
+      tc_commit(bar(kMmaDone2));
+      mbar_wait_drain_inl(bar(kMmaDone2), 0, wc, site(17));
+    }
+    __syncwarp();
+    named_bar_arrive(kEndBarrier, kThreads);
   } else {
-    named_bar_arrive(kEndBarrier, kThreads);   // warps 14, 15
+    named_bar_arrive(kEndBarrier, kThreads);   // warp 15 (and 14 at d = 64)
   }
   }
   // No code after the roles: their register counts differ (setmaxnreg).

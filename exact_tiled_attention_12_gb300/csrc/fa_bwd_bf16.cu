@@ -414,10 +414,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
     const uint32_t lane_off = (uint32_t)(g * 32) << 16;
     // Pacing of the reductions issued after the columns are released: they
     // run beside the next dPᵀ product and the compute warps' next tile, and
-    // issued in one burst they slow both (measured on GB300: +8 % for the
-    // whole backward when spread).  Each thread sleeps between groups of 8
-    // so that its 64 reductions span about a third of the previous step, as
-    // timed between its own dQ hand-overs (no pause on the first step).
+    // issued in one burst they slow both.  Each thread pauses after every 4
+    // floats it adds, so that its reductions span about a quarter of the
+    // previous step, as timed between its own dQ hand-overs (no pause on the
+    // first step).  Measured on GB300 against unpaced reductions: +10 % for
+    // the whole backward at d = 128 (7 longer pauses, after every 8 floats,
+    // gained 8 %), +4.5 % at d = 64.
     uint32_t t_prev = 0;
     uint32_t pause_ns = 0;
     for (int i = 0; i < n; ++i) {
@@ -426,11 +428,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       ok = __all_sync(kFull, ok);
       if (!ok) break;
       {
-        // 7 pauses of step / 40 (cycles read as ns at ~2 GHz: about a third
-        // of the step).  Pauses feed back into the step they are measured
-        // on: on GB300 step / 25 already ran away (the backward 15 % slower,
-        // step / 20 35 %), so the pause stays well short of that and is
-        // capped.  32-bit clock: the unsigned difference survives a wrap.
+        // 15 pauses of step / 120 (cycles read as ns at ~2 GHz: a quarter of
+        // the step; `pause_ns` holds step / 40 and is divided at each pause,
+        // a form that measured 0.5 % faster than holding step / 120).  Pauses
+        // feed back into the step they are measured on: on GB300, pauses
+        // adding up to ~60 % of the step already ran away (the backward 15 %
+        // slower, ~70 %: 35 %), and a third of the step after every 4 floats
+        // (step / 80) was slower than a quarter, so the share stays well short
+        // of that and each pause is capped.  32-bit clock: the unsigned
+        // difference survives a wrap.
         const uint32_t t_now = (uint32_t)clock();
         if (i > 0) {
           const uint32_t p = (t_now - t_prev) / 40u;
@@ -461,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
             red_add_f32(base + (size_t)(64 + c) * DR, u2f(v[c]));
-            if ((c & 7) == 7 && c < 63 && pause_ns > 0) __nanosleep(pause_ns);
+            if ((c & 3) == 3 && c < 63 && pause_ns > 0) __nanosleep(pause_ns / 3u);
           }
         } else {
           tc_fence_before();
@@ -478,7 +484,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         if (!chk) continue;
         float* base = a.dqacc + ((size_t)wrow0 + (size_t)q0 + (size_t)r) * D;
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) red_add_v4_f32(base + c, u2f(v[c]), u2f(v[c + 1]), u2f(v[c + 2]), u2f(v[c + 3]));
+        for (int c = 0; c < 64; c += 4) {
+          red_add_v4_f32(base + c, u2f(v[c]), u2f(v[c + 1]), u2f(v[c + 2]), u2f(v[c + 3]));
+          if (c < 60 && pause_ns > 0) __nanosleep(pause_ns / 3u);
+        }
       }
     }
     tc_fence_before();

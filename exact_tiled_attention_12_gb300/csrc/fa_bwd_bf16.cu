@@ -23,19 +23,26 @@
 //                     both read the dSᵀ tile and K MN-major from smem
 // Every product is M = 128 with N ≥ 64 (N = 128 except dV, dK, dQ at d = 64).
 //
-// Tensor memory (512 columns): dV [0, d), dK [d, 2d), Sᵀ/Pᵀ [2d, 2d+128),
-// dPᵀ/dQ [2d+128, 2d+256).  dQ reuses the dPᵀ columns once the compute warps
-// have read dPᵀ; the next dPᵀ waits until dQ has been drained.
+// Tensor memory (512 columns), d = 128: dV [0, 128), dK [128, 256), Sᵀ/Pᵀ
+// [256, 384), dPᵀ/dQᵀ [384, 512).  dQᵀ reuses the dPᵀ columns once the
+// compute warps have read dPᵀ; the next dPᵀ waits until dQᵀ has been
+// drained, and the next Sᵀ goes over Pᵀ right after dV.  d = 64: dV [0, 64),
+// dK [64, 128), two Sᵀ/Pᵀ buffers [128, 256) and [384, 512) used by
+// alternate tiles, dPᵀ [256, 384).  Tile i's dQ goes into the last 64
+// columns of its Sᵀ buffer (Pᵀ holds the first 64), so the next dPᵀ is
+// issued right after dQ and dK, and Sᵀ of tile i + 2 is issued into that
+// buffer once dV has read Pᵀ and dQ has been drained: the compute warps
+// find each tile's scores ready (measured on GB300: +5.9 % at d = 64).
 //
 // CTA: 16 warps.  Warps 0-7 compute Pᵀ/dSᵀ (warp w owns key rows 32(w%4)..+31
 // and query columns 64(w/4)..+63); warps 8-11 drain each tile's dQ from
 // tensor memory into the fp32 accumulator with global reductions, so those
 // run while the compute warps work on the next tile; warp 12 issues TMA,
-// warp 13 issues the MMAs (except dK) and owns tensor memory, warp 14
-// issues dK += dSᵀ Q once warp 13 has issued the next Sᵀ — the products
-// keep their order in the pipe, and the main issuing thread, which sets the
-// pace (clock64 traces on GB300), has 8 fewer products a step (+1.4 %).  The
-// grid is head-major (K/V tile fastest).
+// warp 13 issues the MMAs and owns tensor memory; at d = 128 warp 14 issues
+// dK += dSᵀ Q once warp 13 has issued the next Sᵀ — the products keep their
+// order in the pipe, and the main issuing thread, which sets the pace
+// (clock64 traces on GB300), has 8 fewer products a step (+1.4 %).  The grid
+// is head-major (K/V tile fastest).
 #include "fa_kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -66,9 +73,9 @@ constexpr int kPolyEvery = 0;
 
 template <int D>
 struct BwdCfg {
-  // Stages of the Q / dO / LSE / D ring (measured on GB300: four stages at
-  // d = 64, where shared memory has room for them, were slower than two).
-  static constexpr int kQS = 2;
+  // Stages of the Q / dO / LSE / D ring: d = 64 issues each Sᵀ two tiles
+  // ahead (a second Sᵀ buffer), so its ring holds three tiles.
+  static constexpr int kQS = D == 64 ? 3 : 2;
   // shared memory (offsets from a 1024-byte aligned base)
   static constexpr int kTile = 128 * D * 2;        // one 128 × D bf16 tile (D/64 boxes)
   static constexpr int kK = 0;
@@ -85,6 +92,8 @@ struct BwdCfg {
   static constexpr uint32_t kColDK = D;
   static constexpr uint32_t kColS = 2 * D;
   static constexpr uint32_t kColDP = 2 * D + 128;
+  // d = 64: a second Sᵀ buffer in the 128 columns the 64-wide accumulators leave free.
+  static constexpr uint32_t kColS2 = 2 * D + 256;
 };
 
 // Barrier slots (8 bytes each) inside the barrier block.
@@ -103,7 +112,8 @@ struct BwdBars {
   static constexpr int kSIssued = kSFull + 7;    // warp 13 has issued step i's products before dK
   static constexpr int kDkDone = kSFull + 8;     // dK of step i done: dSᵀ may be overwritten
   static constexpr int kMmaDone2 = kSFull + 9;   // every product of the dK warp has finished
-  static constexpr int kNumBars = kSFull + 10;
+  static constexpr int kSFull2 = kSFull + 10;    // the second Sᵀ buffer (d = 64)
+  static constexpr int kNumBars = kSFull + 11;
   static_assert(8 * kNumBars + 8 <= 256, "barrier block too small");
 };
 
@@ -167,11 +177,23 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
   // dK from its own warp where it measured faster (the 128-column layout:
   // d = 96, 128); at d = 64 the extra hand-over costs more than it saves.
   constexpr bool kDkSplit = D == 128;
+  // Two Sᵀ buffers where tensor memory has room for them (d = 64): step i
+  // uses buffer i mod 2, and the MMA thread issues Sᵀ of tile i + 2 as soon
+  // as dV of tile i has read its Pᵀ, so the compute warps find the next
+  // tile's scores ready when they finish a tile.
+  constexpr bool kSDouble = D == 64;
+  static_assert(kSDouble != kDkSplit, "the 64-column layout issues dK inline, the 128-column one from warp 14");
+  static_assert(!kSDouble || C::kColS2 + 128 <= 512, "second score buffer outside tensor memory");
   using Bar = BwdBars<QS>;
   constexpr int kKVFull = Bar::kKVFull, kQFull = Bar::kQFull, kQEmpty = Bar::kQEmpty, kSFull = Bar::kSFull,
                 kDPFull = Bar::kDPFull, kPdsFull = Bar::kPdsFull, kDqFull = Bar::kDqFull,
                 kDqDrained = Bar::kDqDrained, kDKVFull = Bar::kDKVFull, kMmaDone = Bar::kMmaDone,
-                kNumBars = Bar::kNumBars, kSIssued = Bar::kSIssued, kDkDone = Bar::kDkDone, kMmaDone2 = Bar::kMmaDone2;
+                kNumBars = Bar::kNumBars, kSIssued = Bar::kSIssued, kDkDone = Bar::kDkDone, kMmaDone2 = Bar::kMmaDone2,
+                kSFull2 = Bar::kSFull2;
+  // Sᵀ buffer of step i: its tensor-memory columns, its barrier and the parity of its use.
+  auto s_cols = [](int i) -> uint32_t { return (kSDouble && (i & 1)) ? C::kColS2 : C::kColS; };
+  auto s_bar_id = [](int i) -> int { return (kSDouble && (i & 1)) ? kSFull2 : kSFull; };
+  auto s_parity = [](int i) -> uint32_t { return kSDouble ? (uint32_t)((i >> 1) & 1) : (uint32_t)(i & 1); };
   // Dynamic shared memory starts on a 1024-byte boundary (no static shared
   // memory is declared); 128-byte swizzled tiles need that alignment.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -246,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       mbar_init(bar(kQEmpty + s), (kDkSplit ? 2 : 1) + 32 * kComputeWarps);   // the issuing thread(s), the compute warps
     }
     mbar_init(bar(kSFull), 1);
+    mbar_init(bar(kSFull2), 1);
     mbar_init(bar(kDPFull), 1);
     mbar_init(bar(kPdsFull), 32 * kComputeWarps);
     mbar_init(bar(kDqFull), 1);
@@ -290,7 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
       const int st = i % QS;
       const uint32_t par = (uint32_t)(i & 1);
       const int q0 = qtile(i) * kBM;
-      ok = mbar_wait_inl(bar(kSFull), par, wc, site(1)) &&
+      const uint32_t scol = s_cols(i);
+      ok = mbar_wait_inl(bar(s_bar_id(i)), s_parity(i), wc, site(1)) &&
            mbar_wait_inl(bar(kQFull + st), (uint32_t)((i / QS) & 1), wc, site(3));
       ok = __all_sync(kFull, ok);
       // The pre-pass stored −LSE·log2(e) and −D, so each pair of columns is
@@ -310,8 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         for (int ch = 0; ch < 2; ++ch) {
           const int c0 = h * 64 + ch * 32;
           uint32_t s[32];
-          if (dcheck(tmem_ok(C::kColS + c0, 32, 512), wc, kChkTmem, 18))
-            tmem_ld_x32(tmem + lane_off + C::kColS + (uint32_t)c0, s);
+          if (dcheck(tmem_ok(scol + c0, 32, 512), wc, kChkTmem, 18))
+            tmem_ld_x32(tmem + lane_off + scol + (uint32_t)c0, s);
           if (masked)
             p_chunk<true, kPolyEvery>(s, sl2x2, nlse + (c0 >> 1), r - c0 - delta, p + ch * 16);
           else if (ragged_cta)
@@ -337,8 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
           f2_unpack(p[half * 16 + e], a0, a1);
           pk[e] = pack2<F16>(a0, a1);
         }
-        if (dcheck(tmem_ok(C::kColS + h * 32 + 16 * half, 16, 512), wc, kChkTmem, 19))
-          tmem_st_x16(tmem + lane_off + C::kColS + (uint32_t)(h * 32 + 16 * half), pk);
+        if (dcheck(tmem_ok(scol + h * 32 + 16 * half, 16, 512), wc, kChkTmem, 19))
+          tmem_st_x16(tmem + lane_off + scol + (uint32_t)(h * 32 + 16 * half), pk);
       }
       // dK of the previous step reads dSᵀ from shared memory: it must be done
       // before this step's dSᵀ is written there.
@@ -477,8 +501,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         // dQ: lane = query row r, columns = the 64 head dims; 16-byte vector
         // reductions along the row.
         uint32_t v[64];
-        const bool chk = dcheck(tmem_ok(C::kColDP, 64, 512), wc, kChkTmem, 24);
-        if (chk) tmem_ld_x64(tmem + lane_off + C::kColDP, v);
+        const uint32_t dq_col = s_cols(i) + 64u;   // the last 64 columns of step i's Sᵀ buffer
+        const bool chk = dcheck(tmem_ok(dq_col, 64, 512), wc, kChkTmem, 24);
+        if (chk) tmem_ld_x64(tmem + lane_off + dq_col, v);
         tc_fence_before();
         mbar_arrive(bar(kDqDrained));
         if (!chk) continue;
@@ -557,6 +582,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         tc_commit(bar(kSFull));
         issue_sd(0, C::kColDP, sbase + C::kV);
         tc_commit(bar(kDPFull));
+        if (kSDouble && n > 1) {
+          ok = mbar_wait_inl(bar(kQFull + 1), 0, wc, site(12));
+          if (ok) {
+            tc_fence_after();
+            issue_sd(1, C::kColS2, sbase + C::kK);
+            tc_commit(bar(kSFull2));
+          }
+        }
       }
       for (int i = 0; ok && i < n; ++i) {
         const int st = i % QS;
@@ -569,61 +602,92 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
         const uint32_t qb = sbase + C::kQ + st * C::kTile;
         const uint32_t ob = sbase + C::kDO + st * C::kTile;
         // Debug build: every column range and operand tile of this step's products.
-        const bool chk = dcheck(tmem_ok(C::kColDP, D == 128 ? kBM : D, 512) && tmem_ok(C::kColDV, DR, 512) &&
-                                    tmem_ok(C::kColDK, DR, 512) && tmem_ok(C::kColS, kBM / 2, 512),
+        const bool chk = dcheck(tmem_ok(kSDouble ? s_cols(i) + 64 : C::kColDP, D == 128 ? kBM : D, 512) &&
+                                    tmem_ok(C::kColDV, DR, 512) && tmem_ok(C::kColDK, DR, 512) &&
+                                    tmem_ok(s_cols(i), kBM / 2, 512),
                                 wc, kChkTmem, 26) &&
                          dcheck(smem_ok(C::kDS, 2 * kBox, C::kBar, 1024) && smem_ok(qb - sbase, C::kTile, C::kBar, 1024) &&
                                     smem_ok(ob - sbase, C::kTile, C::kBar, 1024),
                                 wc, kChkSmem, 26);
-        // dQ into the dPᵀ columns first, so its drain overlaps dV and dK.
-        // Both operands are read MN-major, dSᵀ [keys][queries] and K [keys][dims].
-#pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          if (!chk) break;
-          const uint64_t dsd = sdesc_sw128(ds + (uint32_t)(ks * 2048), kBox, 1024);
-          const uint64_t kd = sdesc_sw128(sbase + C::kK + (uint32_t)(ks * 2048), kBox, 1024);
-          if constexpr (D == 128)
-            mma_ss(tmem + C::kColDP, kd, dsd, kIdQ, ks > 0 ? 1u : 0u);
-          else
-            mma_ss(tmem + C::kColDP, dsd, kd, kIdQ, ks > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(kDqFull));
-        // dV += Pᵀ dO, Pᵀ from tensor memory
-#pragma unroll
-        for (int ks = 0; ks < kBM / 16; ++ks)
-          if (chk) mma_ts(tmem + C::kColDV, tmem + C::kColS + (uint32_t)(8 * ks),
-                 sdesc_sw128(ob + (uint32_t)(ks * 2048), kBox, 1024), kIdKV, (i > 0 || ks > 0) ? 1u : 0u);
-        // Sᵀ of the next tile overwrites Pᵀ: issued right after dV, which
-        // reads it (the products run in issue order), and before dK, so the
-        // compute warps can start on it sooner.
         const bool next = i + 1 < n;
-        if (next) {
-          if (!mbar_wait_inl(bar(kQFull + (i + 1) % QS), (uint32_t)(((i + 1) / QS) & 1), wc, site(12))) {
-            ok = false;
-            break;
+        if constexpr (kSDouble) {
+          // d = 64.  dQ = dS K into the last 64 columns of this step's Sᵀ
+          // buffer (read already; Pᵀ is in the first 64), dK += dSᵀ Q, then
+          // the next dPᵀ — its columns are free once dSᵀ is formed, and its
+          // barrier tells the compute warps that dQ and dK have read dSᵀ —
+          // then dV += Pᵀ dO, and Sᵀ two tiles ahead into this buffer once the
+          // reducers have read dQ out of it.
+          const uint32_t sb = s_cols(i);
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks) {
+            if (!chk) break;
+            mma_ss(tmem + sb + 64u, sdesc_sw128(ds + (uint32_t)(ks * 2048), kBox, 1024),
+                   sdesc_sw128(sbase + C::kK + (uint32_t)(ks * 2048), kBox, 1024), kIdQ, ks > 0 ? 1u : 0u);
           }
-          tc_fence_after();
-          issue_sd(i + 1, C::kColS, sbase + C::kK);
-          tc_commit(bar(kSFull));
-        }
-        if constexpr (kDkSplit) {
-          // dK += dSᵀ Q of this step is issued by warp 14, after these products.
-          mbar_arrive(bar(kSIssued));
-        } else {
+          tc_commit(bar(kDqFull));
 #pragma unroll
           for (int ks = 0; ks < kBM / 16; ++ks)
             if (chk) mma_ss(tmem + C::kColDK, sdesc_sw128(ds + (uint32_t)((ks >> 2) * kBox + (ks & 3) * 32), 16, 1024),
                    sdesc_sw128(qb + (uint32_t)(ks * 2048), kBox, 1024), kIdKV, (i > 0 || ks > 0) ? 1u : 0u);
-        }
-        tc_commit(bar(kQEmpty + st));
-        if (next) {
-          if (!mbar_wait_inl(bar(kDqDrained), (uint32_t)(i & 1), wc, site(13))) {
-            ok = false;
-            break;
+          if (next) {
+            issue_sd(i + 1, C::kColDP, sbase + C::kV);
+            tc_commit(bar(kDPFull));
           }
-          tc_fence_after();
-          issue_sd(i + 1, C::kColDP, sbase + C::kV);
-          tc_commit(bar(kDPFull));
+#pragma unroll
+          for (int ks = 0; ks < kBM / 16; ++ks)
+            if (chk) mma_ts(tmem + C::kColDV, tmem + sb + (uint32_t)(8 * ks),
+                   sdesc_sw128(ob + (uint32_t)(ks * 2048), kBox, 1024), kIdKV, (i > 0 || ks > 0) ? 1u : 0u);
+          tc_commit(bar(kQEmpty + st));
+          if (i + 2 < n) {
+            if (!mbar_wait_inl(bar(kQFull + (i + 2) % QS), (uint32_t)(((i + 2) / QS) & 1), wc, site(12)) ||
+                !mbar_wait_inl(bar(kDqDrained), (uint32_t)(i & 1), wc, site(13))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_sd(i + 2, sb, sbase + C::kK);
+            tc_commit(bar(s_bar_id(i)));
+          }
+        } else {
+          // dQ into the dPᵀ columns first, so its drain overlaps dV and dK.
+          // Both operands are read MN-major, dSᵀ [keys][queries] and K [keys][dims].
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks) {
+            if (!chk) break;
+            const uint64_t dsd = sdesc_sw128(ds + (uint32_t)(ks * 2048), kBox, 1024);
+            const uint64_t kd = sdesc_sw128(sbase + C::kK + (uint32_t)(ks * 2048), kBox, 1024);
+            mma_ss(tmem + C::kColDP, kd, dsd, kIdQ, ks > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(kDqFull));
+          // dV += Pᵀ dO, Pᵀ from tensor memory
+#pragma unroll
+          for (int ks = 0; ks < kBM / 16; ++ks)
+            if (chk) mma_ts(tmem + C::kColDV, tmem + s_cols(i) + (uint32_t)(8 * ks),
+                   sdesc_sw128(ob + (uint32_t)(ks * 2048), kBox, 1024), kIdKV, (i > 0 || ks > 0) ? 1u : 0u);
+          // Sᵀ of the next tile overwrites Pᵀ: issued right after dV, which
+          // reads it (the products run in issue order), and before dK, so the
+          // compute warps can start on it sooner.
+          if (next) {
+            if (!mbar_wait_inl(bar(kQFull + (i + 1) % QS), (uint32_t)(((i + 1) / QS) & 1), wc, site(12))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_sd(i + 1, C::kColS, sbase + C::kK);
+            tc_commit(bar(kSFull));
+          }
+          // dK += dSᵀ Q of this step is issued by warp 14, after these products.
+          mbar_arrive(bar(kSIssued));
+          tc_commit(bar(kQEmpty + st));
+          if (next) {
+            if (!mbar_wait_inl(bar(kDqDrained), (uint32_t)(i & 1), wc, site(13))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_sd(i + 1, C::kColDP, sbase + C::kV);
+            tc_commit(bar(kDPFull));
+          }
         }
       }
       if (ok) tc_commit(bar(kDKVFull));

@@ -74,6 +74,8 @@ BF16_SHAPES = [
     (2, 2, 1000, 128),  # ragged with several K/V stages
     (1, 2, 256, 96),    # d = 96: tiles padded to 128 columns
     (2, 1, 333, 96),
+    (2, 1, 256, 64),    # d = 64, two query tiles: both score buffers, nothing issued two tiles ahead
+    (1, 1, 896, 64),    # d = 64, seven query tiles: each score buffer reused, the Q/dO ring wraps twice
 ]
 
 

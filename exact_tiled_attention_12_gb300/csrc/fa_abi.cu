@@ -331,12 +331,21 @@ fa_status prep_impl(const void* o, const void* dO, const float* lse, int B, int 
                                             dtype == FA_DTYPE_FP16 ? 1 : 0, cs));
 }
 
+// The d = 256 backward tiles the keys by 64 and, under the causal mask, puts
+// those tiles in the grid's second dimension (at most 65,535): past that it
+// cannot launch, so such shapes are refused before any work is queued.
+fa_status check_bwd_grid(const Shape& s, int causal, fa_dtype dtype) {
+  if (is16(dtype) && s.d == 256 && causal && (s.Nk + 63) / 64 > 65535) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
 fa_status tiles_impl(const void* q, const void* k, const void* v, const void* dO, void* dq, void* dk, void* dv, int B,
                      int H, int Nq, int Nk, int d, float scale, int causal, fa_dtype dtype, void* workspace,
                      size_t workspace_bytes, fa_stream_t stream) {
   Shape s;
   fa_status st = check_shape(B, H, Nq, Nk, d, dtype, causal, &s);
   if (st != FA_OK) return st;
+  if ((st = check_bwd_grid(s, causal, dtype)) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (s.empty()) return FA_OK;
   if ((st = check_ptrs({q, k, v, dO, dk, dv}, dtype)) != FA_OK) return st;
@@ -402,6 +411,7 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, c
   Shape s;
   fa_status st = check_shape(B, H, Nq, Nk, d, dtype, causal, &s);
   if (st != FA_OK) return st;
+  if ((st = check_bwd_grid(s, causal, dtype)) != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (s.no_heads() || (Nq == 0 && Nk == 0)) return FA_OK;
   if (Nq == 0) {

@@ -38,6 +38,11 @@
  *               cached prefix), so query i sees keys j ≤ i + Nk − Nq, which
  *               needs Nq ≤ Nk (FA_ERR_UNSUPPORTED otherwise).
  *   scale       finite and > 0; callers usually pass 1/sqrt(d).
+ *   Limits      (FA_ERR_UNSUPPORTED past them; the grids' second dimension)
+ *               at most 65,535 heads (B·H) and 65,535 tiles of 128 keys per
+ *               head (8,388,480 keys); the d = 256 backward under the causal
+ *               mask at most 65,535 tiles of 64 keys (4,194,240 keys); fewer
+ *               than 2^31 query rows in all.
  *   Empty       B, H or N equal to 0 is a valid empty problem: FA_OK, nothing
  *               launched, pointers may be NULL.
  *   Ownership   the caller owns every buffer.  The library allocates no device

@@ -101,6 +101,15 @@ def test_backward_argument_checks(L):
     assert L.fa_bwd_tiles(*([FAKE] * 7), 1, 1, 128, 64, 0.125, 0, 0, None, 0, None) == 4
     assert L.fa_bwd_dq_finish(FAKE, 1, 1, 100, 64, 0.125, 0, None, 0, None) == 4
     assert L.fa_bwd_dq_finish(FAKE, 1, 1, 100, 80, 0.125, 0, None, 0, None) == 2
+    # d = 256 under the causal mask tiles the keys by 64 in the grid's second
+    # dimension: 65,535 tiles are accepted (the missing workspace is then the
+    # first error), one key more is refused before anything is queued
+    edge = 65535 * 64
+    for n, code in ((edge, 4), (edge + 1, 2)):
+        assert L.fa_bwd(*([FAKE] * 9), 1, 1, n, 256, 0.0625, 1, 0, None, 0, None) == code
+        assert L.fa_bwd_tiles(*([FAKE] * 7), 1, 1, n, 256, 0.0625, 1, 0, None, 0, None) == code
+    # without the mask the key tiles run along the first dimension: accepted
+    assert L.fa_bwd(*([FAKE] * 9), 1, 1, edge + 1, 256, 0.0625, 0, 0, None, 0, None) == 4
 
 
 def _fwd_kv(L, Nq=128, Nk=256, causal=0, B=1, d=64, dtype=0):

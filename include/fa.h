@@ -42,7 +42,8 @@
  *               at most 65,535 heads (B·H) and 65,535 tiles of 128 keys per
  *               head (8,388,480 keys); the d = 256 backward under the causal
  *               mask at most 65,535 tiles of 64 keys (4,194,240 keys); fewer
- *               than 2^31 query rows in all.
+ *               than 2^31 query rows and 2^31 key rows in all (counted in
+ *               whole 128-row tiles per head for the 16-bit types).
  *   Empty       B, H or N equal to 0 is a valid empty problem: FA_OK, nothing
  *               launched, pointers may be NULL.
  *   Ownership   the caller owns every buffer.  The library allocates no device

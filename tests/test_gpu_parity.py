@@ -12,7 +12,7 @@ import torch
 
 from exact_tiled_attention_12_gb300.synthetic import WORKLOADS, make_inputs, make_workload_inputs
 
-from ._helpers import compare, run_library, run_oracle_heads, to64
+from ._helpers import BF16_GRAD_RTOL_FRO, BF16_LSE_ATOL, compare, rel_fro, run_library, run_oracle_heads, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -119,6 +119,41 @@ def test_bf16_stress_ragged(causal):
     0, far above rows whose scores are all very negative; they must neither
     enter the softmax nor turn dQ into inf · 0."""
     _check(2, 1, 300, 64, causal, "bf16", dist="stress", seed=6)
+
+
+@pytest.mark.parametrize("dtype,d,scale", [(dt, d, sc) for dt, d in (("bf16", 64), ("bf16", 128)) for sc in (1e-3, 0.3, 1.0)]
+                         + [("fp32", 64, 1e-3), ("fp32", 64, 0.3)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_scales(dtype, d, scale, causal):
+    """Scales other than 1/sqrt(d) (the softmax of the scaled scores, "Flash
+    Attention" tutorial 1.FlashAttention 整体结构 一): nearly uniform rows
+    (10⁻³) up to sharp ones (1.0: scores with a standard deviation of 8-11,
+    so a row's weight sits on a few keys).
+
+    The O bound for bf16 is derived, not the workloads' 1e-2: P is rounded to
+    bf16 (8 significant bits, relative error ≤ 2⁻⁸) before P V while ℓ sums
+    the unrounded values, so the weights on V are off by at most 2⁻⁸ in all,
+    and O itself is stored in bf16; hence |O − O_ref| ≤ 2⁻⁸·(max|V| + |O_ref|)
+    (+10⁻³ for the fp32 sums).  A sharp row puts O near a single V_j, where
+    these roundings no longer average out: at scale 1.0 they reach ~0.017
+    for |V_j| ≈ 4.  LSE, the gradients (relative Frobenius) and fp32 keep the
+    workloads' tolerances; fp32 stays at scores of the default's size, its
+    1e-5 bar being absolute."""
+    q, k, v, do = make_inputs(1, 2, 384, d, dtype, "normal", 40 + d + int(causal), device="cuda")
+    gpu = run_library(q, k, v, do, causal, scale)
+    ref = run_oracle_heads(q, k, v, do, causal, scale, _all_heads(1, 2))
+    flat = {key: val.reshape((-1,) + val.shape[2:]) for key, val in gpu.items()}
+    if dtype == "fp32":
+        compare(flat, ref, dtype)
+        return
+    for key in ("O", "LSE", "dQ", "dK", "dV"):
+        assert np.all(np.isfinite(flat[key])), key
+    vmax = np.abs(to64(v).reshape(2, -1)).max(axis=1).reshape(2, 1, 1)
+    bound = 2.0 ** -8 * (vmax + np.abs(ref["O"])) + 1e-3
+    assert np.all(np.abs(flat["O"] - ref["O"]) <= bound), float(np.max(np.abs(flat["O"] - ref["O"]) - bound))
+    assert np.max(np.abs(flat["LSE"] - ref["LSE"])) <= BF16_LSE_ATOL
+    for key in ("dQ", "dK", "dV"):
+        assert rel_fro(flat[key], ref[key]) <= BF16_GRAD_RTOL_FRO, (key, rel_fro(flat[key], ref[key]))
 
 
 # ------------------------------------------------------------------ closed forms on the GPU

@@ -311,6 +311,13 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
     a.opart = static_cast<float*>(workspace);
     a.lpart = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.opart_bytes);
   }
+  // Short K/V ranges without the mask and with more units than SMs: one
+  // persistent CTA per SM, so units' start-up and drain overlap.
+  a.persist_ctas = 0;
+  const int sms = sm_count_current_device();
+  if (d != 256 && !causal && a.splits <= 1 && s.nk_pad() / 128 <= fa::kFwdPersistMaxTiles && sms > 0 &&
+      fa::fwd_units(B, H, Nq, d) > sms)
+    a.persist_ctas = sms;
   return from_cuda(fa::launch_fwd_bf16(a, cs));
 }
 

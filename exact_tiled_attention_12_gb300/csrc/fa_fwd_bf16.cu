@@ -515,6 +515,366 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_kernel(const __grid_c
   }
 }
 
+// Persistent form of the forward for problems without the mask whose units
+// see few K/V tiles (every unit sees all of them; no split): one CTA per SM
+// walks the units u = blockIdx.x, blockIdx.x + gridDim.x, ...  The K/V ring,
+// the score and P barriers count on across units; the next unit's Q load
+// starts as soon as the current unit's last scores are computed (QEmpty),
+// its first scores while the softmax warps still write the current unit's
+// O, and its first P V product once they have read O out of tensor memory
+// (OEmpty).  So a unit's start-up and drain overlap its neighbours' work
+// instead of leaving the SM idle between one-unit CTAs.
+template <int DR, bool RAGGED, bool F16>
+__global__ void __launch_bounds__(kThreads, 1) fa_fwd_bf16_persist_kernel(const __grid_constant__ FwdArgs a) {
+  constexpr int D = DR <= 64 ? 64 : 128;
+  using L = FwdLayout<D>;
+  constexpr int KS = L::kKS, VS = L::kVS;
+  using Bar = FwdBars<KS, VS>;
+  constexpr int kQFull = Bar::kQFull, kKFull = Bar::kKFull, kKEmpty = Bar::kKEmpty, kVFull = Bar::kVFull,
+                kVEmpty = Bar::kVEmpty, kSFull = Bar::kSFull, kPFull = Bar::kPFull, kOFull = Bar::kOFull,
+                kMmaDone = Bar::kMmaDone;
+  constexpr int kQEmpty = Bar::kNumBars;        // the unit's scores are done: Q may be reloaded
+  constexpr int kOEmpty = Bar::kNumBars + 1;    // +tile: O_t has been read out
+  constexpr int kNumBars = Bar::kNumBars + 3;
+  static_assert(8 * kNumBars + 8 <= 512, "barrier block too small");
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t sbase = smem_u32(smem_raw);
+  uint8_t* sgen = smem_raw;
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) atomicCAS(a.fault, 0u, site(0));
+    return;
+  }
+  const uint32_t bars = sbase + L::kBar;
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sgen + L::kBar + 8 * kNumBars);
+  int* abort_flag = reinterpret_cast<int*>(sgen + L::kBar + 8 * kNumBars + 4);
+  const WaitCtx wc{abort_flag, a.fault};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int Nq = a.Nq, Nk = a.Nk;
+  const int pairs = (Nq + 2 * kBM - 1) / (2 * kBM);      // two-tile units per head
+  const int units = a.B * a.H * pairs;
+  const int n_kv = (Nk + kBN - 1) / kBN;                 // every unit visits every K/V tile
+  const int kv_tail = Nk - (n_kv - 1) * kBN;
+  const bool ragged_last = RAGGED && kv_tail < kBN;      // the last tile holds keys past Nk
+  // Query tiles of a unit that exist: tile 1 of a head's last pair may not.
+  auto tiles_of = [&](int u, int t) -> int { return (u % pairs) * 2 * kBM + t * kBM < Nq ? n_kv : 0; };
+  auto load_rows = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar_addr, int x, int pos, int n, int bh) {
+    bool chk = dcheck(smem_ok(dst - sbase, kBoxBytes, (uint32_t)L::kBar, 1024), wc, kChkSmem, 11) &&
+               dcheck(tma_x_ok(x, 64, D), wc, kChkTmaX, 11);
+    if constexpr (RAGGED)
+      chk = chk && dcheck(tma_head_ok(pos, n, bh, a.B * a.H), wc, kChkTmaRows, 11);
+    else
+      chk = chk && dcheck(tma_rows_ok((long long)bh * n + pos, kBM, (long long)a.B * a.H * n), wc, kChkTmaRows, 11);
+    if (!chk) {
+      mbar_complete_tx(bar_addr, kBoxBytes);
+      return;
+    }
+    if constexpr (RAGGED)
+      tma_load_3d(dst, map, bar_addr, x, pos, bh);
+    else
+      tma_load_2d(dst, map, bar_addr, x, bh * n + pos);
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kQFull), 1);
+    mbar_init(bar(kQEmpty), 1);
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(bar(kKFull + s), 1);
+      mbar_init(bar(kKEmpty + s), 1);
+    }
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(bar(kVFull + s), 1);
+      mbar_init(bar(kVEmpty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(kSFull + t), 1);
+      mbar_init(bar(kPFull + t), 128);
+      mbar_init(bar(kOFull + t), 1);
+      mbar_init(bar(kOEmpty + t), 128);
+    }
+    mbar_init(bar(kMmaDone), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  auto s_col = [](int t) -> uint32_t { return (uint32_t)(128 * t); };
+  auto o_col = [](int t) -> uint32_t { return (uint32_t)(256 + D * t); };
+
+  if (warp < 8) {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const float sl2 = a.scale_log2;
+    int n_s = 0;      // scores of tile t consumed so far (SFull phases)
+    int n_o = 0;      // units of tile t finished so far (OFull / OEmpty phases)
+    bool ok = true;
+    for (int u = (int)blockIdx.x; ok && u < units; u += (int)gridDim.x) {
+      const int nt = tiles_of(u, t);
+      if (nt == 0) continue;
+      const int bh = u / pairs;
+      const int qt = (u % pairs) * 2 * kBM + t * kBM;
+      float m_ref = -INFINITY;
+      float ell = 0.f;
+      for (int j = 0; j < nt; ++j, ++n_s) {
+        ok = mbar_wait(bar(kSFull + t), (uint32_t)(n_s & 1), wc, site(12));
+        ok = __all_sync(kFull, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t s[128];
+        if (dcheck(tmem_ok(s_col(t), 128, 512), wc, kChkTmem, 12)) tmem_ld_x128(tmem + lane_off + s_col(t), s);
+        if (ragged_last && j == nt - 1) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= kv_tail) s[c] = f2u(-INFINITY);
+        }
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; c += 8) {
+          mx0 = max3(mx0, u2f(s[c]), u2f(s[c + 1]));
+          mx1 = max3(mx1, u2f(s[c + 2]), u2f(s[c + 3]));
+          mx2 = max3(mx2, u2f(s[c + 4]), u2f(s[c + 5]));
+          mx3 = max3(mx3, u2f(s[c + 6]), u2f(s[c + 7]));
+        }
+        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        const bool move = mx > m_ref + 8.0f;
+        const float m_new = move ? mx : m_ref;
+        const float alpha = ex2(m_ref - m_new);
+        if (j > 0 && __any_sync(kFull, move)) {
+          // The previous P V into O_t has completed (it was issued before
+          // these scores) and the next one waits for P_full: O_t is ours.
+#pragma unroll
+          for (int cc = 0; cc < DR / 32; ++cc) {
+            if (!dcheck(tmem_ok(o_col(t) + 32 * cc, 32, 512), wc, kChkTmem, 13)) continue;
+            uint32_t o[32];
+            tmem_ld_x32(tmem + lane_off + o_col(t) + 32 * cc, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+            tmem_st_x32(tmem + lane_off + o_col(t) + 32 * cc, o);
+          }
+        }
+        ell *= alpha;
+        m_ref = m_new;
+        const uint32_t p_addr = tmem + lane_off + s_col(t);
+        if (!dcheck(tmem_ok(s_col(t), kBN / 2, 512), wc, kChkTmem, 14)) {
+        } else if (ragged_last && j == nt - 1)
+          ell += exp_tile_to_p<0, F16>(s, sl2, m_ref, p_addr);
+        else
+          ell += exp_tile_to_p<kPolyEvery, F16>(s, sl2, m_ref, p_addr);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kPFull + t));
+      }
+      if (!ok) break;
+      // Epilogue of this unit's tile: O = Õ / ℓ and LSE; O_t is released to
+      // the next unit's first P V as soon as it has been read.
+      ok = mbar_wait(bar(kOFull + t), (uint32_t)(n_o & 1), wc, site(13));
+      ok = __all_sync(kFull, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int q = qt + r;
+      const float inv = 1.0f / ell;
+      const float lse = (m_ref + log2f(ell)) * 0.69314718055994530942f;
+      const bool live = !RAGGED || q < Nq;
+      uint16_t* orow = static_cast<uint16_t*>(a.o) + ((size_t)bh * (size_t)Nq + (size_t)q) * DR;
+#pragma unroll
+      for (int cc = 0; cc < DR / 32; ++cc) {
+        if (!dcheck(tmem_ok(o_col(t) + 32 * cc, 32, 512), wc, kChkTmem, 15)) continue;
+        uint32_t o[32];
+        tmem_ld_x32(tmem + lane_off + o_col(t) + 32 * cc, o);   // warp-collective: every lane loads
+        if (cc == DR / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(bar(kOEmpty + t));
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack2<F16>(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
+        if (live) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            st_global_v4(orow + 32 * cc + 8 * v4, pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+      if (live) a.lse[(size_t)bh * (size_t)Nq + (size_t)q] = lse;
+      ++n_o;
+    }
+  } else if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&a.tm_q);
+      prefetch_tmap(&a.tm_k);
+      prefetch_tmap(&a.tm_v);
+      const uint32_t tile = (uint32_t)L::kTile;
+      int g = 0;                      // K/V tiles issued so far, over all units
+      int n_q = 0;                    // Q loads issued
+      int issued_k[KS] = {}, issued_v[VS] = {};
+      bool ok = true;
+      for (int u = (int)blockIdx.x; ok && u < units; u += (int)gridDim.x) {
+        const int bh = u / pairs;
+        const int q0 = (u % pairs) * 2 * kBM;
+        const int nt1 = tiles_of(u, 1);
+        for (int j = 0; j < n_kv; ++j, ++g) {
+          // Tile g goes to K stage g % KS (its use g / KS) and V stage g % VS.
+          const int sk = g % KS, sv = g % VS;
+          if (g >= KS && !mbar_wait(bar(kKEmpty + sk), (uint32_t)((g / KS - 1) & 1), wc, site(14))) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kKFull + sk), tile);
+          for (int b = 0; b < D / 64; ++b)
+            load_rows(sbase + L::kK + sk * L::kTile + b * kBoxBytes, &a.tm_k, bar(kKFull + sk), 64 * b, j * kBN, Nk,
+                      bh);
+          ++issued_k[sk];
+          if (j == 0) {
+            // Q of this unit once the previous unit's scores have all been computed.
+            if (n_q > 0 && !mbar_wait(bar(kQEmpty), (uint32_t)((n_q - 1) & 1), wc, site(15))) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(kQFull), (nt1 > 0 ? 2u : 1u) * tile);
+            for (int t = 0; t < (nt1 > 0 ? 2 : 1); ++t)
+              for (int b = 0; b < D / 64; ++b)
+                load_rows(sbase + L::kQ + t * L::kTile + b * kBoxBytes, &a.tm_q, bar(kQFull), 64 * b, q0 + t * kBM,
+                          Nq, bh);
+            ++n_q;
+          }
+          if (g >= VS && !mbar_wait(bar(kVEmpty + sv), (uint32_t)((g / VS - 1) & 1), wc, site(16))) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kVFull + sv), tile);
+          for (int b = 0; b < D / 64; ++b)
+            load_rows(sbase + L::kV + sv * L::kTile + b * kBoxBytes, &a.tm_v, bar(kVFull + sv), 64 * b, j * kBN, Nk,
+                      bh);
+          ++issued_v[sv];
+        }
+      }
+      // Never leave the CTA with copies in flight: wait for the last load of
+      // every barrier (already complete in the normal case).
+      if (n_q > 0) mbar_wait_drain(bar(kQFull), (uint32_t)((n_q - 1) & 1), wc, site(17));
+      for (int s = 0; s < KS; ++s)
+        if (issued_k[s] > 0) mbar_wait_drain(bar(kKFull + s), (uint32_t)((issued_k[s] - 1) & 1), wc, site(17));
+      for (int s = 0; s < VS; ++s)
+        if (issued_v[s] > 0) mbar_wait_drain(bar(kVFull + s), (uint32_t)((issued_v[s] - 1) & 1), wc, site(17));
+    }
+  } else {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_f16kind(128, kBN, false, false, F16);
+      constexpr uint32_t kIdO = idesc_f16kind(128, DR, false, true, F16);
+      int g = 0;                  // K/V tiles consumed so far, over all units
+      int n_q = 0;                // units started (QFull / QEmpty phases)
+      int n_p[2] = {0, 0};        // P of tile t consumed (PFull phases)
+      int n_o[2] = {0, 0};        // units of tile t finished (OFull / OEmpty phases)
+      int k_ready = -1;           // last K tile (global index) seen complete
+      bool ok = true;
+      auto issue_s = [&](int t, int gk) -> bool {
+        if (k_ready < gk) {
+          if (!mbar_wait(bar(kKFull + gk % KS), (uint32_t)((gk / KS) & 1), wc, site(18))) return false;
+          k_ready = gk;
+        }
+        tc_fence_after();
+        const uint64_t qd = sdesc_sw128(sbase + L::kQ + t * L::kTile, 16, 1024);
+        const uint64_t kd = sdesc_sw128(sbase + L::kK + (gk % KS) * L::kTile, 16, 1024);
+        const bool chk = dcheck(tmem_ok(s_col(t), kBN, 512), wc, kChkTmem, 16) &&
+                         dcheck(smem_ok(L::kQ + t * L::kTile, L::kTile, L::kBar, 1024), wc, kChkSmem, 16) &&
+                         dcheck(smem_ok(L::kK + (gk % KS) * L::kTile, L::kTile, L::kBar, 1024), wc, kChkSmem, 16);
+#pragma unroll
+        for (int ks = 0; ks < DR / 16; ++ks) {
+          if (!chk) break;
+          const uint32_t off = (uint32_t)((ks >> 2) * kBoxBytes + (ks & 3) * 32);
+          mma_ss(tmem + s_col(t), sdesc_add(qd, off), sdesc_add(kd, off), kIdS, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(kSFull + t));
+        return true;
+      };
+      for (int u = (int)blockIdx.x; ok && u < units; u += (int)gridDim.x, g += n_kv, ++n_q) {
+        const int nt[2] = {tiles_of(u, 0), tiles_of(u, 1)};
+        const int t_last = nt[1] > 0 ? 1 : 0;        // the tile whose last scores finish the unit's use of Q
+        if (!mbar_wait(bar(kQFull), (uint32_t)(n_q & 1), wc, site(19))) {
+          ok = false;
+          break;
+        }
+        for (int t = 0; t < 2 && ok; ++t)
+          if (nt[t] > 0) ok = issue_s(t, g);
+        if (!ok) break;
+        if (n_kv == 1) tc_commit(bar(kQEmpty));
+        tc_commit(bar(kKEmpty + g % KS));
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int gj = g + j;
+          if (!mbar_wait(bar(kVFull + gj % VS), (uint32_t)((gj / VS) & 1), wc, site(20))) {
+            ok = false;
+            break;
+          }
+          const uint64_t vd = sdesc_sw128(sbase + L::kV + (gj % VS) * L::kTile, kBoxBytes, 1024);
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (nt[t] == 0) continue;
+            if (!mbar_wait(bar(kPFull + t), (uint32_t)(n_p[t] & 1), wc, site(21))) {
+              ok = false;
+              break;
+            }
+            ++n_p[t];
+            // The first product into O_t overwrites it: the previous unit's
+            // epilogue must have read it out.
+            if (j == 0 && n_o[t] > 0 && !mbar_wait(bar(kOEmpty + t), (uint32_t)((n_o[t] - 1) & 1), wc, site(22))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const bool chk = dcheck(tmem_ok(o_col(t), DR, 512), wc, kChkTmem, 17) &&
+                             dcheck(tmem_ok(s_col(t), kBN / 2, 512), wc, kChkTmem, 17) &&
+                             dcheck(smem_ok(L::kV + (gj % VS) * L::kTile, L::kTile, L::kBar, 1024), wc, kChkSmem, 17);
+#pragma unroll
+            for (int ks = 0; ks < kBN / 16; ++ks)
+              if (chk)
+                mma_ts(tmem + o_col(t), tmem + s_col(t) + (uint32_t)(8 * ks), sdesc_add(vd, (uint32_t)(ks * 2048)),
+                       kIdO, (j > 0 || ks > 0) ? 1u : 0u);
+            if (j == n_kv - 1) tc_commit(bar(kOFull + t));
+            if (j + 1 < n_kv) {
+              ok = issue_s(t, gj + 1);
+              if (ok && t == t_last && j + 2 == n_kv) tc_commit(bar(kQEmpty));
+            }
+          }
+          if (!ok) break;
+          tc_commit(bar(kVEmpty + gj % VS));
+          if (j + 1 < n_kv) tc_commit(bar(kKEmpty + (gj + 1) % KS));
+        }
+        for (int t = 0; t < 2; ++t)
+          if (nt[t] > 0) ++n_o[t];
+      }
+      // Every product must be finished before tensor memory is released.
+      tc_commit(bar(kMmaDone));
+      mbar_wait_drain(bar(kMmaDone), 0, wc, site(23));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int DR, bool RAGGED, bool F16>
+cudaError_t launch_persist(const FwdArgs& a, cudaStream_t s) {
+  auto kern = fa_fwd_bf16_persist_kernel<DR, RAGGED, F16>;
+  const size_t smem = FwdLayout<(DR <= 64 ? 64 : 128)>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)a.persist_ctas, kThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <int DR, bool CAUSAL, bool RAGGED, bool F16>
 cudaError_t launch_impl(const FwdArgs& a, cudaStream_t s) {
   auto kern = fa_fwd_bf16_kernel<DR, CAUSAL, RAGGED, F16>;
@@ -657,6 +1017,14 @@ size_t fwd_bf16_smem_bytes(int d) {
 
 template <bool F16>
 static cudaError_t dispatch_fwd(const FwdArgs& a, bool ragged, cudaStream_t s) {
+  if (a.persist_ctas > 0 && !a.causal && a.splits <= 1) {
+    switch (a.d) {
+      case 128: return ragged ? launch_persist<128, true, F16>(a, s) : launch_persist<128, false, F16>(a, s);
+      case 96: return ragged ? launch_persist<96, true, F16>(a, s) : launch_persist<96, false, F16>(a, s);
+      case 64: return ragged ? launch_persist<64, true, F16>(a, s) : launch_persist<64, false, F16>(a, s);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (a.d == 128) {
     if (ragged) return a.causal ? launch_impl<128, true, true, F16>(a, s) : launch_impl<128, false, true, F16>(a, s);
     return a.causal ? launch_impl<128, true, false, F16>(a, s) : launch_impl<128, false, false, F16>(a, s);

@@ -63,7 +63,13 @@ struct FwdArgs {
   int n_full, splits, part_rows;
   float* opart;
   float* lpart;
+  // > 0: the persistent forward (d ≤ 128, no mask, no split) on this many
+  // CTAs, each walking the units with a stride of persist_ctas.
+  int persist_ctas;
 };
+// Largest K/V tile count per unit for which the forward runs persistent when
+// there are more units than SMs (its start-up and drain then weigh most).
+constexpr int kFwdPersistMaxTiles = 16;
 // Work units of the forward: 256 query rows (two tiles) per CTA, 128 at d = 256.
 int fwd_unit_rows(int d);
 int fwd_units(int B, int H, int Nq, int d);

@@ -107,6 +107,20 @@ def test_bf16_split_forward(B, H, N, d):
             assert np.max(np.abs(to64(l_split[b, h]) - ref_l)) <= 1e-3
 
 
+@pytest.mark.parametrize("B,H,N,d", [(8, 32, 1000, 64), (4, 40, 2048, 128), (2, 96, 777, 96), (1, 200, 256, 128)])
+def test_bf16_persistent_forward(B, H, N, d):
+    """More two-tile units than SMs and at most 16 K/V tiles each, without
+    the mask: the forward runs as one persistent CTA per SM walking the
+    units (ragged N, d = 64, 96, 128; units of 2 to 16 K/V tiles).  Forward
+    and backward of the first and last heads against the oracle."""
+    q, k, v, do = make_inputs(B, H, N, d, "bf16", "normal", 50 + N + d, device="cuda")
+    scale = d ** -0.5
+    gpu = run_library(q, k, v, do, False, scale)
+    heads = [(0, 0), (B - 1, H - 1)]
+    ref = run_oracle_heads(q, k, v, do, False, scale, heads)
+    compare({key: np.stack([val[b, h] for b, h in heads]) for key, val in gpu.items()}, ref, "bf16")
+
+
 def test_bf16_stress_small():
     """Scores scaled to magnitudes in the hundreds (Q, K drawn ×8, d = 64)."""
     errs = _check(2, 2, 512, 64, False, "bf16", dist="stress", seed=5)

@@ -394,6 +394,13 @@ fa_status tiles_impl(const void* q, const void* k, const void* v, const void* dO
   a.scale = scale;
   a.causal = causal;
   a.fault = fault;
+  // d = 64 without the mask, few query tiles per head and more K/V tiles than
+  // SMs: one persistent CTA per SM, so K/V tiles' start-up and drain overlap.
+  a.persist_ctas = 0;
+  const int sms = sm_count_current_device();
+  if (d == 64 && !causal && sms > 0 && s.nq_pad() / 128 <= fa::kBwdPersistMaxTiles &&
+      heads * (s.nk_pad() / 128) > sms)
+    a.persist_ctas = sms;
   return from_cuda(fa::launch_bwd_bf16(a, cs));
 }
 

@@ -739,6 +739,500 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_kernel(const __grid_c
   // No code after the roles: their register counts differ (setmaxnreg).
 }
 
+// Persistent form of the backward at d = 64 for problems without the mask
+// whose CTAs would visit few query tiles: one CTA per SM walks the units
+// (K/V tiles, head-major) u = blockIdx.x, blockIdx.x + gridDim.x, ...  The
+// steps of all its units form one sequence: the Q/dO ring, the score
+// buffers and every step barrier count on across units; K and V alternate
+// between two buffers, so the next unit's K/V tile loads while the current
+// one runs; the next unit's first scores and dPᵀ are issued during the
+// current unit's last steps, and its first dK and dV products (which start
+// the accumulators afresh) wait only until the compute warps have read the
+// current unit's dK and dV out of tensor memory.  Per step it is the d = 64
+// kernel above: two score buffers, dQ in the spent half of a buffer.
+struct BwdCfgP64 {
+  static constexpr int kQS = 3;
+  static constexpr int kTile = 128 * 64 * 2;       // one 128 × 64 bf16 tile = one box
+  static constexpr int kK = 0;                     // 2 unit buffers
+  static constexpr int kV = kK + 2 * kTile;        // 2 unit buffers
+  static constexpr int kQ = kV + 2 * kTile;        // kQS stages
+  static constexpr int kDO = kQ + kQS * kTile;     // kQS stages
+  static constexpr int kDS = kDO + kQS * kTile;    // dSᵀ [128 keys][128 queries]: 2 boxes
+  static constexpr int kLSE = kDS + 2 * kBox;      // kQS stages of 128 floats
+  static constexpr int kDV = kLSE + kQS * kBM * 4; // kQS stages of 128 floats
+  static constexpr int kBar = kDV + kQS * kBM * 4;
+  static constexpr int kBytes = kBar + 256;
+  static constexpr uint32_t kColDV = 0, kColDK = 64, kColS = 128, kColDP = 256, kColS2 = 384;
+  // barriers
+  static constexpr int kKVFull = 0;                // +buffer
+  static constexpr int kKVEmpty = 2;               // +buffer
+  static constexpr int kQFull = 4;                 // +stage
+  static constexpr int kQEmpty = kQFull + kQS;     // +stage
+  static constexpr int kSFull = kQEmpty + kQS;
+  static constexpr int kSFull2 = kSFull + 1;
+  static constexpr int kDPFull = kSFull + 2;
+  static constexpr int kPdsFull = kSFull + 3;
+  static constexpr int kDqFull = kSFull + 4;
+  static constexpr int kDqDrained = kSFull + 5;
+  static constexpr int kDKVFull = kSFull + 6;      // a unit's dK and dV are complete
+  static constexpr int kDKVEmpty = kSFull + 7;     // ... and have been read out
+  static constexpr int kMmaDone = kSFull + 8;
+  static constexpr int kNumBars = kSFull + 9;
+};
+static_assert(BwdCfgP64::kBytes <= 232448, "shared memory exceeds the 227 KB a CTA may use");
+static_assert(8 * BwdCfgP64::kNumBars + 8 <= 256, "barrier block too small");
+
+template <bool RAGGED, bool F16>
+__global__ void __launch_bounds__(kThreads, 1) fa_bwd_bf16_persist64_kernel(const __grid_constant__ BwdArgs a) {
+  constexpr int D = 64, DR = 64;
+  using C = BwdCfgP64;
+  constexpr int QS = C::kQS;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t sbase = smem_u32(smem_raw);
+  uint8_t* sgen = smem_raw;
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) atomicCAS(a.fault, 0u, site(0));
+    return;
+  }
+  const uint32_t bars = sbase + C::kBar;
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sgen + C::kBar + 8 * C::kNumBars);
+  int* abort_flag = reinterpret_cast<int*>(sgen + C::kBar + 8 * C::kNumBars + 4);
+  const WaitCtx wc{abort_flag, a.fault};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int Nq = a.Nq, Nk = a.Nk;
+  const int n_kv = (Nk + kBN - 1) / kBN;                           // K/V tiles per head
+  const int n = RAGGED ? (Nq + kBM - 1) / kBM : Nq / kBM;          // query tiles per head = steps per unit
+  const int units = a.B * a.H * n_kv;
+  // This CTA's units and steps: unit k (k-th of the CTA) is u = blockIdx.x + k·gridDim.x;
+  // step g of the CTA is step g mod n of its unit g / n.
+  const int my_units = (int)blockIdx.x < units ? (units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int total = my_units * n;
+  auto unit_of = [&](int k) -> int { return (int)blockIdx.x + k * (int)gridDim.x; };
+  auto s_cols = [](int g) -> uint32_t { return (g & 1) ? C::kColS2 : C::kColS; };
+  auto s_bar_id = [](int g) -> int { return (g & 1) ? C::kSFull2 : C::kSFull; };
+  auto s_parity = [](int g) -> uint32_t { return (uint32_t)((g >> 1) & 1); };
+  auto load_rows = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar_addr, int x, int pos, int nrows, int bh) {
+    bool chk = dcheck(smem_ok(dst - sbase, kBox, (uint32_t)C::kBar, 1024), wc, kChkSmem, 40) &&
+               dcheck(tma_x_ok(x, 64, D), wc, kChkTmaX, 40);
+    if constexpr (RAGGED)
+      chk = chk && dcheck(tma_head_ok(pos, nrows, bh, a.B * a.H), wc, kChkTmaRows, 40);
+    else
+      chk = chk && dcheck(tma_rows_ok((long long)bh * nrows + pos, 128, (long long)a.B * a.H * nrows), wc,
+                          kChkTmaRows, 40);
+    if (!chk) {
+      mbar_complete_tx(bar_addr, kBox);
+      return;
+    }
+    if constexpr (RAGGED)
+      tma_load_3d(dst, map, bar_addr, x, pos, bh);
+    else
+      tma_load_2d(dst, map, bar_addr, x, bh * nrows + pos);
+  };
+  auto load_bulk = [&](uint32_t dst, const float* src, uint32_t bytes, uint32_t bar_addr) {
+    if (!dcheck(smem_ok(dst - sbase, bytes, (uint32_t)C::kBar, 16) &&
+                    bulk_ok(reinterpret_cast<uint64_t>(src), dst, bytes), wc, kChkBulk, 41)) {
+      mbar_complete_tx(bar_addr, bytes);
+      return;
+    }
+    bulk_load(dst, src, bytes, bar_addr);
+  };
+  // Workspace row of query 0 of head bh (whole tiles per head when ragged).
+  auto wrow_of = [&](int bh) -> int { return RAGGED ? bh * n * kBM : bh * Nq; };
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(C::kKVFull + b), 1);
+      mbar_init(bar(C::kKVEmpty + b), 1);
+    }
+    for (int s = 0; s < QS; ++s) {
+      mbar_init(bar(C::kQFull + s), 1);
+      mbar_init(bar(C::kQEmpty + s), 1 + 32 * kComputeWarps);   // the MMA thread and the compute warps
+    }
+    mbar_init(bar(C::kSFull), 1);
+    mbar_init(bar(C::kSFull2), 1);
+    mbar_init(bar(C::kDPFull), 1);
+    mbar_init(bar(C::kPdsFull), 32 * kComputeWarps);
+    mbar_init(bar(C::kDqFull), 1);
+    mbar_init(bar(C::kDqDrained), 32 * kRedWarps);
+    mbar_init(bar(C::kDKVFull), 1);
+    mbar_init(bar(C::kDKVEmpty), 32 * kComputeWarps);
+    mbar_init(bar(C::kMmaDone), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp < kComputeWarps) {
+    // ------------------------------------------------------------ Pᵀ, dSᵀ, and each unit's dK, dV
+    setmaxnreg_inc<kRegsCompute>();
+    const int gq = warp & 3;
+    const int h = warp >> 2;                       // query columns [64h, 64h + 64)
+    const int r = gq * 32 + lane;                  // key row within the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(gq * 32) << 16;
+    const float sl2 = a.scale_log2;
+    const uint32_t ds_tile = sbase + C::kDS;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
+    bool ok = true;
+    // Unit k of this CTA, step i within it, Q/dO stage st of step g and the
+    // parity of that stage's use, all kept incrementally (no divisions).
+    int k = 0, i = 0, st = 0, qph = 0;
+    int bh = 0, kv0 = 0, dead_lim = 0;
+    bool dead_key = false, ragged_cta = false;
+    for (int g = 0; g < total; ++g) {
+      if (i == 0) {
+        const int u = unit_of(k);
+        bh = u / n_kv;
+        kv0 = (u - bh * n_kv) * kBN;
+        dead_key = RAGGED && kv0 + r >= Nk;
+        ragged_cta = RAGGED && kv0 + kBN > Nk;
+        dead_lim = dead_key ? (1 << 30) : -(1 << 30);
+      }
+      const int kv = kv0 + r;
+      const uint32_t scol = s_cols(g);
+      ok = mbar_wait_inl(bar(s_bar_id(g)), s_parity(g), wc, site(40)) &&
+           mbar_wait_inl(bar(C::kQFull + st), (uint32_t)qph, wc, site(41));
+      ok = __all_sync(kFull, ok);
+      const uint64_t* nlse = reinterpret_cast<const uint64_t*>(sgen + C::kLSE + st * kBM * 4);
+      const uint64_t* ndv = reinterpret_cast<const uint64_t*>(sgen + C::kDV + st * kBM * 4);
+      uint64_t p[32];
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          const int c0 = h * 64 + ch * 32;
+          uint32_t s[32];
+          if (dcheck(tmem_ok(scol + c0, 32, 512), wc, kChkTmem, 40))
+            tmem_ld_x32(tmem + lane_off + scol + (uint32_t)c0, s);
+          if (ragged_cta)
+            p_chunk<true, 0>(s, sl2x2, nlse + (c0 >> 1), dead_lim, p + ch * 16);
+          else
+            p_chunk<false, kPolyEvery>(s, sl2x2, nlse + (c0 >> 1), r - c0, p + ch * 16);
+        }
+      }
+      if (ok) ok = mbar_wait_inl(bar(C::kDPFull), (uint32_t)(g & 1), wc, site(42));
+      ok = pair_sync_and(1 + gq, ok);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float a0, a1;
+          f2_unpack(p[half * 16 + e], a0, a1);
+          pk[e] = pack2<F16>(a0, a1);
+        }
+        if (dcheck(tmem_ok(scol + h * 32 + 16 * half, 16, 512), wc, kChkTmem, 41))
+          tmem_st_x16(tmem + lane_off + scol + (uint32_t)(h * 32 + 16 * half), pk);
+      }
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c0 = h * 64 + ch * 32;
+        uint32_t dp[32];
+        if (dcheck(tmem_ok(C::kColDP + c0, 32, 512), wc, kChkTmem, 42))
+          tmem_ld_x32(tmem + lane_off + C::kColDP + (uint32_t)c0, dp);
+        uint32_t dk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint64_t ds = f2_mul(p[ch * 16 + e], f2_add(f2_pack(u2f(dp[2 * e]), u2f(dp[2 * e + 1])), ndv[(c0 >> 1) + e]));
+          float d0, d1;
+          f2_unpack(ds, d0, d1);
+          dk[e] = pack2<F16>(d0, d1);
+        }
+        const uint32_t row_addr = ds_tile + (uint32_t)(h * kBox + r * 128);
+        if (!dcheck(smem_ok(row_addr - sbase, 128, (uint32_t)C::kBar, 128), wc, kChkSmem, 43)) continue;
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) {
+          const int chunk = ch * 4 + w4;
+          st_shared_v4(row_addr + (uint32_t)(((chunk ^ (r & 7)) & 7) * 16), dk[4 * w4], dk[4 * w4 + 1],
+                       dk[4 * w4 + 2], dk[4 * w4 + 3]);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      fence_proxy_async_smem();
+      mbar_arrive(bar(C::kPdsFull));
+      mbar_arrive(bar(C::kQEmpty + st));
+      if (i == n - 1) {
+        // The unit's dK and dV: read them out (then the next unit's first
+        // dK and dV products may start the accumulators afresh) and store.
+        ok = mbar_wait_inl(bar(C::kDKVFull), (uint32_t)(k & 1), wc, site(43));
+        ok = __all_sync(kFull, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t col = h == 0 ? C::kColDV : C::kColDK;
+        const float mul = h == 0 ? 1.0f : a.scale;
+        uint32_t v0[32], v1[32];
+        if (dcheck(tmem_ok(col, 64, 512), wc, kChkTmem, 44)) {
+          tmem_ld_x32(tmem + lane_off + col, v0);
+          tmem_ld_x32(tmem + lane_off + col + 32, v1);
+        }
+        tc_fence_before();
+        mbar_arrive(bar(C::kDKVEmpty));
+        uint16_t* dst = static_cast<uint16_t*>(h == 0 ? a.dv : a.dk) + ((size_t)bh * (size_t)Nk + (size_t)kv) * DR;
+        if (!dead_key) {
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const uint32_t x0 = cc ? v1[2 * e] : v0[2 * e], x1 = cc ? v1[2 * e + 1] : v0[2 * e + 1];
+              pk[e] = pack2<F16>(u2f(x0) * mul, u2f(x1) * mul);
+            }
+#pragma unroll
+            for (int w4 = 0; w4 < 4; ++w4)
+              st_global_v4(dst + 32 * cc + 8 * w4, pk[4 * w4], pk[4 * w4 + 1], pk[4 * w4 + 2], pk[4 * w4 + 3]);
+          }
+        }
+      }
+      if (++st == QS) {
+        st = 0;
+        qph ^= 1;
+      }
+      if (++i == n) {
+        i = 0;
+        ++k;
+      }
+    }
+    tc_fence_before();
+    named_bar_arrive(kEndBarrier, kThreads);
+  } else if (warp < kRedWarp + kRedWarps) {
+    // ------------------------------------------------------------ dQ reductions (as in the d = 64 kernel)
+    setmaxnreg_dec<kRegsRed>();
+    const int gq = warp & 3;
+    const int r = gq * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(gq * 32) << 16;
+    uint32_t t_prev = 0;
+    uint32_t pause_ns = 0;
+    int k = 0, i = 0, wrow0 = wrow_of(unit_of(0) / n_kv);
+    for (int g = 0; g < total; ++g) {
+      if (g > 0 && ++i == n) {
+        i = 0;
+        ++k;
+        wrow0 = wrow_of(unit_of(k) / n_kv);
+      }
+      bool ok = mbar_wait_inl(bar(C::kDqFull), (uint32_t)(g & 1), wc, site(44));
+      ok = __all_sync(kFull, ok);
+      if (!ok) break;
+      {
+        const uint32_t t_now = (uint32_t)clock();
+        if (g > 0) {
+          const uint32_t pp = (t_now - t_prev) / 40u;
+          pause_ns = pp < 200u ? pp : 200u;
+        }
+        t_prev = t_now;
+      }
+      tc_fence_after();
+      uint32_t v[64];
+      const uint32_t dq_col = s_cols(g) + 64u;
+      const bool chk = dcheck(tmem_ok(dq_col, 64, 512), wc, kChkTmem, 45);
+      if (chk) tmem_ld_x64(tmem + lane_off + dq_col, v);
+      tc_fence_before();
+      mbar_arrive(bar(C::kDqDrained));
+      if (!chk) continue;
+      float* base = a.dqacc + ((size_t)wrow0 + (size_t)(i * kBM) + (size_t)r) * D;
+#pragma unroll
+      for (int c = 0; c < 64; c += 4) {
+        red_add_v4_f32(base + c, u2f(v[c]), u2f(v[c + 1]), u2f(v[c + 2]), u2f(v[c + 3]));
+        if (c < 60 && pause_ns > 0) __nanosleep(pause_ns / 3u);
+      }
+    }
+    tc_fence_before();
+    named_bar_arrive(kEndBarrier, kThreads);
+  } else {
+  setmaxnreg_dec<kRegsMisc>();
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&a.tm_q);
+      prefetch_tmap(&a.tm_k);
+      prefetch_tmap(&a.tm_v);
+      prefetch_tmap(&a.tm_do);
+      int issued_kv[2] = {}, issued_q[QS] = {};
+      int g = 0;
+      bool ok = true;
+      for (int k = 0; ok && k < my_units; ++k) {
+        const int u = unit_of(k);
+        const int bh = u / n_kv, kv0 = (u % n_kv) * kBN;
+        const int b = k & 1;
+        // Buffer b last held unit k − 2: its products must be done.
+        if (k >= 2 && !mbar_wait_inl(bar(C::kKVEmpty + b), (uint32_t)(((k >> 1) - 1) & 1), wc, site(45))) break;
+        mbar_arrive_expect_tx(bar(C::kKVFull + b), 2u * C::kTile);
+        load_rows(sbase + C::kK + b * C::kTile, &a.tm_k, bar(C::kKVFull + b), 0, kv0, Nk, bh);
+        load_rows(sbase + C::kV + b * C::kTile, &a.tm_v, bar(C::kKVFull + b), 0, kv0, Nk, bh);
+        ++issued_kv[b];
+        const int wrow0 = wrow_of(bh);
+        for (int i = 0; i < n; ++i, ++g) {
+          const int s = g % QS;
+          if (g >= QS && !mbar_wait_inl(bar(C::kQEmpty + s), (uint32_t)((g / QS - 1) & 1), wc, site(46))) {
+            ok = false;
+            break;
+          }
+          const int q0 = i * kBM;
+          mbar_arrive_expect_tx(bar(C::kQFull + s), 2u * C::kTile + 2u * kBM * 4);
+          load_rows(sbase + C::kQ + s * C::kTile, &a.tm_q, bar(C::kQFull + s), 0, q0, Nq, bh);
+          load_rows(sbase + C::kDO + s * C::kTile, &a.tm_do, bar(C::kQFull + s), 0, q0, Nq, bh);
+          load_bulk(sbase + C::kLSE + s * kBM * 4, a.lse2 + wrow0 + q0, kBM * 4, bar(C::kQFull + s));
+          load_bulk(sbase + C::kDV + s * kBM * 4, a.dvec + wrow0 + q0, kBM * 4, bar(C::kQFull + s));
+          ++issued_q[s];
+        }
+      }
+      for (int b = 0; b < 2; ++b)
+        if (issued_kv[b] > 0) mbar_wait_drain_inl(bar(C::kKVFull + b), (uint32_t)((issued_kv[b] - 1) & 1), wc, site(47));
+      for (int s = 0; s < QS; ++s)
+        if (issued_q[s] > 0) mbar_wait_drain_inl(bar(C::kQFull + s), (uint32_t)((issued_q[s] - 1) & 1), wc, site(47));
+    }
+    __syncwarp();
+    named_bar_arrive(kEndBarrier, kThreads);
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_f16kind(128, kBM, false, false, F16);  // Sᵀ = K Qᵀ, dPᵀ = V dOᵀ
+      constexpr uint32_t kIdKV = idesc_f16kind(128, DR, false, true, F16);   // dV += Pᵀ dO, dK += dSᵀ Q
+      constexpr uint32_t kIdQ = idesc_f16kind(128, D, true, true, F16);      // dQ = dS K (M = queries, N = 64)
+      int kv_ready = -1;          // last unit whose K/V tile was seen complete
+      auto need_kv = [&](int k) -> bool {
+        if (kv_ready >= k) return true;
+        if (!mbar_wait_inl(bar(C::kKVFull + (k & 1)), (uint32_t)((k >> 1) & 1), wc, site(48))) return false;
+        kv_ready = k;
+        return true;
+      };
+      // Sᵀ (A = K) or dPᵀ (A = V) of a step whose unit uses K/V buffer b and
+      // whose Q/dO sit in stage st, into `col`.
+      auto issue_sd = [&](int b, int st, uint32_t col, bool scores) {
+        const uint32_t a_tile = sbase + (scores ? C::kK : C::kV) + b * C::kTile;
+        const uint32_t b_tile = sbase + (scores ? C::kQ : C::kDO) + st * C::kTile;
+        if (!(dcheck(tmem_ok(col, kBM, 512), wc, kChkTmem, 46) &&
+              dcheck(smem_ok(a_tile - sbase, C::kTile, C::kBar, 1024), wc, kChkSmem, 46) &&
+              dcheck(smem_ok(b_tile - sbase, C::kTile, C::kBar, 1024), wc, kChkSmem, 46)))
+          return;
+#pragma unroll
+        for (int ks = 0; ks < DR / 16; ++ks)
+          mma_ss(tmem + col, sdesc_sw128(a_tile + (uint32_t)(ks * 32), 16, 1024),
+                 sdesc_sw128(b_tile + (uint32_t)(ks * 32), 16, 1024), kIdS, ks > 0 ? 1u : 0u);
+      };
+      bool ok = total > 0 && need_kv(0) && mbar_wait_inl(bar(C::kQFull), 0, wc, site(49));
+      if (ok) {
+        tc_fence_after();
+        issue_sd(0, 0, s_cols(0), true);
+        tc_commit(bar(s_bar_id(0)));
+        issue_sd(0, 0, C::kColDP, false);
+        tc_commit(bar(C::kDPFull));
+        if (total > 1) {
+          const int k1 = n == 1 ? 1 : 0;
+          ok = need_kv(k1) && mbar_wait_inl(bar(C::kQFull + 1), 0, wc, site(49));
+          if (ok) {
+            tc_fence_after();
+            issue_sd(k1 & 1, 1, s_cols(1), true);
+            tc_commit(bar(s_bar_id(1)));
+          }
+        }
+      }
+      // Unit k, step i within it and Q/dO stage st of step g, kept incrementally.
+      int k = 0, i = 0, st = 0;
+      for (int g = 0; ok && g < total; ++g) {
+        const int b = k & 1;
+        if (!mbar_wait_inl(bar(C::kPdsFull), (uint32_t)(g & 1), wc, site(50))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ds = sbase + C::kDS;
+        const uint32_t kb = sbase + C::kK + b * C::kTile;
+        const uint32_t qb = sbase + C::kQ + st * C::kTile;
+        const uint32_t ob = sbase + C::kDO + st * C::kTile;
+        const uint32_t sb = s_cols(g);
+        const bool chk = dcheck(tmem_ok(sb, 128, 512) && tmem_ok(C::kColDV, DR, 512) && tmem_ok(C::kColDK, DR, 512),
+                                wc, kChkTmem, 47) &&
+                         dcheck(smem_ok(C::kDS, 2 * kBox, C::kBar, 1024) && smem_ok(qb - sbase, C::kTile, C::kBar, 1024) &&
+                                    smem_ok(ob - sbase, C::kTile, C::kBar, 1024) &&
+                                    smem_ok(kb - sbase, C::kTile, C::kBar, 1024),
+                                wc, kChkSmem, 47);
+        // dQ = dS K into the spent half of this step's score buffer.
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          if (!chk) break;
+          mma_ss(tmem + sb + 64u, sdesc_sw128(ds + (uint32_t)(ks * 2048), kBox, 1024),
+                 sdesc_sw128(kb + (uint32_t)(ks * 2048), kBox, 1024), kIdQ, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(C::kDqFull));
+        // The unit's first dK and dV start the accumulators afresh: the
+        // previous unit's must have been read out.
+        if (i == 0 && k > 0 && !mbar_wait_inl(bar(C::kDKVEmpty), (uint32_t)((k - 1) & 1), wc, site(51))) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int ks = 0; ks < kBM / 16; ++ks)
+          if (chk) mma_ss(tmem + C::kColDK, sdesc_sw128(ds + (uint32_t)((ks >> 2) * kBox + (ks & 3) * 32), 16, 1024),
+                 sdesc_sw128(qb + (uint32_t)(ks * 2048), kBox, 1024), kIdKV, (i > 0 || ks > 0) ? 1u : 0u);
+        const int st1 = st + 1 == QS ? 0 : st + 1;
+        if (g + 1 < total) {
+          // Its Q/dO stage and K/V buffer were waited for when its scores were issued.
+          issue_sd(i + 1 == n ? (b ^ 1) : b, st1, C::kColDP, false);
+          tc_commit(bar(C::kDPFull));
+        }
+#pragma unroll
+        for (int ks = 0; ks < kBM / 16; ++ks)
+          if (chk) mma_ts(tmem + C::kColDV, tmem + sb + (uint32_t)(8 * ks),
+                 sdesc_sw128(ob + (uint32_t)(ks * 2048), kBox, 1024), kIdKV, (i > 0 || ks > 0) ? 1u : 0u);
+        tc_commit(bar(C::kQEmpty + st));
+        if (i == n - 1) {
+          tc_commit(bar(C::kDKVFull));
+          tc_commit(bar(C::kKVEmpty + b));
+        }
+        if (g + 2 < total) {
+          // Step g + 2 belongs to unit k + (i + 2) / n (two units on when n = 1).
+          const int k2 = k + (i + 2 >= n ? 1 : 0) + (n == 1 ? 1 : 0);
+          const int st2 = st1 + 1 == QS ? 0 : st1 + 1;
+          if (!need_kv(k2) ||
+              !mbar_wait_inl(bar(C::kQFull + st2), (uint32_t)(((g + 2) / QS) & 1), wc, site(52)) ||
+              !mbar_wait_inl(bar(C::kDqDrained), (uint32_t)(g & 1), wc, site(53))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_sd(k2 & 1, st2, sb, true);
+          tc_commit(bar(s_bar_id(g)));
+        }
+        st = st1;
+        if (++i == n) {
+          i = 0;
+          ++k;
+        }
+      }
+      tc_commit(bar(C::kMmaDone));
+      mbar_wait_drain_inl(bar(C::kMmaDone), 0, wc, site(54));
+    }
+    __syncwarp();
+    named_bar_sync(kEndBarrier, kThreads);
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  } else {
+    named_bar_arrive(kEndBarrier, kThreads);   // warps 14, 15
+  }
+  }
+}
+
+template <bool RAGGED, bool F16>
+cudaError_t launch_persist64(const BwdArgs& a, cudaStream_t s) {
+  auto kern = fa_bwd_bf16_persist64_kernel<RAGGED, F16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BwdCfgP64::kBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)a.persist_ctas, kThreads, BwdCfgP64::kBytes, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <int DR, bool CAUSAL, bool RAGGED, bool F16>
 cudaError_t launch_impl(const BwdArgs& a, cudaStream_t s) {
   auto kern = fa_bwd_bf16_kernel<DR, CAUSAL, RAGGED, F16>;
@@ -855,6 +1349,10 @@ static cudaError_t dispatch_bwd(const BwdArgs& a, bool ragged, cudaStream_t s) {
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t s) {
   if (a.d == 256) return launch_bwd_d256(a, s);
   const bool ragged = a.Nq % kBM != 0 || a.Nk % kBN != 0;
+  if (a.persist_ctas > 0 && a.d == 64 && !a.causal) {
+    if (a.f16) return ragged ? launch_persist64<true, true>(a, s) : launch_persist64<false, true>(a, s);
+    return ragged ? launch_persist64<true, false>(a, s) : launch_persist64<false, false>(a, s);
+  }
   return a.f16 ? dispatch_bwd<true>(a, ragged, s) : dispatch_bwd<false>(a, ragged, s);
 }
 

@@ -103,7 +103,16 @@ struct BwdArgs {
   float scale;
   int causal;
   unsigned int* fault;
+  // > 0: the persistent backward (d = 64, no mask) on this many CTAs, each
+  // walking the K/V tiles with a stride of persist_ctas.
+  int persist_ctas;
 };
+// Largest query-tile count per head for which the d = 64 backward runs
+// persistent when there are more K/V tiles than SMs.  Measured on GB300
+// (B·H·N fixed at 128·1024, d = 64): 2 tiles +13.5 %, 4 +7.7 %, 8 +1.2 %,
+// 16 −4.1 % against one K/V tile per CTA: its steps are a little slower, so
+// it pays only where a CTA's start-up and drain weigh most.
+constexpr int kBwdPersistMaxTiles = 8;
 int bwd_bf16_block_m(int d);
 size_t bwd_bf16_smem_bytes(int d);
 // Dispatches on d (64, 96, 128; 256 goes to launch_bwd_d256).

@@ -121,6 +121,27 @@ def test_bf16_persistent_forward(B, H, N, d):
     compare({key: np.stack([val[b, h] for b, h in heads]) for key, val in gpu.items()}, ref, "bf16")
 
 
+@pytest.mark.parametrize("dtype,B,H,N", [("bf16", 1, 200, 128), ("bf16", 2, 96, 256), ("bf16", 8, 24, 1024),
+                                          ("bf16", 3, 40, 700), ("fp16", 2, 64, 384)])
+def test_persistent_backward_d64(dtype, B, H, N):
+    """d = 64 without the mask, more K/V tiles than SMs and at most 8 query
+    tiles per head: the backward runs as one persistent CTA per SM walking
+    the K/V tiles (1, 2, 8 and ragged query tiles per unit; fp16 too).
+    First and last heads against the oracle, every head for inf/NaN and the
+    gradient invariants."""
+    q, k, v, do = make_inputs(B, H, N, 64, dtype, "normal", 60 + N + H, device="cuda")
+    scale = 64 ** -0.5
+    gpu = run_library(q, k, v, do, False, scale)
+    for key in ("O", "LSE", "dQ", "dK", "dV"):
+        assert np.all(np.isfinite(gpu[key])), key
+    dk, dv, dov = gpu["dK"], gpu["dV"], to64(do)
+    assert np.linalg.norm(dk.sum(axis=2)) <= 2e-2 * np.linalg.norm(dk)
+    assert np.linalg.norm(dv.sum(axis=2) - dov.sum(axis=2)) <= 2e-2 * np.linalg.norm(dv)
+    heads = [(0, 0), (B - 1, H - 1)]
+    ref = run_oracle_heads(q, k, v, do, False, scale, heads)
+    compare({key: np.stack([val[b, h] for b, h in heads]) for key, val in gpu.items()}, ref, "bf16")
+
+
 def test_bf16_stress_small():
     """Scores scaled to magnitudes in the hundreds (Q, K drawn ×8, d = 64)."""
     errs = _check(2, 2, 512, 64, False, "bf16", dist="stress", seed=5)

@@ -338,11 +338,22 @@ def time_steps(h, flush, warmup, steps=None, min_seconds=0.0, world=1):
     }
 
 
-def dominant_kernel(w):
+# The library's choice of backward kernel at d = 64 without the mask
+# (kBwdPersistMaxTiles in csrc/fa_kernels.h): the persistent form when a head
+# has at most this many 128-row query tiles and there are more K/V tiles than SMs.
+BWD_PERSIST_MAX_TILES = 8
+
+
+def dominant_kernel(w, n_sms=0):
+    if n_sms <= 0 and torch.cuda.is_available():
+        n_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     if w.dtype == "fp32":
         return "dkv_f32_kernel + dq_f32_kernel (fa_bwd_tiles, fp32 SIMT)"
     if w.d == 256:
         return f"fa_bwd_d256 dkv + dq kernels<causal={int(w.causal)}> (fa_bwd_tiles)"
+    tiles = -(-w.N // 128)
+    if w.d == 64 and not w.causal and tiles <= BWD_PERSIST_MAX_TILES and w.B * w.H * tiles > n_sms > 0:
+        return "fa_bwd_bf16_persist64_kernel (fa_bwd_tiles)"
     return f"fa_bwd_bf16_kernel<d={w.d},causal={int(w.causal)}> (fa_bwd_tiles)"
 
 

@@ -60,3 +60,15 @@ def test_smi_fallback_parses_reasons():
     assert out["samples"] == 2 and out["sm_max_mhz"] == 2070.0
     assert out["sm_mhz"] == (2070 + 1980) / 2
     assert out["reasons"] == ["sw_power_cap"]
+
+
+def test_dominant_kernel_names_the_persistent_backward():
+    """The d = 64 unmasked stress workload (8 query tiles a head, 1024 K/V
+    tiles) runs the persistent backward on a 152-SM GPU; with more SMs than
+    K/V tiles, or at d = 128, the one-tile-per-CTA kernel."""
+    import bench
+    from exact_tiled_attention_12_gb300.synthetic import WORKLOADS
+
+    assert bench.dominant_kernel(WORKLOADS["bf16_stress_n1024"], 152).startswith("fa_bwd_bf16_persist64_kernel")
+    assert bench.dominant_kernel(WORKLOADS["bf16_stress_n1024"], 2048).startswith("fa_bwd_bf16_kernel<d=64")
+    assert bench.dominant_kernel(WORKLOADS["bf16_n2048"], 152).startswith("fa_bwd_bf16_kernel<d=128")

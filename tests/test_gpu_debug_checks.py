@@ -59,6 +59,8 @@ CASES = [
     ("bf16", 1, 2, 300, 300, 256, True),     # d = 256, ragged
     ("bf16", 2, 2, 1, 4096, 128, False),     # a decoding step
     ("fp32", 1, 1, 96, 96, 64, True),
+    ("bf16", 8, 32, 1000, 1000, 64, False),  # persistent forward and persistent d = 64 backward, ragged
+    ("bf16", 4, 40, 2048, 2048, 128, False), # persistent forward at d = 128
 ]
 
 

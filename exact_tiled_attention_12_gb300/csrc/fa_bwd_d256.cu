@@ -26,11 +26,13 @@
 //      dQ += dS K_j                        (A = dS from tensor memory, N = 256)
 //    Tensor memory: S_b [64b, 64b + 64), dP_b [128 + 64b, ...), dQ [256, 512);
 //    dS (16-bit) is written over the dP columns its thread read.  The MMA
-//    order dQ_j, dP_{j+2}, S_{j+2} overlaps the elementwise work of tile
-//    j + 1 with the products; K streams through a ring of two tiles (released
-//    once dQ_j has read them), V through one.  Each K or V tile is released
-//    with one commit, not one per box: the MMA thread's commits sit on the
-//    issue path (on GB300 one commit per box was 1.8 % slower at N = 8192).
+//    order dQ_j, S_{j+1}, dP_{j+2} overlaps the elementwise work of tile
+//    j + 1 with dP_{j+2}; K streams through a ring of two tiles (released
+//    once dQ_j has read them, so K_{j+1} has had a whole step to load when
+//    S_{j+1} wants it), V through one.  Each K or V tile is released with one
+//    commit, not one per box: the MMA thread's commits sit on its issue path.
+//    (On GB300, against dQ_j, dP_{j+2}, S_{j+2} with one commit per box:
+//    +1.8 % for the commits, +1-2.5 % for the order.)
 //
 // Both kernels: warps 0-7 do the elementwise work, thread (w, lane) owning
 // query row 32(w mod 4) + lane and key columns 32⌊w/4⌋ .. +31 of a 64-key
@@ -100,9 +102,9 @@ static_assert(kBytes <= 232448, "shared memory exceeds the 227 KB a CTA may use"
 enum Bar : int {
   kKVFull = 0,
   kQFull = 1,        // + box (box 0 also carries −LSE₂ and −D)
-  kQEmpty = 5,       // + box
+  kQEmpty = 5,       // + box; only boxes 0 and 2 are used: one release per half of the head dims
   kDOFull = 9,       // + box
-  kDOEmpty = 13,     // + box
+  kDOEmpty = 13,     // + box, as kQEmpty
   kSFull = 17,
   kDPFull = 18,
   kPdsFull = 19,
@@ -298,9 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
       bool ok = true;
       for (int i = 0; ok && i < n; ++i) {
         const int q0 = (i0 + i) * kBM;
-        // Q boxes free up first (dKᵀ is issued before dVᵀ), then dO boxes.
+        // Q boxes free up first (dKᵀ is issued before dVᵀ), then dO boxes; the
+        // two boxes of a half of the head dims are released with one commit
+        // (one per box measured 1-2 % slower on GB300: the MMA thread's
+        // commits sit on its issue path).
         for (int bx = 0; ok && bx < 4; ++bx) {
-          if (i > 0 && !mbar_wait(bar(kQEmpty + bx), (uint32_t)((i - 1) & 1), wc, site(5))) {
+          if (i > 0 && (bx & 1) == 0 && !mbar_wait(bar(kQEmpty + bx), (uint32_t)((i - 1) & 1), wc, site(5))) {
             ok = false;
             break;
           }
@@ -313,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
           ++issued_q[bx];
         }
         for (int bx = 0; ok && bx < 4; ++bx) {
-          if (i > 0 && !mbar_wait(bar(kDOEmpty + bx), (uint32_t)((i - 1) & 1), wc, site(6))) {
+          if (i > 0 && (bx & 1) == 0 && !mbar_wait(bar(kDOEmpty + bx), (uint32_t)((i - 1) & 1), wc, site(6))) {
             ok = false;
             break;
           }
@@ -379,7 +384,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
             if (chk) mma_ss(tmem + kColDK + 64u * h, sdesc_add(q_mn, 2 * h * kQBox + ks * 2048), sdesc_add(ds_mn, ks * 2048),
                    kIdT, (i > 0 || ks > 0) ? 1u : 0u);
           tc_commit(bar(kQEmpty + 2 * h));
-          tc_commit(bar(kQEmpty + 2 * h + 1));
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -388,7 +392,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
             if (chk) mma_ss(tmem + kColDV + 64u * h, sdesc_add(do_mn, 2 * h * kQBox + ks * 2048), sdesc_add(p_mn, ks * 2048),
                    kIdT, (i > 0 || ks > 0) ? 1u : 0u);
           tc_commit(bar(kDOEmpty + 2 * h));
-          tc_commit(bar(kDOEmpty + 2 * h + 1));
         }
         // The next tile's S and dP overwrite the columns the compute warps
         // have read; its P / dS stores wait for S, i.e. for these products.
@@ -645,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
         return true;
       };
       // K_0, V_0, K_1, V_1, then V_j before K_j: V_j waits for dP_{j-1},
-      // K_j for dQ_{j-2}, and the MMA order is dQ_{j-2}, dP_j, S_j.
+      // K_j for dQ_{j-2}; the MMA order is dQ_{j-2}, S_{j-1}, dP_j.
       bool ok = load_k(0) && load_v(0);
       if (ok && n > 1) ok = load_k(1) && load_v(1);
       for (int j = 2; ok && j < n; ++j) ok = load_v(j) && load_k(j);
@@ -714,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
       };
       bool ok = mbar_wait(bar(kQFull), 0, wc, site(10));
       if (ok && n > 0) ok = issue_s(0) && issue_dp(0);
-      if (ok && n > 1) ok = issue_s(1) && issue_dp(1);
+      if (ok && n > 1) ok = issue_dp(1);
       for (int j = 0; ok && j < n; ++j) {
         if (!mbar_wait(bar(kDsFull + (j & 1)), (uint32_t)((j >> 1) & 1), wc, site(11))) {
           ok = false;
@@ -722,7 +725,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
         }
         tc_fence_after();
         issue_dq(j);
-        if (j + 2 < n) ok = issue_dp(j + 2) && issue_s(j + 2);
+        if (j + 1 < n) ok = issue_s(j + 1);
+        if (ok && j + 2 < n) ok = issue_dp(j + 2);
       }
       if (ok) tc_commit(bar(kDqFull));
       tc_commit(bar(kMmaDone));

@@ -17,9 +17,9 @@
 //      dVᵀ_h += dO_hᵀ P, dKᵀ_h += Q_hᵀ dS   (M = 128 head dims of half h, N = 64)
 //    Tensor memory: S [0, 64), dP [64, 128), dVᵀ [128, 256), dKᵀ [256, 384).
 //    P and dS go to shared memory ([query][key], 128-byte swizzle) as the B
-//    operands.  Q and dO stream box by box (64 head dims × 128 rows): a box
-//    is reloaded for the next query tile as soon as the products that read it
-//    have completed.
+//    operands.  Q and dO stream in boxes of 64 head dims × 128 rows, two
+//    boxes (one half of the head dims) per barrier: a half is reloaded for
+//    the next query tile as soon as the products that read it have completed.
 //
 //  * dq: a CTA owns 128 queries and walks 64-key tiles, recomputing S and dP:
 //      S_b = Q K_jᵀ, dP_b = dO V_jᵀ into buffer b = j mod 2
@@ -29,10 +29,11 @@
 //    order dQ_j, S_{j+1}, dP_{j+2} overlaps the elementwise work of tile
 //    j + 1 with dP_{j+2}; K streams through a ring of two tiles (released
 //    once dQ_j has read them, so K_{j+1} has had a whole step to load when
-//    S_{j+1} wants it), V through one.  Each K or V tile is released with one
-//    commit, not one per box: the MMA thread's commits sit on its issue path.
-//    (On GB300, against dQ_j, dP_{j+2}, S_{j+2} with one commit per box:
-//    +1.8 % for the commits, +1-2.5 % for the order.)
+//    S_{j+1} wants it), V through one.  Each K or V tile lands on one barrier
+//    and is released with one commit, not one per box: the MMA thread's waits
+//    and commits sit on its issue path.  (On GB300, against dQ_j, dP_{j+2},
+//    S_{j+2} with a wait and a commit per box: +1.8 % for the commits,
+//    +1-2.5 % for the order, +3-4 % for the waits.)
 //
 // Both kernels: warps 0-7 do the elementwise work, thread (w, lane) owning
 // query row 32(w mod 4) + lane and key columns 32⌊w/4⌋ .. +31 of a 64-key
@@ -101,10 +102,14 @@ static_assert(kBytes <= 232448, "shared memory exceeds the 227 KB a CTA may use"
 
 enum Bar : int {
   kKVFull = 0,
-  kQFull = 1,        // + box (box 0 also carries −LSE₂ and −D)
-  kQEmpty = 5,       // + box; only boxes 0 and 2 are used: one release per half of the head dims
-  kDOFull = 9,       // + box
-  kDOEmpty = 13,     // + box, as kQEmpty
+  // Q and dO land and are released per half of the head dims (boxes 0-1 on
+  // barrier + 0, boxes 2-3 on + 2; + 1 and + 3 unused): the MMA thread's
+  // waits and commits sit on its issue path (one per box measured 5 % slower
+  // on GB300).
+  kQFull = 1,        // + 2·half (half 0 also carries −LSE₂ and −D)
+  kQEmpty = 5,       // + 2·half
+  kDOFull = 9,       // + 2·half
+  kDOEmpty = 13,     // + 2·half
   kSFull = 17,
   kDPFull = 18,
   kPdsFull = 19,
@@ -300,17 +305,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
       bool ok = true;
       for (int i = 0; ok && i < n; ++i) {
         const int q0 = (i0 + i) * kBM;
-        // Q boxes free up first (dKᵀ is issued before dVᵀ), then dO boxes; the
-        // two boxes of a half of the head dims are released with one commit
-        // (one per box measured 1-2 % slower on GB300: the MMA thread's
-        // commits sit on its issue path).
+        // Q boxes free up first (dKᵀ is issued before dVᵀ), then dO boxes,
+        // half by half of the head dims.
         for (int bx = 0; ok && bx < 4; ++bx) {
           if (i > 0 && (bx & 1) == 0 && !mbar_wait(bar(kQEmpty + bx), (uint32_t)((i - 1) & 1), wc, site(5))) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(kQFull + bx), (uint32_t)kQBox + (bx == 0 ? 2u * kBM * 4 : 0u));
-          load_rows(sbase + kQ + bx * kQBox, &a.tm_q, bar(kQFull + bx), 64 * bx, q0, Nq);
+          if ((bx & 1) == 0) mbar_arrive_expect_tx(bar(kQFull + bx), 2u * kQBox + (bx == 0 ? 2u * kBM * 4 : 0u));
+          load_rows(sbase + kQ + bx * kQBox, &a.tm_q, bar(kQFull + (bx & 2)), 64 * bx, q0, Nq);
           if (bx == 0) {
             load_bulk(sbase + kLSE, a.lse2 + wrow0 + q0, kBM * 4, bar(kQFull));
             load_bulk(sbase + kDV, a.dvec + wrow0 + q0, kBM * 4, bar(kQFull));
@@ -322,14 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(kDOFull + bx), (uint32_t)kQBox);
-          load_rows(sbase + kDO + bx * kQBox, &a.tm_do, bar(kDOFull + bx), 64 * bx, q0, Nq);
+          if ((bx & 1) == 0) mbar_arrive_expect_tx(bar(kDOFull + bx), 2u * kQBox);
+          load_rows(sbase + kDO + bx * kQBox, &a.tm_do, bar(kDOFull + (bx & 2)), 64 * bx, q0, Nq);
           ++issued_do[bx];
         }
       }
       // Never leave the CTA with copies in flight.
       mbar_wait_drain(bar(kKVFull), 0, wc, site(7));
-      for (int bx = 0; bx < 4; ++bx) {
+      for (int bx = 0; bx < 4; bx += 2) {
         if (issued_q[bx] > 0) mbar_wait_drain(bar(kQFull + bx), (uint32_t)((issued_q[bx] - 1) & 1), wc, site(7));
         if (issued_do[bx] > 0) mbar_wait_drain(bar(kDOFull + bx), (uint32_t)((issued_do[bx] - 1) & 1), wc, site(7));
       }
@@ -347,8 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
                          dcheck(smem_ok(a_tile - sbase, 4 * kQBox, kBar, 1024) &&
                                     smem_ok(b_tile - sbase, 4 * kKBox, kBar, 1024), wc, kChkSmem, 54);
         for (int bx = 0; bx < 4; ++bx) {
-          if (!mbar_wait(bar(full + bx), (uint32_t)(i & 1), wc, site(8))) return false;
-          tc_fence_after();
+          if ((bx & 1) == 0) {
+            if (!mbar_wait(bar(full + bx), (uint32_t)(i & 1), wc, site(8))) return false;
+            tc_fence_after();
+          }
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             if (chk) mma_ss(dcol, sdesc_add(ad, bx * kQBox + 32u * k), sdesc_add(bd, bx * kKBox + 32u * k), kIdS,
@@ -434,9 +439,9 @@ static_assert(kBytes <= 232448, "shared memory exceeds the 227 KB a CTA may use"
 
 enum Bar : int {
   kQFull = 0,                    // Q, dO, −LSE₂, −D
-  kKFull = 1,                    // + ring slot (box)
+  kKFull = 1,                    // + tile of the ring (2; kKSlots reserved): its four boxes land together
   kKEmpty = kKFull + kKSlots,    // + tile of the ring (2): its four boxes are released together
-  kVFull = kKEmpty + 2,          // + box
+  kVFull = kKEmpty + 2,          // the V tile (4 reserved)
   kVEmpty = kVFull + 4,          // the V tile, released once dP has read all four boxes
   kSFull = kVEmpty + 1,          // + buffer (2)
   kDPFull = kSFull + 2,          // + buffer
@@ -517,9 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kQFull), 1);
-    for (int s = 0; s < kKSlots; ++s) mbar_init(bar(kKFull + s), 1);
+    for (int t = 0; t < 2; ++t) mbar_init(bar(kKFull + t), 1);
     for (int t = 0; t < 2; ++t) mbar_init(bar(kKEmpty + t), 1);
-    for (int bx = 0; bx < 4; ++bx) mbar_init(bar(kVFull + bx), 1);
+    mbar_init(bar(kVFull), 1);
     mbar_init(bar(kVEmpty), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(kSFull + b), 1);
@@ -632,8 +637,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
         for (int bx = 0; bx < 4; ++bx) {
           const int gi = 4 * j + bx, slot = gi % kKSlots, round = gi / kKSlots;
           if (round > 0 && bx == 0 && !mbar_wait(bar(kKEmpty + (j & 1)), (uint32_t)((round - 1) & 1), wc, site(5))) return false;
-          mbar_arrive_expect_tx(bar(kKFull + slot), (uint32_t)kKBox);
-          load_rows(sbase + kK + slot * kKBox, &a.tm_k, bar(kKFull + slot), 64 * bx, j * kBN, Nk);
+          if (bx == 0) mbar_arrive_expect_tx(bar(kKFull + (j & 1)), 4u * kKBox);
+          load_rows(sbase + kK + slot * kKBox, &a.tm_k, bar(kKFull + (j & 1)), 64 * bx, j * kBN, Nk);
           ++k_boxes;
         }
         return true;
@@ -641,8 +646,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
       auto load_v = [&](int j) -> bool {
         for (int bx = 0; bx < 4; ++bx) {
           if (j > 0 && bx == 0 && !mbar_wait(bar(kVEmpty), (uint32_t)((j - 1) & 1), wc, site(6))) return false;
-          mbar_arrive_expect_tx(bar(kVFull + bx), (uint32_t)kKBox);
-          load_rows(sbase + kV + bx * kKBox, &a.tm_v, bar(kVFull + bx), 64 * bx, j * kBN, Nk);
+          if (bx == 0) mbar_arrive_expect_tx(bar(kVFull), 4u * kKBox);
+          load_rows(sbase + kV + bx * kKBox, &a.tm_v, bar(kVFull), 64 * bx, j * kBN, Nk);
           ++v_loads[bx];
         }
         return true;
@@ -653,13 +658,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
       if (ok && n > 1) ok = load_k(1) && load_v(1);
       for (int j = 2; ok && j < n; ++j) ok = load_v(j) && load_k(j);
       mbar_wait_drain(bar(kQFull), 0, wc, site(7));
-      for (int s = 0; s < kKSlots; ++s) {
-        if (s >= k_boxes) continue;
-        const int last = s + (k_boxes - 1 - s) / kKSlots * kKSlots;
-        mbar_wait_drain(bar(kKFull + s), (uint32_t)((last / kKSlots) & 1), wc, site(7));
+      const int k_tiles = k_boxes / 4;
+      for (int t = 0; t < 2 && t < k_tiles; ++t) {
+        const int last = t + (k_tiles - 1 - t) / 2 * 2;
+        mbar_wait_drain(bar(kKFull + t), (uint32_t)((last / 2) & 1), wc, site(7));
       }
-      for (int bx = 0; bx < 4; ++bx)
-        if (v_loads[bx] > 0) mbar_wait_drain(bar(kVFull + bx), (uint32_t)((v_loads[bx] - 1) & 1), wc, site(7));
+      if (v_loads[0] > 0) mbar_wait_drain(bar(kVFull), (uint32_t)((v_loads[0] - 1) & 1), wc, site(7));
     }
   } else {
     // ------------------------------------------------------------ MMA issuer
@@ -674,8 +678,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
         const bool chk = dcheck(tmem_ok(kColS + 64u * (j & 1), kBN, 512), wc, kChkTmem, 61);
         for (int bx = 0; bx < 4; ++bx) {
           const int gi = 4 * j + bx, slot = gi % kKSlots;
-          if (!mbar_wait(bar(kKFull + slot), (uint32_t)((gi / kKSlots) & 1), wc, site(8))) return false;
-          tc_fence_after();
+          if (bx == 0) {
+            if (!mbar_wait(bar(kKFull + (j & 1)), (uint32_t)((gi / kKSlots) & 1), wc, site(8))) return false;
+            tc_fence_after();
+          }
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             if (chk) mma_ss(col, sdesc_add(q_k, bx * kQBox + 32u * k), sdesc_add(k_k, slot * kKBox + 32u * k), kIdS,
@@ -688,8 +694,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dq_kernel(const __gri
         const uint32_t col = tmem + kColDP + 64u * (uint32_t)(j & 1);
         const bool chk = dcheck(tmem_ok(kColDP + 64u * (j & 1), kBN, 512), wc, kChkTmem, 62);
         for (int bx = 0; bx < 4; ++bx) {
-          if (!mbar_wait(bar(kVFull + bx), (uint32_t)(j & 1), wc, site(9))) return false;
-          tc_fence_after();
+          if (bx == 0) {
+            if (!mbar_wait(bar(kVFull), (uint32_t)(j & 1), wc, site(9))) return false;
+            tc_fence_after();
+          }
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             if (chk) mma_ss(col, sdesc_add(do_k, bx * kQBox + 32u * k), sdesc_add(v_k, bx * kKBox + 32u * k), kIdS,

@@ -102,20 +102,19 @@ static_assert(kBytes <= 232448, "shared memory exceeds the 227 KB a CTA may use"
 
 enum Bar : int {
   kKVFull = 0,
-  // Q and dO land and are released per half of the head dims (boxes 0-1 on
-  // barrier + 0, boxes 2-3 on + 2; + 1 and + 3 unused): the MMA thread's
-  // waits and commits sit on its issue path (one per box measured 5 % slower
-  // on GB300).
-  kQFull = 1,        // + 2·half (half 0 also carries −LSE₂ and −D)
-  kQEmpty = 5,       // + 2·half
-  kDOFull = 9,       // + 2·half
-  kDOEmpty = 13,     // + 2·half
-  kSFull = 17,
-  kDPFull = 18,
-  kPdsFull = 19,
-  kDKVFull = 20,
-  kMmaDone = 21,
-  kNumBars = 22,
+  // Q and dO land and are released per half of the head dims (boxes 0-1,
+  // boxes 2-3): the MMA thread's waits and commits sit on its issue path (one
+  // per box measured 5 % slower on GB300).
+  kQFull = 1,        // + half (half 0 also carries −LSE₂ and −D)
+  kQEmpty = 3,       // + half
+  kDOFull = 5,       // + half
+  kDOEmpty = 7,      // + half
+  kSFull = 9,
+  kDPFull = 10,
+  kPdsFull = 11,
+  kDKVFull = 12,
+  kMmaDone = 13,
+  kNumBars = 14,
 };
 static_assert(8 * kNumBars + 8 <= 256, "barrier block too small");
 
@@ -187,11 +186,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kKVFull), 1);
-    for (int bx = 0; bx < 4; ++bx) {
-      mbar_init(bar(kQFull + bx), 1);
-      mbar_init(bar(kQEmpty + bx), 1);
-      mbar_init(bar(kDOFull + bx), 1);
-      mbar_init(bar(kDOEmpty + bx), 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar(kQFull + h), 1);
+      mbar_init(bar(kQEmpty + h), 1);
+      mbar_init(bar(kDOFull + h), 1);
+      mbar_init(bar(kDOEmpty + h), 1);
     }
     mbar_init(bar(kSFull), 1);
     mbar_init(bar(kDPFull), 1);
@@ -308,12 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
         // Q boxes free up first (dKᵀ is issued before dVᵀ), then dO boxes,
         // half by half of the head dims.
         for (int bx = 0; ok && bx < 4; ++bx) {
-          if (i > 0 && (bx & 1) == 0 && !mbar_wait(bar(kQEmpty + bx), (uint32_t)((i - 1) & 1), wc, site(5))) {
+          if (i > 0 && (bx & 1) == 0 && !mbar_wait(bar(kQEmpty + (bx >> 1)), (uint32_t)((i - 1) & 1), wc, site(5))) {
             ok = false;
             break;
           }
-          if ((bx & 1) == 0) mbar_arrive_expect_tx(bar(kQFull + bx), 2u * kQBox + (bx == 0 ? 2u * kBM * 4 : 0u));
-          load_rows(sbase + kQ + bx * kQBox, &a.tm_q, bar(kQFull + (bx & 2)), 64 * bx, q0, Nq);
+          if ((bx & 1) == 0) mbar_arrive_expect_tx(bar(kQFull + (bx >> 1)), 2u * kQBox + (bx == 0 ? 2u * kBM * 4 : 0u));
+          load_rows(sbase + kQ + bx * kQBox, &a.tm_q, bar(kQFull + (bx >> 1)), 64 * bx, q0, Nq);
           if (bx == 0) {
             load_bulk(sbase + kLSE, a.lse2 + wrow0 + q0, kBM * 4, bar(kQFull));
             load_bulk(sbase + kDV, a.dvec + wrow0 + q0, kBM * 4, bar(kQFull));
@@ -321,20 +320,20 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
           ++issued_q[bx];
         }
         for (int bx = 0; ok && bx < 4; ++bx) {
-          if (i > 0 && (bx & 1) == 0 && !mbar_wait(bar(kDOEmpty + bx), (uint32_t)((i - 1) & 1), wc, site(6))) {
+          if (i > 0 && (bx & 1) == 0 && !mbar_wait(bar(kDOEmpty + (bx >> 1)), (uint32_t)((i - 1) & 1), wc, site(6))) {
             ok = false;
             break;
           }
-          if ((bx & 1) == 0) mbar_arrive_expect_tx(bar(kDOFull + bx), 2u * kQBox);
-          load_rows(sbase + kDO + bx * kQBox, &a.tm_do, bar(kDOFull + (bx & 2)), 64 * bx, q0, Nq);
+          if ((bx & 1) == 0) mbar_arrive_expect_tx(bar(kDOFull + (bx >> 1)), 2u * kQBox);
+          load_rows(sbase + kDO + bx * kQBox, &a.tm_do, bar(kDOFull + (bx >> 1)), 64 * bx, q0, Nq);
           ++issued_do[bx];
         }
       }
       // Never leave the CTA with copies in flight.
       mbar_wait_drain(bar(kKVFull), 0, wc, site(7));
       for (int bx = 0; bx < 4; bx += 2) {
-        if (issued_q[bx] > 0) mbar_wait_drain(bar(kQFull + bx), (uint32_t)((issued_q[bx] - 1) & 1), wc, site(7));
-        if (issued_do[bx] > 0) mbar_wait_drain(bar(kDOFull + bx), (uint32_t)((issued_do[bx] - 1) & 1), wc, site(7));
+        if (issued_q[bx] > 0) mbar_wait_drain(bar(kQFull + (bx >> 1)), (uint32_t)((issued_q[bx] - 1) & 1), wc, site(7));
+        if (issued_do[bx] > 0) mbar_wait_drain(bar(kDOFull + (bx >> 1)), (uint32_t)((issued_do[bx] - 1) & 1), wc, site(7));
       }
     }
   } else {
@@ -351,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
                                     smem_ok(b_tile - sbase, 4 * kKBox, kBar, 1024), wc, kChkSmem, 54);
         for (int bx = 0; bx < 4; ++bx) {
           if ((bx & 1) == 0) {
-            if (!mbar_wait(bar(full + bx), (uint32_t)(i & 1), wc, site(8))) return false;
+            if (!mbar_wait(bar(full + (bx >> 1)), (uint32_t)(i & 1), wc, site(8))) return false;
             tc_fence_after();
           }
 #pragma unroll
@@ -388,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
           for (int ks = 0; ks < kBM / 16; ++ks)
             if (chk) mma_ss(tmem + kColDK + 64u * h, sdesc_add(q_mn, 2 * h * kQBox + ks * 2048), sdesc_add(ds_mn, ks * 2048),
                    kIdT, (i > 0 || ks > 0) ? 1u : 0u);
-          tc_commit(bar(kQEmpty + 2 * h));
+          tc_commit(bar(kQEmpty + h));
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -396,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_bwd_d256_dkdv_kernel(const __g
           for (int ks = 0; ks < kBM / 16; ++ks)
             if (chk) mma_ss(tmem + kColDV + 64u * h, sdesc_add(do_mn, 2 * h * kQBox + ks * 2048), sdesc_add(p_mn, ks * 2048),
                    kIdT, (i > 0 || ks > 0) ? 1u : 0u);
-          tc_commit(bar(kDOEmpty + 2 * h));
+          tc_commit(bar(kDOEmpty + h));
         }
         // The next tile's S and dP overwrite the columns the compute warps
         // have read; its P / dS stores wait for S, i.e. for these products.
@@ -439,10 +438,10 @@ static_assert(kBytes <= 232448, "shared memory exceeds the 227 KB a CTA may use"
 
 enum Bar : int {
   kQFull = 0,                    // Q, dO, −LSE₂, −D
-  kKFull = 1,                    // + tile of the ring (2; kKSlots reserved): its four boxes land together
-  kKEmpty = kKFull + kKSlots,    // + tile of the ring (2): its four boxes are released together
-  kVFull = kKEmpty + 2,          // the V tile (4 reserved)
-  kVEmpty = kVFull + 4,          // the V tile, released once dP has read all four boxes
+  kKFull = 1,                    // + tile of the ring (2): its four boxes land together
+  kKEmpty = kKFull + 2,          // + tile of the ring (2): its four boxes are released together
+  kVFull = kKEmpty + 2,          // the V tile
+  kVEmpty = kVFull + 1,          // the V tile, released once dP has read all four boxes
   kSFull = kVEmpty + 1,          // + buffer (2)
   kDPFull = kSFull + 2,          // + buffer
   kDsFull = kDPFull + 2,         // + buffer
